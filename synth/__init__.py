@@ -1,0 +1,288 @@
+"""Seeded synthetic inputs for the block-scaled GEMM + Amax.
+
+This module only draws random numbers and encodes them into the input
+formats the operation consumes (FP8/FP4 codes plus E8M0 block scales laid out
+in the 128-row scale atoms).  It holds none of the operation's own arithmetic:
+no decoding, no dot products, no reductions.  Both the CUDA path's tests and
+the CPU oracle are fed from here; neither of them is imported.
+
+Layouts produced (page "GEMM + Amax (SM100)", section "Parameters"):
+
+* ``A``: uint8, shape (L, M, K) -- k-major (M, K, L) with strides (K, 1, M*K);
+  (L, M, K/2) for packed E2M1, element 2i in the low nibble.
+* ``B``: uint8, shape (L, N, K) or (L, N, K/2), likewise.
+* ``SFA`` / ``SFB``: uint8, the C-contiguous physical scale tensor
+  (L, ceil(MN/128), ceil(K/(4*sfv)), 32, 4, 4), whose permutation by
+  (3, 4, 1, 5, 2, 0) is the logical (32, 4, ceil(MN/128), 4, ceil(K/(4*sfv)), L)
+  view ("Using JAX arrays").  Padding entries (rows past MN, K-blocks past
+  ceil(K/sfv)) hold 127 (a scale of 1).
+
+Workloads (seed = 1000 + workload number):
+
+1. E4M3 256x256x256, L=1: codes uniform over the 254 finite E4M3 bytes,
+   scale bytes uniform in [124, 130]; C fp32 n-major.
+2. MXFP8 4096^3, L=1: A, B ~ N(0,1), per-32 K-block E4M3 with scale
+   2^(floor(log2(block amax)) - 8); C bf16 n-major.
+3. Batched MXFP8 L=8, 2048x2048x8192: A ~ N(0,1) with ceil(1% of M) rows
+   per batch multiplied by 64 before quantising, A to E5M2, B to E4M3;
+   C fp32 n-major.
+4. FP4 E2M1 8192^3, L=1, sf_vec_size 16, scale 2^(floor(log2(block amax)) - 2);
+   C bf16 n-major.
+5. Ragged MXFP8 L=2, 8000x1000x7168: A ~ U[-1,1], B ~ N(0, 0.02), E4M3;
+   C fp32 m-major.
+
+The exponent offset of a block scale is the element format's largest
+exponent (E4M3 8, E5M2 15, E2M1 2); the scaled block is saturated to the
+format's largest finite value and rounded to nearest, ties to even.  A block
+whose amax is zero gets the scale byte 127.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+ELEM_EMAX = {"e4m3": 8, "e5m2": 15, "e2m1": 2}
+ELEM_MAX = {"e4m3": 448.0, "e5m2": 57344.0, "e2m1": 6.0}
+_E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float32)
+
+
+def _cdiv(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+@dataclasses.dataclass(frozen=True)
+class Problem:
+    M: int
+    N: int
+    K: int
+    L: int
+    a_dtype: str = "e4m3"
+    b_dtype: str = "e4m3"
+    sfv: int = 32
+    c_dtype: str = "f32"
+    c_major: str = "n"
+    sf_dtype: str = "ue8m0"
+
+    @property
+    def t_m(self) -> int:
+        return _cdiv(self.M, 128)
+
+    @property
+    def t_n(self) -> int:
+        return _cdiv(self.N, 128)
+
+    @property
+    def t_k(self) -> int:
+        return _cdiv(self.K, 4 * self.sfv)
+
+    def row_bytes(self, dtype: str) -> int:
+        return self.K // 2 if dtype == "e2m1" else self.K
+
+    @property
+    def c_itemsize(self) -> int:
+        return {"f32": 4, "f16": 2, "bf16": 2}[self.c_dtype]
+
+    def describe(self) -> str:
+        ab = self.a_dtype if self.a_dtype == self.b_dtype else f"{self.a_dtype}x{self.b_dtype}"
+        return (f"{ab} M={self.M} N={self.N} K={self.K} L={self.L} sfv={self.sfv} "
+                f"C={self.c_dtype} {self.c_major}-major")
+
+
+@dataclasses.dataclass
+class Inputs:
+    problem: Problem
+    A: np.ndarray
+    B: np.ndarray
+    SFA: np.ndarray
+    SFB: np.ndarray
+    name: str = ""
+
+
+WORKLOADS = {
+    1: ("e4m3-256^3-uniform-codes",
+        Problem(256, 256, 256, 1, "e4m3", "e4m3", 32, "f32", "n")),
+    2: ("mxfp8-4096^3-bf16",
+        Problem(4096, 4096, 4096, 1, "e4m3", "e4m3", 32, "bf16", "n")),
+    3: ("mxfp8-batched-L8-2048x2048x8192-e5m2xe4m3-outliers",
+        Problem(2048, 2048, 8192, 8, "e5m2", "e4m3", 32, "f32", "n")),
+    4: ("mxfp4-8192^3-sfv16-bf16",
+        Problem(8192, 8192, 8192, 1, "e2m1", "e2m1", 16, "bf16", "n")),
+    5: ("mxfp8-ragged-L2-8000x1000x7168-mmajor",
+        Problem(8000, 1000, 7168, 2, "e4m3", "e4m3", 32, "f32", "m")),
+}
+
+
+# ---------------------------------------------------------------- encoding
+
+def _encode_fp8(y: np.ndarray, dtype: str) -> np.ndarray:
+    """float32 values already inside the format's range -> FP8 bytes (RNE)."""
+    tdt = torch.float8_e4m3fn if dtype == "e4m3" else torch.float8_e5m2
+    return torch.from_numpy(np.ascontiguousarray(y, dtype=np.float32)).to(tdt).view(
+        torch.uint8).numpy()
+
+
+def _encode_e2m1(y: np.ndarray) -> np.ndarray:
+    """float32 values in [-6, 6] -> 4-bit E2M1 codes (one per uint8), RNE."""
+    a = np.abs(y).astype(np.float32)
+    i = np.searchsorted(_E2M1_GRID, a, side="right") - 1
+    i = np.clip(i, 0, 7)
+    j = np.minimum(i + 1, 7)
+    lo, hi = _E2M1_GRID[i], _E2M1_GRID[j]
+    d_lo, d_hi = a - lo, hi - a
+    up = (j != i) & ((d_hi < d_lo) | ((d_hi == d_lo) & (j % 2 == 0)))
+    code = np.where(up, j, i).astype(np.uint8)
+    code |= np.where(y < 0, np.uint8(8), np.uint8(0)).astype(np.uint8)
+    return code
+
+
+def _pack_e2m1(codes: np.ndarray) -> np.ndarray:
+    """(..., K) 4-bit codes -> (..., K/2) bytes, element 2i in the low nibble."""
+    lo = codes[..., 0::2]
+    hi = codes[..., 1::2]
+    return (lo | (hi << 4)).astype(np.uint8)
+
+
+def quantize_blocks(x: np.ndarray, dtype: str, sfv: int):
+    """x: (R, K) float32 with K % sfv == 0.  Returns (codes (R, K or K/2) uint8,
+    scale bytes (R, K/sfv) uint8)."""
+    R, K = x.shape
+    xb = x.reshape(R, K // sfv, sfv)
+    amax = np.max(np.abs(xb), axis=2)
+    _, e = np.frexp(amax)  # amax = f * 2^e, f in [0.5, 1) => floor(log2 amax) = e - 1
+    sf = (e.astype(np.int64) - 1) - ELEM_EMAX[dtype] + 127
+    sf = np.where(amax > 0, sf, 127)
+    sf = np.clip(sf, 1, 254).astype(np.uint8)
+    inv = np.ldexp(np.float32(1.0), (127 - sf.astype(np.int32))).astype(np.float32)
+    y = xb * inv[:, :, None]
+    m = ELEM_MAX[dtype]
+    y = np.clip(y, -m, m).reshape(R, K)
+    if dtype == "e2m1":
+        codes = _pack_e2m1(_encode_e2m1(y))
+    else:
+        codes = _encode_fp8(y, dtype)
+    return codes, sf
+
+
+def pack_scale_atoms(sf: np.ndarray, rows: int, K: int, sfv: int, pad: int = 127) -> np.ndarray:
+    """Logical scales (L, rows, ceil(K/sfv)) -> physical (L, T, T_k, 32, 4, 4) bytes.
+
+    Row r = 128*t + 32*m1 + m0 goes to [l, t, kt, m0, m1, kin] for K-block
+    kb = 4*kt + kin."""
+    L = sf.shape[0]
+    t, t_k = _cdiv(rows, 128), _cdiv(K, 4 * sfv)
+    full = np.full((L, t * 128, t_k * 4), pad, dtype=np.uint8)
+    full[:, :rows, :sf.shape[2]] = sf
+    x = full.reshape(L, t, 4, 32, t_k, 4)          # [l, t, m1, m0, kt, kin]
+    x = x.transpose(0, 1, 4, 3, 2, 5)               # [l, t, kt, m0, m1, kin]
+    return np.ascontiguousarray(x)
+
+
+def scale_shape(rows: int, K: int, sfv: int, L: int):
+    return (L, _cdiv(rows, 128), _cdiv(K, 4 * sfv), 32, 4, 4)
+
+
+# ---------------------------------------------------------------- workloads
+
+_FINITE_E4M3 = np.array([b for b in range(256) if b not in (0x7F, 0xFF)], dtype=np.uint8)
+
+
+def uniform_codes(p: Problem, seed: int, sf_lo: int = 124, sf_hi: int = 130) -> Inputs:
+    """Codes uniform over the finite codes of each format; every scale byte
+    (padding included) uniform in [sf_lo, sf_hi]."""
+    rng = np.random.default_rng(seed)
+
+    def codes(rows, dtype):
+        if dtype == "e4m3":
+            return _FINITE_E4M3[rng.integers(0, len(_FINITE_E4M3), size=(p.L, rows, p.K))]
+        if dtype == "e5m2":
+            fin = np.array([b for b in range(256) if (b & 0x7C) != 0x7C], dtype=np.uint8)
+            return fin[rng.integers(0, len(fin), size=(p.L, rows, p.K))]
+        c = rng.integers(0, 16, size=(p.L, rows, p.K)).astype(np.uint8)
+        return _pack_e2m1(c)
+
+    A = codes(p.M, p.a_dtype)
+    B = codes(p.N, p.b_dtype)
+    SFA = rng.integers(sf_lo, sf_hi + 1, size=scale_shape(p.M, p.K, p.sfv, p.L)).astype(np.uint8)
+    SFB = rng.integers(sf_lo, sf_hi + 1, size=scale_shape(p.N, p.K, p.sfv, p.L)).astype(np.uint8)
+    return Inputs(p, A, B, SFA, SFB)
+
+
+def quantized(p: Problem, seed: int, a_dist: str = "normal", b_dist: str = "normal",
+              b_sigma: float = 1.0, outlier_frac: float = 0.0, outlier_scale: float = 64.0
+              ) -> Inputs:
+    """Real-valued draws quantised per sf_vec_size K-block (see module doc)."""
+    if p.K % p.sfv:
+        raise ValueError("quantised workloads need K % sf_vec_size == 0")
+    rng = np.random.default_rng(seed)
+    a_bytes = p.row_bytes(p.a_dtype)
+    b_bytes = p.row_bytes(p.b_dtype)
+    A = np.empty((p.L, p.M, a_bytes), dtype=np.uint8)
+    B = np.empty((p.L, p.N, b_bytes), dtype=np.uint8)
+    sfa = np.empty((p.L, p.M, p.K // p.sfv), dtype=np.uint8)
+    sfb = np.empty((p.L, p.N, p.K // p.sfv), dtype=np.uint8)
+    for l in range(p.L):
+        if a_dist == "uniform":
+            x = rng.uniform(-1.0, 1.0, size=(p.M, p.K)).astype(np.float32)
+        else:
+            x = rng.standard_normal((p.M, p.K), dtype=np.float32)
+        if outlier_frac > 0:
+            n_out = int(math.ceil(outlier_frac * p.M))
+            rows = rng.choice(p.M, size=n_out, replace=False)
+            x[rows] *= np.float32(outlier_scale)
+        A[l], sfa[l] = quantize_blocks(x, p.a_dtype, p.sfv)
+    for l in range(p.L):
+        x = rng.standard_normal((p.N, p.K), dtype=np.float32)
+        if b_sigma != 1.0:
+            x *= np.float32(b_sigma)
+        B[l], sfb[l] = quantize_blocks(x, p.b_dtype, p.sfv)
+    SFA = pack_scale_atoms(sfa, p.M, p.K, p.sfv)
+    SFB = pack_scale_atoms(sfb, p.N, p.K, p.sfv)
+    return Inputs(p, A, B, SFA, SFB)
+
+
+def workload(number: int, **shape) -> Inputs:
+    """Inputs of workload `number` (1..5).  Keyword overrides (M, N, K, L)
+    keep the recipe and change the shape (parity cases at reduced size)."""
+    name, p = WORKLOADS[number]
+    if shape:
+        p = dataclasses.replace(p, **shape)
+    seed = 1000 + number
+    if number == 1:
+        inp = uniform_codes(p, seed)
+    elif number == 2:
+        inp = quantized(p, seed)
+    elif number == 3:
+        inp = quantized(p, seed, outlier_frac=0.01, outlier_scale=64.0)
+    elif number == 4:
+        inp = quantized(p, seed)
+    elif number == 5:
+        inp = quantized(p, seed, a_dist="uniform", b_sigma=0.02)
+    else:
+        raise KeyError(number)
+    inp.name = name if not shape else name + "@" + ",".join(f"{k}={v}" for k, v in shape.items())
+    return inp
+
+
+def c_shape(p: Problem):
+    """Memory shape of C: (L, M, N) for n-major, (L, N, M) for m-major."""
+    return (p.L, p.M, p.N) if p.c_major == "n" else (p.L, p.N, p.M)
+
+
+def sample_points(p: Problem, count: int, seed: int, extra=()) -> np.ndarray:
+    """`count` seeded (m, n, l) points, the four corners of every batch and
+    the last row/column (ragged tails) included, plus any `extra` points."""
+    rng = np.random.default_rng(seed)
+    pts = [rng.integers(0, p.M, count), rng.integers(0, p.N, count), rng.integers(0, p.L, count)]
+    pts = np.stack(pts, axis=1)
+    corners = []
+    for l in range(p.L):
+        for m in (0, p.M - 1):
+            for n in (0, p.N - 1):
+                corners.append((m, n, l))
+    allp = [pts, np.array(corners, dtype=np.int64).reshape(-1, 3)]
+    if len(extra):
+        allp.append(np.asarray(extra, dtype=np.int64).reshape(-1, 3))
+    return np.concatenate(allp, axis=0).astype(np.int64)
