@@ -1,0 +1,355 @@
+"""Benchmark of the block-scaled GEMM + Amax on GB300.
+
+One step = one launch of the whole hot path (operand/scale loads, block-scaled
+MMA, epilogue with the fused Amax) over one batch of seeded synthetic input
+of the chosen workload (default: MXFP8 4096^3, bf16 C).  Metric: TFLOP/s =
+2*M*N*K*L / kernel time (CUDA events on the launching stream), L2 flushed
+between steps.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+Under torchrun (N > 1) every rank runs its own replica of the workload on its
+own GPU (no data exchanged); rank 0 prints the max-over-ranks timing.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "block-scaled GEMM+amax TFLOP/s on 1 GB300; % of FP8/FP4 dense tensor peak"
+L2_FLUSH_BYTES = 512 << 20  # > 4x the 129 MB L2
+NOMINAL_RATIO = {"fp8": 4.5 / 2.25, "fp4": 13.5 / 2.25}  # dense tensor peak vs bf16
+FALLBACK_BF16_TFLOPS = 1900.0
+# DRAM bytes per launch of the GEMM kernel from an ncu capture, keyed by the
+# kernel source it was taken on (sha256 prefix of csrc/bsgemm.cu) and workload.
+TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    path = os.path.join(ROOT, "block_scaled_precision_04_gb300", "csrc", "bsgemm.cu")
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def workload_numbers(p: synth.Problem):
+    fp4 = p.a_dtype == "e2m1"
+    ab = lambda rows: p.L * rows * (p.K // 2 if fp4 else p.K)
+    sf = lambda rows: p.L * p.t_k * (-(-rows // 128)) * 512
+    c = p.L * p.M * p.N * p.c_itemsize
+    flops = 2.0 * p.M * p.N * p.K * p.L
+    return {"flops": flops, "bytes": ab(p.M) + ab(p.N) + sf(p.M) + sf(p.N) + c,
+            "h2d": ab(p.M) + ab(p.N) + sf(p.M) + sf(p.N), "d2h": c + 4,
+            "kind": "fp4" if fp4 else "fp8"}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, 6800.0, "fallback"
+
+
+def config_of(number: int, p: synth.Problem, name: str) -> dict:
+    return {"workload": name, "M": p.M, "N": p.N, "K": p.K, "L": p.L, "a_dtype": p.a_dtype,
+            "b_dtype": p.b_dtype, "sf_vec_size": p.sfv, "sf_dtype": p.sf_dtype,
+            "c_dtype": p.c_dtype, "c_major": p.c_major, "seed": 1000 + number,
+            "l2": "flushed between timed steps (512 MiB write)"}
+
+
+# ------------------------------------------------------------ CPU oracle leg
+
+def oracle_sample(inp, target_s: float, max_rows: int | None = None):
+    """Time the oracle (as it stands) on the first r rows of every batch, r
+    sized so the run takes about target_s seconds."""
+    import oracle
+    p = inp.problem
+    args = (p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv, inp.A, inp.B, inp.SFA, inp.SFB)
+    r = 2
+    t0 = time.perf_counter()
+    _, _, threads = oracle.gemm(*args, rows=(0, r), want_s=False)
+    t = time.perf_counter() - t0
+    rows = int(max(2, min(p.M, (target_s / max(t, 1e-3)) * r)))
+    if max_rows:
+        rows = min(rows, max_rows)
+    t0 = time.perf_counter()
+    _, _, threads = oracle.gemm(*args, rows=(0, rows), want_s=False)
+    t = time.perf_counter() - t0
+    flops = 2.0 * rows * p.N * p.K * p.L
+    return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of every batch (all N, all K): "
+                      f"{flops / 1e9:.1f} GFLOP in {t:.1f} s, double precision"}, rows, t
+
+
+# --------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [r.split(",") for r in f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- GPU leg
+
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import torch
+    import block_scaled_precision_04_gb300 as bsg
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    name, p = synth.WORKLOADS[args.workload]
+    inp = synth.workload(args.workload)
+    nums = workload_numbers(p)
+    op = bsg.GemmAmax(bsg.make_problem(p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv,
+                                       p.c_dtype, p.c_major), device=local_rank)
+    info = op.describe()
+    hA, hB, hSFA, hSFB = [torch.from_numpy(np.ascontiguousarray(x)) for x in
+                          (inp.A, inp.B, inp.SFA, inp.SFB)]
+    A, B, SFA, SFB = [t.to(dev) for t in (hA, hB, hSFA, hSFB)]
+    ctype = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[p.c_dtype]
+    C = torch.empty(synth.c_shape(p), dtype=ctype, device=dev)
+    amax = torch.zeros(1, dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    s = stream.cuda_stream
+
+    def launch():
+        bsg.check(bsg.bsg_run(op.plan, A.data_ptr(), B.data_ptr(), SFA.data_ptr(),
+                              SFB.data_ptr(), C.data_ptr(), amax.data_ptr(),
+                              op.workspace.data_ptr(), op.ws_bytes, s), "bsg_run")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        launch()
+    torch.cuda.synchronize(dev)
+    bsg.check(op.device_status(), "device status (warm-up)")
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        wall0 = time.perf_counter()
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record(stream)
+            launch()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+    if dist is not None:
+        dist.barrier()
+    bsg.check(op.device_status(), "device status")
+    times_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    total_ms = sum(times_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / args.steps
+    value = world * nums["flops"] * args.steps / (total_ms / 1e3) / 1e12
+
+    # end to end through the C ABI with host buffers (pinned), copies included
+    e2e = None
+    if not args.no_e2e:
+        pA, pB, pSFA, pSFB = [t.pin_memory() for t in (hA, hB, hSFA, hSFB)]
+        pC = torch.empty(synth.c_shape(p), dtype=ctype).pin_memory()
+        pamax = torch.empty(1, dtype=torch.float32).pin_memory()
+        bufs = bsg.bsg_device_buffers(A.data_ptr(), B.data_ptr(), SFA.data_ptr(), SFB.data_ptr(),
+                                      C.data_ptr(), amax.data_ptr(), op.workspace.data_ptr(),
+                                      op.ws_bytes)
+        run_host = lambda: bsg.check(bsg.bsg_run_host(
+            op.plan, pA.data_ptr(), pB.data_ptr(), pSFA.data_ptr(), pSFB.data_ptr(),
+            pC.data_ptr(), pamax.data_ptr(), bufs, s), "bsg_run_host")
+        for _ in range(max(1, args.warmup)):
+            run_host()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            run_host()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / args.steps
+        if dist is not None:
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * nums["flops"] / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": nums["h2d"],
+               "d2h_bytes_per_step": nums["d2h"]}
+
+    bf16, hbm, source = peaks()
+    peak = bf16 * NOMINAL_RATIO[nums["kind"]]
+    achieved = nums["flops"] / (ms / 1e3) / 1e12
+    traffic = TRAFFIC.get((kernel_source_hash(), args.workload))
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": f"{source} bf16 {bf16} TFLOP/s x nominal dense "
+                               f"{nums['kind']}/bf16 ratio {NOMINAL_RATIO[nums['kind']]:g}",
+                "kernel": info["kernel_name"],
+                "hbm_gbs_algorithmic": round(nums["bytes"] / (ms / 1e3) / 1e9, 1),
+                "hbm_frac_of_" + source: round(nums["bytes"] / (ms / 1e3) / 1e9 / hbm, 4)}
+
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": f"{p.a_dtype}x{p.b_dtype} codes, e8m0 scales, fp32 accumulate",
+            "data": "synthetic (seeded; see synth)", "config": config_of(args.workload, p, name),
+            "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps,
+            "clocks": clk.summary(), "wall_s_timed_region": round(wall, 4),
+            "plan": {k: info[k] for k in ("tile_m", "tile_n", "stages", "grid", "smem_bytes",
+                                          "num_tiles")},
+            "step_ms_min": round(min(times_ms), 5), "step_ms_median": round(statistics.median(times_ms), 5)}
+    if rank == 0 and not args.no_cpu:
+        cb, _, _ = oracle_sample(inp, args.cpu_seconds)
+        line["cpu_baseline"] = cb
+    elif rank == 0:
+        line["cpu_baseline"] = None
+    return line
+
+
+def run_reference(args):
+    """The CPU oracle, as it stands, on a bounded sample of the same workload
+    per step."""
+    name, p = synth.WORKLOADS[args.workload]
+    inp = synth.workload(args.workload)
+    nums = workload_numbers(p)
+    per_step = max(0.5, args.ref_seconds / max(1, args.steps + args.warmup))
+    _, rows, _ = oracle_sample(inp, per_step)
+    import oracle
+    pargs = (p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv, inp.A, inp.B, inp.SFA, inp.SFB)
+    for _ in range(args.warmup):
+        oracle.gemm(*pargs, rows=(0, rows), want_s=False)
+    t0 = time.perf_counter()
+    threads = 0
+    for _ in range(args.steps):
+        _, _, threads = oracle.gemm(*pargs, rows=(0, rows), want_s=False)
+    t = time.perf_counter() - t0
+    flops = 2.0 * rows * p.N * p.K * p.L
+    value = flops * args.steps / t / 1e12
+    sample = f"rows 0..{rows - 1} of every batch per step ({flops / 1e9:.1f} GFLOP, double)"
+    return {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": config_of(args.workload, p, name), "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0, "workload_flops_per_full_step": nums["flops"]}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3  # timing rule: at least three warm-up steps
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,907 @@
+// bsgemm.cu -- block-scaled (MX) batched GEMM + global Amax for sm_103a.
+//
+// Operation ("GEMM + Amax (SM100)", section "Equations"):
+//   C[m,n,l] = sum_k dec(A[m,k,l]) 2^(SFA[m,k/sfv,l]-127) * dec(B[n,k,l]) 2^(SFB[n,k/sfv,l]-127)
+//   Amax     = max |C|  (over the values as stored in C's dtype)
+//
+// Kernel design (one persistent CTA per SM, 6 warps):
+//   warp 0      TMA producer: per K stage, the 128 x 128-byte A tile and the
+//               TILE_N x 128-byte B tile (128-byte swizzle, 3-D tensor maps
+//               over (K bytes, rows, L), out-of-range rows/columns zero
+//               filled), plus the 512-byte scale atoms of those rows (bulk
+//               copies straight from the page's physical atom layout).
+//   warp 1      MMA issuer: copies the stage's scale atoms shared -> tensor
+//               memory (tcgen05.cp 32x128b.warpx4), then issues block-scaled
+//               tcgen05.mma (kind::mxf8f6f4 scale_vec::1X for FP8,
+//               kind::mxf4nvf4 scale_vec::4X / 2X for packed FP4) into a
+//               double-buffered fp32 accumulator in tensor memory; commits
+//               free the smem stage and publish a finished accumulator.
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (one row per thread),
+//               round to C's dtype, store, and keep max |stored value| as an
+//               integer max of the float bits; at exit one atomicMax per CTA.
+//   The last CTA to finish writes Amax and re-zeroes the workspace slots.
+//
+// Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
+// an error word in the workspace, stops its pipeline, drains in-flight
+// copies and MMAs, frees tensor memory and returns.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "bsgemm.h"
+
+namespace {
+
+constexpr int kTileM = 128;
+constexpr int kStageKBytes = 128;  // bytes of K per operand row per stage (one swizzle row)
+constexpr int kMmaKBytes = 32;     // bytes of K per tcgen05.mma (32 FP8 or 64 FP4 elements)
+constexpr int kThreads = 192;
+constexpr int kAtomBytes = 512;    // one scale atom: 128 rows x 4 K-blocks
+constexpr int kMaxChunks = 4;      // scale atoms along K per stage (FP4, sfv 16)
+constexpr int kNumAcc = 2;         // accumulator buffers in tensor memory
+constexpr uint32_t kTmemCols = 512;
+
+// error word bits (workspace word 2); word 3 keeps where the first wait gave up
+constexpr uint32_t kErrTimeout = 1u;
+
+enum MmaKind : int { kKindF8F6F4 = 0, kKindF4x4X = 1, kKindF4x2X = 2 };
+
+struct Params {
+  int M, N, K, L;
+  int tiles_m, tiles_n, num_tiles;
+  int k_bytes;            // bytes per operand row
+  int k_stages;           // ceil(k_bytes / 128)
+  int t_m, t_n, t_k;      // scale atoms: ceil(M/128), ceil(N/128), ceil(K/(4 sfv))
+  int chunks_per_stage;   // atoms along K per stage
+  int mmas_per_chunk;     // MMAs reading one atom column group
+  int sf_id_step;         // scale-byte step between those MMAs
+  int kind;
+  int tile_n;
+  int stages;
+  int c_dtype;            // bsg_dtype
+  int c_major;            // 0 = n-major, 1 = m-major
+  uint32_t idesc;         // instruction descriptor, scale ids zero
+  uint32_t smem_a, smem_b, smem_sfa, smem_sfb, smem_bar;  // offsets in dynamic smem
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  void* c;
+  float* amax;
+  uint32_t* ws;
+  unsigned long long wait_limit_ns;
+};
+
+// ------------------------------------------------------------------ PTX
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_mma(int kind, uint32_t d, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                       uint32_t accumulate) {
+  if (kind == kKindF8F6F4) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+        " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        : "memory");
+  } else if (kind == kKindF4x4X) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X"
+        " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        : "memory");
+  }
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base + i).
+__device__ __forceinline__ void tc_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%"
+      "14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, K-major operand tile with 128-byte
+// swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (unused here)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;                  // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                  // 128-byte swizzle
+  return d;
+}
+
+// Descriptor of one 512-byte scale atom as the source of a 32x128b copy:
+// 32 rows of 16 bytes, no swizzle, 8-row core matrices 128 bytes apart.
+__device__ __forceinline__ uint64_t desc_atom(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128 >> 4) << 16;
+  d |= static_cast<uint64_t>(128 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// ------------------------------------------------------------- helpers
+
+struct Tile {
+  int l, mt, nt;
+};
+
+__device__ __forceinline__ Tile tile_coords(const Params& p, int t) {
+  Tile r;
+  int per_batch = p.tiles_m * p.tiles_n;
+  r.l = t / per_batch;
+  int rem = t - r.l * per_batch;
+  r.mt = rem / p.tiles_n;
+  r.nt = rem - r.mt * p.tiles_n;
+  return r;
+}
+
+// Bounded wait.  Returns false when the pipeline is being abandoned.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Params& p,
+                                      volatile uint32_t* abort_flag, uint32_t where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long start = globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - start > p.wait_limit_ns) {
+      atomicOr(p.ws + 2, kErrTimeout);
+      atomicCAS(p.ws + 3, 0u, where);
+      *abort_flag = 1u;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t abs_bits_f32(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
+
+// --------------------------------------------------------------- kernel
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bsg_gemm_amax_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                         const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // align the dynamic window to 1024 bytes (128-byte swizzle atoms)
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* const smem = smem_raw + (base - raw_addr);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int S = p.stages;
+  const int G = p.tile_n / 128;  // 128-row scale groups of B per tile
+
+  const uint32_t bar0 = base + p.smem_bar;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * S + kNumAcc + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * S + 2 * kNumAcc);
+  uint32_t* const misc = reinterpret_cast<uint32_t*>(smem + p.smem_bar + 8u * (2 * S + 2 * kNumAcc + 1));
+  uint32_t* const tmem_holder = misc + 0;
+  volatile uint32_t* const abort_flag = misc + 1;
+  uint32_t* const cta_amax = misc + 2;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < kNumAcc; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), 4);  // one arrival per epilogue warp
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0u;
+    *cta_amax = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_holder)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t sfa_col = kNumAcc * p.tile_n;   // scale columns after the accumulators
+  const uint32_t sfb_col = sfa_col + 4 * kMaxChunks;
+
+  const uint32_t a_stage_bytes = kTileM * kStageKBytes;
+  const uint32_t b_stage_bytes = p.tile_n * kStageKBytes;
+  const uint32_t sfa_stage_bytes = kMaxChunks * kAtomBytes;
+  const uint32_t sfb_stage_bytes = kMaxChunks * kAtomBytes * G;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0;  // stages with a load issued (for the drain)
+      uint32_t armed_parity = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        const Tile tc = tile_coords(p, t);
+        for (int ks = 0; ks < p.k_stages; ++ks) {
+          if (!wait_bar(empty_bar(stage), phase ^ 1u, p, abort_flag, 1)) { ok = false; break; }
+          const int chunk0 = ks * p.chunks_per_stage;
+          int nch = p.t_k - chunk0;
+          if (nch > p.chunks_per_stage) nch = p.chunks_per_stage;
+          int groups = p.t_n - tc.nt * G;
+          if (groups > G) groups = G;
+          const uint32_t bytes = a_stage_bytes + b_stage_bytes +
+                                 static_cast<uint32_t>(nch) * kAtomBytes * (1u + groups);
+          mbar_arrive_expect_tx(full_bar(stage), bytes);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          tma_load_3d(base + p.smem_a + stage * a_stage_bytes, &tmap_a, ks * kStageKBytes,
+                      tc.mt * kTileM, tc.l, full_bar(stage));
+          tma_load_3d(base + p.smem_b + stage * b_stage_bytes, &tmap_b, ks * kStageKBytes,
+                      tc.nt * p.tile_n, tc.l, full_bar(stage));
+          const size_t a_atom = (static_cast<size_t>(tc.l) * p.t_m + tc.mt) * p.t_k + chunk0;
+          bulk_load(base + p.smem_sfa + stage * sfa_stage_bytes, p.sfa + a_atom * kAtomBytes,
+                    nch * kAtomBytes, full_bar(stage));
+          for (int g = 0; g < groups; ++g) {
+            const size_t b_atom =
+                (static_cast<size_t>(tc.l) * p.t_n + tc.nt * G + g) * p.t_k + chunk0;
+            bulk_load(base + p.smem_sfb + stage * sfb_stage_bytes + g * kMaxChunks * kAtomBytes,
+                      p.sfb + b_atom * kAtomBytes, nch * kAtomBytes, full_bar(stage));
+          }
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // drain: every issued load must have landed before the CTA may exit
+      for (int s = 0; s < S; ++s) {
+        if (armed & (1u << s)) {
+          const unsigned long long start = globaltimer();
+          while (!mbar_try_wait(full_bar(s), (armed_parity >> s) & 1u)) {
+            if (globaltimer() - start > p.wait_limit_ns) {
+              atomicOr(p.ws + 2, kErrTimeout);
+              atomicCAS(p.ws + 3, 0u, 10u);
+              break;
+            }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        const Tile tc = tile_coords(p, t);
+        int groups = p.t_n - tc.nt * G;
+        if (groups > G) groups = G;
+        if (!wait_bar(acce_bar(acc), acc_phase ^ 1u, p, abort_flag, 2)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * p.tile_n;
+        for (int ks = 0; ks < p.k_stages; ++ks) {
+          if (!wait_bar(full_bar(stage), phase, p, abort_flag, 3)) { ok = false; break; }
+          tc_fence_after();
+          const int chunk0 = ks * p.chunks_per_stage;
+          int nch = p.t_k - chunk0;
+          if (nch > p.chunks_per_stage) nch = p.chunks_per_stage;
+          const uint32_t sa = base + p.smem_sfa + stage * sfa_stage_bytes;
+          const uint32_t sb = base + p.smem_sfb + stage * sfb_stage_bytes;
+          for (int c = 0; c < nch; ++c) {
+            tc_cp_sf(tmem + sfa_col + 4 * c, desc_atom(sa + c * kAtomBytes));
+            for (int g = 0; g < groups; ++g)
+              tc_cp_sf(tmem + sfb_col + 4 * (c * G + g),
+                       desc_atom(sb + g * kMaxChunks * kAtomBytes + c * kAtomBytes));
+          }
+          int nmma = (p.k_bytes - ks * kStageKBytes + kMmaKBytes - 1) / kMmaKBytes;
+          if (nmma > kStageKBytes / kMmaKBytes) nmma = kStageKBytes / kMmaKBytes;
+          const uint32_t a_tile = base + p.smem_a + stage * a_stage_bytes;
+          const uint32_t b_tile = base + p.smem_b + stage * b_stage_bytes;
+          for (int j = 0; j < nmma; ++j) {
+            const int c = j / p.mmas_per_chunk;
+            const uint32_t sf_id = static_cast<uint32_t>((j % p.mmas_per_chunk) * p.sf_id_step);
+            const uint32_t idesc = p.idesc | (sf_id << 29) | (sf_id << 4);
+            tc_mma(p.kind, d_tmem, desc_sw128(a_tile + j * kMmaKBytes),
+                   desc_sw128(b_tile + j * kMmaKBytes), idesc, tmem + sfa_col + 4 * c,
+                   tmem + sfb_col + 4 * G * c, (ks > 0 || j > 0) ? 1u : 0u);
+          }
+          tc_commit(empty_bar(stage));  // frees the smem stage once these MMAs finish
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(accf_bar(acc));  // accumulator ready for the epilogue
+        if (++acc == kNumAcc) { acc = 0; acc_phase ^= 1u; }
+      }
+      // drain: all MMAs and copies issued by this thread complete before exit
+      tc_commit(drain_bar);
+      const unsigned long long start = globaltimer();
+      while (!mbar_try_wait(drain_bar, 0)) {
+        if (globaltimer() - start > p.wait_limit_ns) {
+          atomicOr(p.ws + 2, kErrTimeout);
+          atomicCAS(p.ws + 3, 0u, 11u);
+          break;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // tensor-memory lane quarter this warp may read
+    uint32_t vmax = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+      const Tile tc = tile_coords(p, t);
+      // one lane waits, the warp follows its verdict (tcgen05.ld is warp-collective)
+      int ready = 0;
+      if (lane == 0) ready = wait_bar(accf_bar(acc), acc_phase, p, abort_flag, 4) ? 1 : 0;
+      ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
+      if (!ready) break;
+      tc_fence_after();
+      const int row = tc.mt * kTileM + q * 32 + lane;
+      const bool row_ok = row < p.M;
+      const size_t batch_off = static_cast<size_t>(tc.l) * p.M * p.N;
+      for (int cc = 0; cc < p.tile_n; cc += 32) {
+        uint32_t r[32];
+        tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * p.tile_n + cc, r);
+        const int n0 = tc.nt * p.tile_n + cc;
+        if (p.c_major == 0) {
+          // n-major: this thread owns 32 consecutive elements of row `row`
+          if (p.c_dtype == BSG_F32) {
+            float* dst = static_cast<float*>(p.c) + batch_off + static_cast<size_t>(row) * p.N + n0;
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              if (row_ok && n0 + i < p.N) {
+                float4 v = make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                                       __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                vmax = max(vmax, max(max(abs_bits_f32(v.x), abs_bits_f32(v.y)),
+                                     max(abs_bits_f32(v.z), abs_bits_f32(v.w))));
+                *reinterpret_cast<float4*>(dst + i) = v;
+              }
+            }
+          } else {
+            uint16_t* dst = static_cast<uint16_t*>(p.c) + batch_off + static_cast<size_t>(row) * p.N + n0;
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              if (row_ok && n0 + i < p.N) {
+                uint32_t w[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const float f0 = __uint_as_float(r[i + 2 * j]);
+                  const float f1 = __uint_as_float(r[i + 2 * j + 1]);
+                  uint32_t h0, h1, b0, b1;
+                  if (p.c_dtype == BSG_BF16) {
+                    h0 = __bfloat16_as_ushort(__float2bfloat16_rn(f0));
+                    h1 = __bfloat16_as_ushort(__float2bfloat16_rn(f1));
+                    b0 = (h0 << 16) & 0x7FFFFFFFu;
+                    b1 = (h1 << 16) & 0x7FFFFFFFu;
+                  } else {
+                    const __half x0 = __float2half_rn(f0), x1 = __float2half_rn(f1);
+                    h0 = __half_as_ushort(x0);
+                    h1 = __half_as_ushort(x1);
+                    b0 = abs_bits_f32(__half2float(x0));
+                    b1 = abs_bits_f32(__half2float(x1));
+                  }
+                  vmax = max(vmax, max(b0, b1));
+                  w[j] = h0 | (h1 << 16);
+                }
+                *reinterpret_cast<uint4*>(dst + i) = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            }
+          }
+        } else {
+          // m-major: for each column the 32 lanes write 32 consecutive rows
+          const size_t colstride = static_cast<size_t>(p.M);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (row_ok && n0 + j < p.N) {
+              const size_t idx = batch_off + static_cast<size_t>(n0 + j) * colstride + row;
+              const float f = __uint_as_float(r[j]);
+              if (p.c_dtype == BSG_F32) {
+                static_cast<float*>(p.c)[idx] = f;
+                vmax = max(vmax, abs_bits_f32(f));
+              } else if (p.c_dtype == BSG_BF16) {
+                const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(f));
+                static_cast<uint16_t*>(p.c)[idx] = static_cast<uint16_t>(h);
+                vmax = max(vmax, (h << 16) & 0x7FFFFFFFu);
+              } else {
+                const __half x = __float2half_rn(f);
+                static_cast<uint16_t*>(p.c)[idx] = __half_as_ushort(x);
+                vmax = max(vmax, abs_bits_f32(__half2float(x)));
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar(acc));
+      if (++acc == kNumAcc) { acc = 0; acc_phase ^= 1u; }
+    }
+    vmax = __reduce_max_sync(0xFFFFFFFFu, vmax);
+    if (lane == 0) atomicMax(cta_amax, vmax);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+  if (threadIdx.x == 0) {
+    // global Amax: max over CTAs, written by the last CTA to arrive, which
+    // also re-zeroes the two workspace slots for the next run
+    atomicMax(p.ws + 0, *cta_amax);
+    __threadfence();
+    const uint32_t arrived = atomicAdd(p.ws + 1, 1u);
+    if (arrived == gridDim.x - 1) {
+      __threadfence();
+      const uint32_t bits = atomicExch(p.ws + 0, 0u);
+      *p.amax = __uint_as_float(bits);
+      atomicExch(p.ws + 1, 0u);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+constexpr size_t kWorkspaceBytes = 256;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int c_size(int d) { return d == BSG_F32 ? 4 : 2; }
+
+}  // namespace
+
+struct bsg_plan {
+  bsg_problem prob;
+  int device;
+  int sm_count;
+  Params base;           // everything but the pointers
+  int grid;
+  int smem_bytes;
+  // tensor maps for the last A/B pointers seen
+  std::mutex mu;
+  const void* map_a_ptr = nullptr;
+  const void* map_b_ptr = nullptr;
+  CUtensorMap map_a;
+  CUtensorMap map_b;
+};
+
+extern "C" {
+
+const char* bsg_status_string(bsg_status s) {
+  switch (s) {
+    case BSG_OK: return "ok";
+    case BSG_ERR_INVALID_ARG: return "invalid argument";
+    case BSG_ERR_UNSUPPORTED: return "unsupported combination";
+    case BSG_ERR_ALIGNMENT: return "misaligned pointer or row (16 bytes required)";
+    case BSG_ERR_ARCH: return "device is not sm_103 (compute capability 10.3)";
+    case BSG_ERR_WORKSPACE: return "workspace missing or too small";
+    case BSG_ERR_CUDA: return "CUDA call failed";
+    case BSG_ERR_DEVICE_TIMEOUT: return "a kernel pipeline wait timed out";
+  }
+  return "unknown status";
+}
+
+bsg_status bsg_problem_check(const bsg_problem* p) {
+  if (!p) return BSG_ERR_INVALID_ARG;
+  const int64_t lim = (int64_t(1) << 31) - 1;
+  if (p->M < 1 || p->N < 1 || p->K < 1 || p->L < 1) return BSG_ERR_INVALID_ARG;
+  if (p->M > lim || p->N > lim || p->K > lim || p->L > lim) return BSG_ERR_INVALID_ARG;
+  const int ops[2] = {p->a_dtype, p->b_dtype};
+  for (int d : ops)
+    if (d != BSG_E4M3 && d != BSG_E5M2 && d != BSG_E2M1) return BSG_ERR_INVALID_ARG;
+  if (p->sf_dtype == BSG_E4M3) return BSG_ERR_UNSUPPORTED;  // NVFP4-style scales
+  if (p->sf_dtype != BSG_UE8M0) return BSG_ERR_INVALID_ARG;
+  if (p->c_dtype == BSG_E4M3 || p->c_dtype == BSG_E5M2 || p->c_dtype == BSG_E2M1)
+    return BSG_ERR_UNSUPPORTED;  // low-precision C
+  if (p->c_dtype != BSG_F32 && p->c_dtype != BSG_F16 && p->c_dtype != BSG_BF16)
+    return BSG_ERR_INVALID_ARG;
+  if (p->sf_vec_size != 16 && p->sf_vec_size != 32) return BSG_ERR_INVALID_ARG;
+  const bool a4 = p->a_dtype == BSG_E2M1, b4 = p->b_dtype == BSG_E2M1;
+  if (a4 != b4) return BSG_ERR_UNSUPPORTED;                  // FP4 x FP8
+  if (!a4 && p->sf_vec_size == 16) return BSG_ERR_UNSUPPORTED;  // FP8 needs sfv 32
+  const char majors[2] = {p->a_major, p->b_major};
+  for (char mj : majors) {
+    if (mj == 'm' || mj == 'n') return BSG_ERR_UNSUPPORTED;  // MN-major operands
+    if (mj != 'k') return BSG_ERR_INVALID_ARG;
+  }
+  if (p->c_major != 'n' && p->c_major != 'm') return BSG_ERR_INVALID_ARG;
+  if (p->tile_m != 0 && p->tile_m != 128) return BSG_ERR_INVALID_ARG;
+  if (p->tile_n != 0 && p->tile_n != 128 && p->tile_n != 256) return BSG_ERR_INVALID_ARG;
+  const int cl[2] = {p->cluster_m, p->cluster_n};
+  for (int c : cl)
+    if (c != 0 && c != 1 && c != 2 && c != 4) return BSG_ERR_INVALID_ARG;
+  const int64_t row_bytes = a4 ? p->K / 2 : p->K;
+  if (a4 && (p->K % 2)) return BSG_ERR_ALIGNMENT;
+  if (row_bytes % 16) return BSG_ERR_ALIGNMENT;
+  const int64_t c_row = (p->c_major == 'n' ? p->N : p->M) * c_size(p->c_dtype);
+  if (c_row % 16) return BSG_ERR_ALIGNMENT;
+  return BSG_OK;
+}
+
+bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) {
+  if (!out) return BSG_ERR_INVALID_ARG;
+  const bsg_status st = bsg_problem_check(prob);
+  if (st != BSG_OK) return st;
+  int major = 0, minor = 0, sms = 0, max_smem = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return BSG_ERR_CUDA;
+  }
+  if (major != 10 || minor != 3) return BSG_ERR_ARCH;
+  if (!get_encode_fn()) return BSG_ERR_CUDA;
+
+  bsg_plan* plan = new (std::nothrow) bsg_plan();
+  if (!plan) return BSG_ERR_INVALID_ARG;
+  plan->prob = *prob;
+  plan->device = device;
+  plan->sm_count = sms;
+
+  Params& k = plan->base;
+  std::memset(&k, 0, sizeof(k));
+  const bool fp4 = prob->a_dtype == BSG_E2M1;
+  const int sfv = prob->sf_vec_size;
+  k.M = static_cast<int>(prob->M);
+  k.N = static_cast<int>(prob->N);
+  k.K = static_cast<int>(prob->K);
+  k.L = static_cast<int>(prob->L);
+  k.tile_n = 128;
+  k.tiles_m = static_cast<int>(cdiv(prob->M, kTileM));
+  k.tiles_n = static_cast<int>(cdiv(prob->N, k.tile_n));
+  k.num_tiles = k.tiles_m * k.tiles_n * k.L;
+  k.k_bytes = static_cast<int>(fp4 ? prob->K / 2 : prob->K);
+  k.k_stages = static_cast<int>(cdiv(k.k_bytes, kStageKBytes));
+  k.t_m = static_cast<int>(cdiv(prob->M, 128));
+  k.t_n = static_cast<int>(cdiv(prob->N, 128));
+  k.t_k = static_cast<int>(cdiv(prob->K, 4 * sfv));
+  // elements of K per stage: 128 (FP8) or 256 (FP4); one atom spans 4*sfv
+  const int k_elems_stage = fp4 ? 2 * kStageKBytes : kStageKBytes;
+  k.chunks_per_stage = k_elems_stage / (4 * sfv);
+  const int k_elems_mma = fp4 ? 2 * kMmaKBytes : kMmaKBytes;
+  if (!fp4) {
+    k.kind = kKindF8F6F4;  // one scale (block 32) per MMA: byte j of the column
+    k.mmas_per_chunk = 4;
+    k.sf_id_step = 1;
+  } else if (sfv == 16) {
+    k.kind = kKindF4x4X;   // four block-16 scales per MMA: the whole column
+    k.mmas_per_chunk = 1;
+    k.sf_id_step = 0;
+  } else {
+    k.kind = kKindF4x2X;   // two block-32 scales per MMA: bytes 0-1 or 2-3
+    k.mmas_per_chunk = 2;
+    k.sf_id_step = 2;
+  }
+  (void)k_elems_mma;
+  uint32_t a_fmt, b_fmt;
+  if (fp4) {
+    a_fmt = b_fmt = 1;  // E2M1 in kind::mxf4nvf4
+  } else {
+    a_fmt = prob->a_dtype == BSG_E5M2 ? 1 : 0;  // kind::mxf8f6f4: E4M3 0, E5M2 1
+    b_fmt = prob->b_dtype == BSG_E5M2 ? 1 : 0;
+  }
+  k.idesc = (a_fmt << 7) | (b_fmt << 10) | (static_cast<uint32_t>(k.tile_n >> 3) << 17) |
+            (1u << 23) /* E8M0 scales */ | (static_cast<uint32_t>(kTileM >> 4) << 24);
+  k.c_dtype = prob->c_dtype;
+  k.c_major = prob->c_major == 'm' ? 1 : 0;
+
+  const int G = k.tile_n / 128;
+  const int per_stage = kTileM * kStageKBytes + k.tile_n * kStageKBytes +
+                        kMaxChunks * kAtomBytes * (1 + G);
+  const int reserve = 1024 /* alignment slack */ + 512 /* barriers and flags */;
+  int stages = (max_smem - reserve) / per_stage;
+  if (stages > 8) stages = 8;
+  if (stages < 2) { delete plan; return BSG_ERR_UNSUPPORTED; }
+  k.stages = stages;
+  k.smem_a = 0;
+  k.smem_b = k.smem_a + stages * kTileM * kStageKBytes;
+  k.smem_sfa = k.smem_b + stages * k.tile_n * kStageKBytes;
+  k.smem_sfb = k.smem_sfa + stages * kMaxChunks * kAtomBytes;
+  k.smem_bar = k.smem_sfb + stages * kMaxChunks * kAtomBytes * G;
+  plan->smem_bytes = static_cast<int>(k.smem_bar) + 8 * (2 * stages + 2 * kNumAcc + 1) + 16 + 1024;
+  k.wait_limit_ns = 1000000000ull;  // one second per wait
+  if (const char* e = std::getenv("BSG_WAIT_LIMIT_NS")) {
+    const unsigned long long v = std::strtoull(e, nullptr, 10);
+    if (v > 0) k.wait_limit_ns = v;
+  }
+  plan->grid = k.num_tiles < sms ? k.num_tiles : sms;
+
+  int prev = 0;
+  cudaGetDevice(&prev);
+  if (prev != device) cudaSetDevice(device);
+  const cudaError_t e = cudaFuncSetAttribute(bsg_gemm_amax_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             plan->smem_bytes);
+  if (prev != device) cudaSetDevice(prev);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    delete plan;
+    return BSG_ERR_CUDA;
+  }
+  if (std::getenv("BSG_LOG"))
+    std::fprintf(stderr,
+                 "[bsgemm] M=%lld N=%lld K=%lld L=%lld tile=128x%d stages=%d grid=%d smem=%d "
+                 "kind=%d tiles=%d\n",
+                 (long long)prob->M, (long long)prob->N, (long long)prob->K, (long long)prob->L,
+                 k.tile_n, stages, plan->grid, plan->smem_bytes, k.kind, k.num_tiles);
+  *out = plan;
+  return BSG_OK;
+}
+
+bsg_status bsg_plan_workspace_size(const bsg_plan* plan, size_t* bytes) {
+  if (!plan || !bytes) return BSG_ERR_INVALID_ARG;
+  *bytes = kWorkspaceBytes;
+  return BSG_OK;
+}
+
+bsg_status bsg_workspace_init(const bsg_plan* plan, void* ws, size_t ws_bytes, void* stream) {
+  if (!plan || !ws) return BSG_ERR_INVALID_ARG;
+  if (ws_bytes < kWorkspaceBytes) return BSG_ERR_WORKSPACE;
+  if (cudaMemsetAsync(ws, 0, kWorkspaceBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return BSG_ERR_CUDA;
+  }
+  return BSG_OK;
+}
+
+static bool encode_operand(CUtensorMap* map, const void* ptr, int64_t row_bytes, int64_t rows,
+                           int64_t L, int box_rows) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(L)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes),
+                           static_cast<cuuint64_t>(row_bytes * rows)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kStageKBytes), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = get_encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr),
+                                     dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const void* SFA,
+                   const void* SFB, void* C, float* amax, void* ws, size_t ws_bytes,
+                   void* stream) {
+  if (!cplan || !A || !B || !SFA || !SFB || !C || !amax) return BSG_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < kWorkspaceBytes || !aligned16(ws)) return BSG_ERR_WORKSPACE;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(SFA) || !aligned16(SFB) || !aligned16(C) ||
+      (reinterpret_cast<uintptr_t>(amax) & 3u))
+    return BSG_ERR_ALIGNMENT;
+  bsg_plan* plan = const_cast<bsg_plan*>(cplan);
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return BSG_ERR_CUDA; }
+  if (dev != plan->device) return BSG_ERR_INVALID_ARG;
+  const bsg_problem& pr = plan->prob;
+  const int64_t row_bytes = plan->base.k_bytes;
+  Params k = plan->base;
+  k.sfa = static_cast<const uint8_t*>(SFA);
+  k.sfb = static_cast<const uint8_t*>(SFB);
+  k.c = C;
+  k.amax = amax;
+  k.ws = static_cast<uint32_t*>(ws);
+  CUtensorMap ma, mb;
+  {
+    std::lock_guard<std::mutex> lock(plan->mu);
+    if (plan->map_a_ptr != A) {
+      if (!encode_operand(&plan->map_a, A, row_bytes, pr.M, pr.L, kTileM)) {
+        plan->map_a_ptr = nullptr;
+        return BSG_ERR_CUDA;
+      }
+      plan->map_a_ptr = A;
+    }
+    if (plan->map_b_ptr != B) {
+      if (!encode_operand(&plan->map_b, B, row_bytes, pr.N, pr.L, k.tile_n)) {
+        plan->map_b_ptr = nullptr;
+        return BSG_ERR_CUDA;
+      }
+      plan->map_b_ptr = B;
+    }
+    ma = plan->map_a;
+    mb = plan->map_b;
+  }
+  bsg_gemm_amax_kernel<<<plan->grid, kThreads, plan->smem_bytes,
+                         static_cast<cudaStream_t>(stream)>>>(ma, mb, k);
+  if (cudaGetLastError() != cudaSuccess) return BSG_ERR_CUDA;
+  return BSG_OK;
+}
+
+bsg_status bsg_run_host(const bsg_plan* plan, const void* hA, const void* hB, const void* hSFA,
+                        const void* hSFB, void* hC, float* h_amax, const bsg_device_buffers* dev,
+                        void* stream) {
+  if (!plan || !hA || !hB || !hSFA || !hSFB || !hC || !h_amax || !dev) return BSG_ERR_INVALID_ARG;
+  const bsg_problem& p = plan->prob;
+  const bool fp4 = p.a_dtype == BSG_E2M1;
+  const size_t a_bytes = static_cast<size_t>(p.L * p.M) * (fp4 ? p.K / 2 : p.K);
+  const size_t b_bytes = static_cast<size_t>(p.L * p.N) * (fp4 ? p.K / 2 : p.K);
+  const size_t sfa_bytes = static_cast<size_t>(p.L * plan->base.t_m * plan->base.t_k) * kAtomBytes;
+  const size_t sfb_bytes = static_cast<size_t>(p.L * plan->base.t_n * plan->base.t_k) * kAtomBytes;
+  const size_t c_bytes = static_cast<size_t>(p.L * p.M * p.N) * c_size(p.c_dtype);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!dev->A || !dev->B || !dev->SFA || !dev->SFB || !dev->C || !dev->amax)
+    return BSG_ERR_INVALID_ARG;
+  if (cudaMemcpyAsync(dev->A, hA, a_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(dev->B, hB, b_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(dev->SFA, hSFA, sfa_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(dev->SFB, hSFB, sfb_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    cudaGetLastError();
+    return BSG_ERR_CUDA;
+  }
+  const bsg_status st = bsg_run(plan, dev->A, dev->B, dev->SFA, dev->SFB, dev->C, dev->amax,
+                                dev->workspace, dev->ws_bytes, stream);
+  if (st != BSG_OK) return st;
+  if (cudaMemcpyAsync(hC, dev->C, c_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(h_amax, dev->amax, sizeof(float), cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+    cudaGetLastError();
+    return BSG_ERR_CUDA;
+  }
+  return BSG_OK;
+}
+
+bsg_status bsg_check_device_status(const bsg_plan* plan, void* ws, void* stream) {
+  if (!plan || !ws) return BSG_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t words[2] = {0, 0};
+  if (cudaStreamSynchronize(s) != cudaSuccess ||
+      cudaMemcpy(words, static_cast<uint8_t*>(ws) + 8, sizeof(words), cudaMemcpyDeviceToHost) !=
+          cudaSuccess ||
+      cudaMemset(static_cast<uint8_t*>(ws) + 8, 0, sizeof(words)) != cudaSuccess) {
+    cudaGetLastError();
+    return BSG_ERR_CUDA;
+  }
+  if (words[0] & kErrTimeout) {
+    if (std::getenv("BSG_LOG"))
+      std::fprintf(stderr, "[bsgemm] device wait timed out (site %u)\n", words[1]);
+    return BSG_ERR_DEVICE_TIMEOUT;
+  }
+  return BSG_OK;
+}
+
+bsg_status bsg_plan_describe(const bsg_plan* plan, bsg_plan_info* info) {
+  if (!plan || !info) return BSG_ERR_INVALID_ARG;
+  std::memset(info, 0, sizeof(*info));
+  info->tile_m = kTileM;
+  info->tile_n = plan->base.tile_n;
+  info->tile_k_bytes = kStageKBytes;
+  info->stages = plan->base.stages;
+  info->grid = plan->grid;
+  info->threads = kThreads;
+  info->smem_bytes = plan->smem_bytes;
+  info->num_tiles = plan->base.num_tiles;
+  info->mma_kind = plan->base.kind;
+  std::snprintf(info->kernel_name, sizeof(info->kernel_name), "bsg_gemm_amax_kernel");
+  return BSG_OK;
+}
+
+void bsg_plan_destroy(bsg_plan* plan) { delete plan; }
+
+}  // extern "C"

@@ -1,0 +1,172 @@
+/*
+ * bsgemm.h -- C ABI of the block-scaled GEMM + Amax library (libbsgemm.so).
+ *
+ * Operation ("GEMM + Amax (SM100)", section "Equations"):
+ *
+ *     Ahat[m,k,l] = dec(A[m,k,l]) * 2^(SFA[m, k/sf_vec_size, l] - 127)
+ *     Bhat[n,k,l] = dec(B[n,k,l]) * 2^(SFB[n, k/sf_vec_size, l] - 127)
+ *     C[m,n,l]    = sum_k Ahat[m,k,l] * Bhat[n,k,l]      (fp32 accumulation)
+ *     Amax        = max_{m,n,l} |C[m,n,l]|               (of the stored C)
+ *
+ * Tensors ("Parameters", "Input/Output tensors"; all device memory of one
+ * GPU, "Environment": all tensors on the same device):
+ *
+ *   A    (M, K, L), k-major: strides (K, 1, M*K) in elements.  FP8 codes one
+ *        per byte; packed FP4 (E2M1) two per byte, element 2i in the low
+ *        nibble, so a row holds K/2 bytes ("Layouts and strides").
+ *   B    (N, K, L), k-major, same element type rules as A.
+ *   SFA  E8M0 bytes, physical C-contiguous (L, ceil(M/128), ceil(K/(4*sfv)),
+ *        32, 4, 4), which is the page's logical (32, 4, ceil(M/128), 4,
+ *        ceil(K/(4*sfv)), L) view permuted ("Using JAX arrays").  Row
+ *        m = 128*mt + 32*m1 + m0 and K-block kb = 4*kt + kin sit at byte
+ *        ((l*T_m + mt)*T_k + kt)*512 + m0*16 + m1*4 + kin.
+ *   SFB  the same for the N rows of B.
+ *   C    (M, N, L), fp32 / fp16 / bf16, n-major strides (N, 1, M*N) or
+ *        m-major strides (1, M, M*N).
+ *   Amax one fp32 (shape (1,1,1)); overwritten by every run, not accumulated.
+ *
+ * Padding entries of SFA/SFB (rows past M or N, K-blocks past
+ * ceil(K/sfv)) multiply zero codes or rows that are never stored; they must
+ * hold a finite scale (any byte but 0xFF) so that 0 * scale stays 0.
+ *
+ * Support ("Support surface and constraints"): A/B k-major; A/B both FP8
+ * (E4M3/E5M2, each on its own) with sf_vec_size 32, or both E2M1 with
+ * sf_vec_size 16 or 32; E8M0 scales; C fp32/fp16/bf16.  Rows of A, B and C
+ * must be 16-byte aligned along their contiguous dimension, every pointer
+ * 16-byte aligned.  Everything else returns BSG_ERR_UNSUPPORTED or
+ * BSG_ERR_INVALID_ARG before any launch (errors are reported before launch,
+ * as "Grouped GEMM (SM100 BF16)", "Scheduling, caching, and errors", does).
+ *
+ * Ownership: the caller owns every device buffer (A, B, SFA, SFB, C, Amax,
+ * workspace).  A plan owns host memory only.  No entry point allocates
+ * device memory.  bsg_run is asynchronous on the given stream and never
+ * synchronises.  No exception or abort crosses this boundary.
+ */
+#ifndef BSGEMM_H
+#define BSGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BSG_OK = 0,
+    BSG_ERR_INVALID_ARG = 1,    /* null pointer, non-positive size, bad enum, bad hint */
+    BSG_ERR_UNSUPPORTED = 2,    /* a combination outside the support surface */
+    BSG_ERR_ALIGNMENT = 3,      /* a pointer or a contiguous row not 16-byte aligned */
+    BSG_ERR_ARCH = 4,           /* device is not compute capability 10.3 (sm_103a) */
+    BSG_ERR_WORKSPACE = 5,      /* workspace missing or smaller than required */
+    BSG_ERR_CUDA = 6,           /* a CUDA runtime/driver call failed */
+    BSG_ERR_DEVICE_TIMEOUT = 7  /* a pipeline wait in the kernel ran out of time */
+} bsg_status;
+
+typedef enum {
+    BSG_E4M3 = 0,   /* float8_e4m3fn codes (A/B) */
+    BSG_E5M2 = 1,   /* float8_e5m2 codes (A/B) */
+    BSG_E2M1 = 2,   /* float4_e2m1fn, packed two per byte (A/B) */
+    BSG_UE8M0 = 3,  /* float8_e8m0fnu scale bytes (SFA/SFB) */
+    BSG_F32 = 4,    /* C */
+    BSG_F16 = 5,    /* C */
+    BSG_BF16 = 6    /* C */
+} bsg_dtype;
+
+/* Problem statement, after the page's constructor arguments ("Common
+ * parameters", "Class-specific parameters").  tile_* and cluster_* are
+ * hints only: 0 lets the library choose; otherwise tile_m must be 128,
+ * tile_n 128 or 256, cluster_* 1, 2 or 4. */
+typedef struct {
+    int64_t M, N, K, L;
+    int32_t a_dtype, b_dtype;   /* bsg_dtype */
+    int32_t sf_dtype;           /* BSG_UE8M0 */
+    int32_t c_dtype;            /* BSG_F32, BSG_F16 or BSG_BF16 */
+    char a_major, b_major;      /* 'k' */
+    char c_major;               /* 'n' or 'm' */
+    char reserved0;
+    int32_t sf_vec_size;        /* 16 or 32 */
+    int32_t tile_m, tile_n;
+    int32_t cluster_m, cluster_n;
+} bsg_problem;
+
+typedef struct bsg_plan bsg_plan;
+
+/* What a plan chose (for logging and the benchmark). */
+typedef struct {
+    int32_t tile_m, tile_n, tile_k_bytes;  /* CTA tile; K bytes per pipeline stage */
+    int32_t stages;                        /* shared-memory pipeline depth */
+    int32_t grid;                          /* persistent CTAs per launch */
+    int32_t threads;                       /* threads per CTA */
+    int32_t smem_bytes;                    /* dynamic shared memory per CTA */
+    int32_t num_tiles;                     /* output tiles per launch */
+    int32_t mma_kind;                      /* 0 mxf8f6f4 1X, 1 mxf4nvf4 4X, 2 mxf4nvf4 2X */
+    int32_t reserved;
+    char kernel_name[64];
+} bsg_plan_info;
+
+/* Host-only validation of a problem against the support surface; touches
+ * no device.  Returns BSG_OK or the first violated rule. */
+bsg_status bsg_problem_check(const bsg_problem *problem);
+
+/* Validate, pick the kernel, tile and pipeline for `device`, and record
+ * them in a new plan (the analogue of check_support() + compile() of the
+ * page's class API, "Class API").  Fails with BSG_ERR_ARCH unless the device
+ * is sm_103.  *out is set only on BSG_OK. */
+bsg_status bsg_plan_create(const bsg_problem *problem, int device, bsg_plan **out);
+
+/* Bytes of device workspace a run of this plan needs (a small fixed
+ * amount: a cross-CTA amax slot, an arrival counter and an error word). */
+bsg_status bsg_plan_workspace_size(const bsg_plan *plan, size_t *bytes);
+
+/* Zero a workspace on `stream` (cudaMemsetAsync).  Must be called once
+ * before a workspace is first used; every run leaves it zeroed again. */
+bsg_status bsg_workspace_init(const bsg_plan *plan, void *workspace, size_t ws_bytes,
+                              void *stream);
+
+/* One launch of the GEMM + Amax on `stream` (a cudaStream_t; NULL is the
+ * legacy default stream) -- the analogue of execute() ("Class API").
+ * A, B, SFA, SFB, C, amax and workspace are device pointers of the plan's
+ * device.  Checks pointers, alignment and the workspace size, then launches
+ * exactly one kernel.  Allocates nothing, never synchronises.  Runs sharing
+ * one workspace must not overlap on the device. */
+bsg_status bsg_run(const bsg_plan *plan, const void *A, const void *B, const void *SFA,
+                   const void *SFB, void *C, float *amax, void *workspace, size_t ws_bytes,
+                   void *stream);
+
+/* Device buffers for bsg_run_host: caller-allocated, sized for the plan. */
+typedef struct {
+    void *A, *B, *SFA, *SFB, *C;
+    float *amax;
+    void *workspace;
+    size_t ws_bytes;
+} bsg_device_buffers;
+
+/* End-to-end form of bsg_run over HOST buffers (preferably pinned): copies
+ * hA, hB, hSFA, hSFB to the device buffers, runs, and copies C and Amax back
+ * to hC and h_amax, all enqueued on `stream` (one cudaMemcpyAsync per
+ * tensor).  Asynchronous like bsg_run: synchronise the stream before reading
+ * hC or *h_amax. */
+bsg_status bsg_run_host(const bsg_plan *plan, const void *hA, const void *hB, const void *hSFA,
+                        const void *hSFB, void *hC, float *h_amax,
+                        const bsg_device_buffers *dev, void *stream);
+
+/* Synchronise `stream`, then read and clear the workspace's device error
+ * word.  Returns BSG_ERR_DEVICE_TIMEOUT if a kernel of an earlier run gave
+ * up on a pipeline wait (its outputs are then invalid), else BSG_OK. */
+bsg_status bsg_check_device_status(const bsg_plan *plan, void *workspace, void *stream);
+
+/* Fill *info with the plan's choices. */
+bsg_status bsg_plan_describe(const bsg_plan *plan, bsg_plan_info *info);
+
+/* Free a plan (host memory only).  NULL is ignored. */
+void bsg_plan_destroy(bsg_plan *plan);
+
+/* Static text for a status code. */
+const char *bsg_status_string(bsg_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSGEMM_H */

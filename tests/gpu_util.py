@@ -1,0 +1,82 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C
+ABI on synth inputs and compare with the oracle."""
+import numpy as np
+import torch
+
+import block_scaled_precision_04_gb300 as bsg
+import oracle
+import synth
+
+TORCH_C = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+
+
+def problem_of(p: synth.Problem, **hints) -> bsg.bsg_problem:
+    return bsg.make_problem(p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv, p.c_dtype,
+                            p.c_major, **hints)
+
+
+def to_device(inp: synth.Inputs, dev="cuda:0"):
+    return [torch.from_numpy(np.ascontiguousarray(x)).to(dev) for x in
+            (inp.A, inp.B, inp.SFA, inp.SFB)]
+
+
+def c_to_logical(c: torch.Tensor, p: synth.Problem) -> np.ndarray:
+    """Device C in its memory layout -> float64 numpy (L, M, N)."""
+    x = c.float().cpu().numpy().astype(np.float64)
+    return x if p.c_major == "n" else x.transpose(0, 2, 1)
+
+
+def run_gpu(inp: synth.Inputs, op=None, runs=1, guard=0, **hints):
+    """Launch `runs` times; returns (C logical float64, amax, raw C tensor, op, guard ok)."""
+    p = inp.problem
+    if op is None:
+        op = bsg.GemmAmax(problem_of(p, **hints))
+    A, B, SFA, SFB = to_device(inp)
+    numel = p.L * p.M * p.N
+    poison = float("nan")
+    buf = torch.full((numel + 2 * guard,), poison, dtype=TORCH_C[p.c_dtype], device="cuda:0")
+    C = buf[guard:guard + numel].view(synth.c_shape(p))
+    amax = torch.full((1,), -1.0, dtype=torch.float32, device="cuda:0")
+    for _ in range(runs):
+        op.run(A, B, SFA, SFB, C, amax)
+    torch.cuda.synchronize()
+    st = op.device_status()
+    assert st == bsg.BSG_OK, bsg.bsg_status_string(st)
+    guard_ok = True
+    if guard:
+        g = torch.cat([buf[:guard], buf[guard + numel:]])
+        guard_ok = bool(torch.isnan(g.float()).all())
+    return c_to_logical(C, p), float(amax.item()), C, op, guard_ok
+
+
+def abs_max_bits(c: np.ndarray) -> int:
+    """max |c| as float32 bit pattern (integer max, as the kernel keeps it)."""
+    u = np.abs(c.astype(np.float32)).view(np.uint32)
+    return int(u.max()) if u.size else 0
+
+
+def assert_parity(inp: synth.Inputs, c_gpu: np.ndarray, amax_gpu: float, ref=None):
+    """Elementwise |C_gpu - C_ref| <= 1e-5 * S + ulp_c(|C_ref|); Amax equal
+    (bit for bit) to max |C_gpu| and within max tau of the oracle's Amax."""
+    p = inp.problem
+    if ref is None:
+        ref = oracle.reference(p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv, inp.A, inp.B,
+                               inp.SFA, inp.SFB, p.c_dtype)
+    finite = np.isfinite(ref["c"])
+    with np.errstate(invalid="ignore"):
+        err = np.abs(c_gpu - ref["c"])
+    # where the oracle's rounded value overflows C's dtype, the stored value
+    # must be that same infinity
+    bad = np.where(finite, ~(err <= ref["tau"]), c_gpu != ref["c"])
+    if bad.any():
+        idx = np.argwhere(bad)[:8]
+        detail = [(tuple(int(v) for v in i), float(c_gpu[tuple(i)]), float(ref["c"][tuple(i)]),
+                   float(ref["tau"][tuple(i)])) for i in idx]
+        raise AssertionError(f"{int(bad.sum())} of {bad.size} elements outside tolerance; "
+                             f"first (l,m,n), gpu, ref, tau: {detail}")
+    assert np.float32(amax_gpu).view(np.uint32) == abs_max_bits(c_gpu), (amax_gpu, np.abs(c_gpu).max())
+    if np.isfinite(ref["amax"]):
+        assert abs(amax_gpu - ref["amax"]) <= float(ref["tau"][finite].max())
+    else:
+        assert amax_gpu == ref["amax"]
+    return ref
