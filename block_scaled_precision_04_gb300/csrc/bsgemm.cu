@@ -46,8 +46,6 @@ constexpr int kStageKBytes = 128;  // bytes of K per operand row per stage (one 
 constexpr int kMmaKBytes = 32;     // bytes of K per tcgen05.mma (32 FP8 or 64 FP4 elements)
 constexpr int kThreads = 192;
 constexpr int kAtomBytes = 512;    // one scale atom: 128 rows x 4 K-blocks
-constexpr int kMaxChunks = 4;      // scale atoms along K per stage (FP4, sfv 16)
-constexpr int kNumAcc = 2;         // accumulator buffers in tensor memory
 constexpr uint32_t kTmemCols = 512;
 
 // error word bits (workspace word 2); word 3 keeps where the first wait gave up
@@ -61,10 +59,6 @@ struct Params {
   int k_bytes;            // bytes per operand row
   int k_stages;           // ceil(k_bytes / 128)
   int t_m, t_n, t_k;      // scale atoms: ceil(M/128), ceil(N/128), ceil(K/(4 sfv))
-  int chunks_per_stage;   // atoms along K per stage
-  int mmas_per_chunk;     // MMAs reading one atom column group
-  int sf_id_step;         // scale-byte step between those MMAs
-  int kind;
   int tile_n;
   int stages;
   int c_dtype;            // bsg_dtype
@@ -218,6 +212,23 @@ __device__ __forceinline__ uint64_t desc_atom(uint32_t saddr) {
 
 // ------------------------------------------------------------- helpers
 
+// Per-kind constants: scale atoms per 128-byte K stage, MMAs per atom
+// column group, and the scale-byte step between those MMAs.
+template <int KIND>
+struct KindTraits;
+template <>
+struct KindTraits<kKindF8F6F4> {  // FP8, block 32: one scale byte per K=32 MMA
+  static constexpr int kChunks = 1, kMmasPerChunk = 4, kSfIdStep = 1;
+};
+template <>
+struct KindTraits<kKindF4x4X> {  // FP4, block 16: four scale bytes per K=64 MMA
+  static constexpr int kChunks = 4, kMmasPerChunk = 1, kSfIdStep = 0;
+};
+template <>
+struct KindTraits<kKindF4x2X> {  // FP4, block 32: two scale bytes per K=64 MMA
+  static constexpr int kChunks = 2, kMmasPerChunk = 2, kSfIdStep = 2;
+};
+
 struct Tile {
   int l, mt, nt;
 };
@@ -232,13 +243,25 @@ __device__ __forceinline__ Tile tile_coords(const Params& p, int t) {
   return r;
 }
 
-// Bounded wait.  Returns false when the pipeline is being abandoned.
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Params& p,
-                                      volatile uint32_t* abort_flag, uint32_t where) {
-  if (mbar_try_wait(bar, parity)) return true;
+// try_wait that may suspend the thread for up to `hint_ns` while the phase is open
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded slow path of a wait.  Returns false when the pipeline is abandoned.
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Params& p,
+                                       volatile uint32_t* abort_flag, uint32_t where) {
   const unsigned long long start = globaltimer();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*abort_flag) return false;
     if (globaltimer() - start > p.wait_limit_ns) {
       atomicOr(p.ws + 2, kErrTimeout);
@@ -249,13 +272,43 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Param
   }
 }
 
+// Fast path inline: one try_wait; the bounded loop only when the phase is open.
+#define BSG_WAIT(bar, parity, site) \
+  (mbar_try_wait((bar), (parity)) || wait_slow((bar), (parity), p, abort_flag, (site)))
+
 __device__ __forceinline__ uint32_t abs_bits_f32(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
+
+// Bounded wait for the drains at exit (no abort flag: always runs).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const Params& p,
+                                           uint32_t where) {
+  const unsigned long long start = globaltimer();
+  while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
+    if (globaltimer() - start > p.wait_limit_ns) {
+      atomicOr(p.ws + 2, kErrTimeout);
+      atomicCAS(p.ws + 3, 0u, where);
+      break;
+    }
+  }
+}
 
 // --------------------------------------------------------------- kernel
 
+template <int KIND, int TILE_N, int NUM_ACC>
 __global__ void __launch_bounds__(kThreads, 1)
     bsg_gemm_amax_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ Params p) {
+  using KT = KindTraits<KIND>;
+  constexpr int G = TILE_N / 128;                       // 128-row scale groups of B per tile
+  constexpr uint32_t kAStage = kTileM * kStageKBytes;   // smem bytes per stage
+  constexpr uint32_t kBStage = TILE_N * kStageKBytes;
+  constexpr uint32_t kSfaStage = KT::kChunks * kAtomBytes;
+  constexpr uint32_t kSfbStage = KT::kChunks * kAtomBytes * G;
+  // scale columns follow the accumulators, one set per smem stage, so that a
+  // stage's tcgen05.cp never rewrites columns an in-flight MMA still reads
+  constexpr uint32_t kSfCols = 4 * KT::kChunks * (1 + G);
+  constexpr uint32_t kSfCol0 = NUM_ACC * TILE_N;
+  constexpr int kMmasPerStage = kStageKBytes / kMmaKBytes;
+
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // align the dynamic window to 1024 bytes (128-byte swizzle atoms)
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -265,27 +318,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int S = p.stages;
-  const int G = p.tile_n / 128;  // 128-row scale groups of B per tile
 
   const uint32_t bar0 = base + p.smem_bar;
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
-  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };
-  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * S + kNumAcc + b); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * S + 2 * kNumAcc);
-  uint32_t* const misc = reinterpret_cast<uint32_t*>(smem + p.smem_bar + 8u * (2 * S + 2 * kNumAcc + 1));
+  const uint32_t full0 = bar0, empty0 = bar0 + 8u * S;
+  const uint32_t accf0 = bar0 + 16u * S, acce0 = accf0 + 8u * NUM_ACC;
+  const uint32_t drain_bar = acce0 + 8u * NUM_ACC;
+  uint32_t* const misc =
+      reinterpret_cast<uint32_t*>(smem + p.smem_bar + 16u * S + 16u * NUM_ACC + 8u);
   uint32_t* const tmem_holder = misc + 0;
   volatile uint32_t* const abort_flag = misc + 1;
   uint32_t* const cta_amax = misc + 2;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(full0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, 1);
     }
-    for (int b = 0; b < kNumAcc; ++b) {
-      mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), 4);  // one arrival per epilogue warp
+    for (int b = 0; b < NUM_ACC; ++b) {
+      mbar_init(accf0 + 8u * b, 1);
+      mbar_init(acce0 + 8u * b, 4);  // one arrival per epilogue warp
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0u;
@@ -308,13 +359,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t sfa_col = kNumAcc * p.tile_n;   // scale columns after the accumulators
-  const uint32_t sfb_col = sfa_col + 4 * kMaxChunks;
-
-  const uint32_t a_stage_bytes = kTileM * kStageKBytes;
-  const uint32_t b_stage_bytes = p.tile_n * kStageKBytes;
-  const uint32_t sfa_stage_bytes = kMaxChunks * kAtomBytes;
-  const uint32_t sfb_stage_bytes = kMaxChunks * kAtomBytes * G;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -324,49 +368,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t armed = 0;  // stages with a load issued (for the drain)
       uint32_t armed_parity = 0;
       bool ok = true;
+      const uint32_t a_dst0 = base + p.smem_a, b_dst0 = base + p.smem_b;
+      const uint32_t sfa_dst0 = base + p.smem_sfa, sfb_dst0 = base + p.smem_sfb;
+      const size_t sf_group_stride = static_cast<size_t>(p.t_k) * kAtomBytes;
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         const Tile tc = tile_coords(p, t);
+        int groups = p.t_n - tc.nt * G;
+        if (groups > G) groups = G;
+        const uint8_t* sfa_src =
+            p.sfa + (static_cast<size_t>(tc.l) * p.t_m + tc.mt) * sf_group_stride;
+        const uint8_t* sfb_src =
+            p.sfb + (static_cast<size_t>(tc.l) * p.t_n + static_cast<size_t>(tc.nt) * G) *
+                        sf_group_stride;
+        const int m0 = tc.mt * kTileM, n0 = tc.nt * TILE_N;
         for (int ks = 0; ks < p.k_stages; ++ks) {
-          if (!wait_bar(empty_bar(stage), phase ^ 1u, p, abort_flag, 1)) { ok = false; break; }
-          const int chunk0 = ks * p.chunks_per_stage;
-          int nch = p.t_k - chunk0;
-          if (nch > p.chunks_per_stage) nch = p.chunks_per_stage;
-          int groups = p.t_n - tc.nt * G;
-          if (groups > G) groups = G;
-          const uint32_t bytes = a_stage_bytes + b_stage_bytes +
-                                 static_cast<uint32_t>(nch) * kAtomBytes * (1u + groups);
-          mbar_arrive_expect_tx(full_bar(stage), bytes);
+          if (!BSG_WAIT(empty0 + 8u * stage, phase ^ 1u, 1)) { ok = false; break; }
+          int nch = p.t_k - ks * KT::kChunks;
+          if (nch > KT::kChunks) nch = KT::kChunks;
+          const uint32_t sf_bytes = static_cast<uint32_t>(nch) * kAtomBytes;
+          const uint32_t fb = full0 + 8u * stage;
+          mbar_arrive_expect_tx(fb, kAStage + kBStage + sf_bytes * (1u + groups));
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          tma_load_3d(base + p.smem_a + stage * a_stage_bytes, &tmap_a, ks * kStageKBytes,
-                      tc.mt * kTileM, tc.l, full_bar(stage));
-          tma_load_3d(base + p.smem_b + stage * b_stage_bytes, &tmap_b, ks * kStageKBytes,
-                      tc.nt * p.tile_n, tc.l, full_bar(stage));
-          const size_t a_atom = (static_cast<size_t>(tc.l) * p.t_m + tc.mt) * p.t_k + chunk0;
-          bulk_load(base + p.smem_sfa + stage * sfa_stage_bytes, p.sfa + a_atom * kAtomBytes,
-                    nch * kAtomBytes, full_bar(stage));
-          for (int g = 0; g < groups; ++g) {
-            const size_t b_atom =
-                (static_cast<size_t>(tc.l) * p.t_n + tc.nt * G + g) * p.t_k + chunk0;
-            bulk_load(base + p.smem_sfb + stage * sfb_stage_bytes + g * kMaxChunks * kAtomBytes,
-                      p.sfb + b_atom * kAtomBytes, nch * kAtomBytes, full_bar(stage));
-          }
+          tma_load_3d(a_dst0 + stage * kAStage, &tmap_a, ks * kStageKBytes, m0, tc.l, fb);
+          tma_load_3d(b_dst0 + stage * kBStage, &tmap_b, ks * kStageKBytes, n0, tc.l, fb);
+          const size_t sf_off = static_cast<size_t>(ks) * KT::kChunks * kAtomBytes;
+          bulk_load(sfa_dst0 + stage * kSfaStage, sfa_src + sf_off, sf_bytes, fb);
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+            if (g < groups)
+              bulk_load(sfb_dst0 + stage * kSfbStage + g * kSfaStage,
+                        sfb_src + g * sf_group_stride + sf_off, sf_bytes, fb);
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
       }
       // drain: every issued load must have landed before the CTA may exit
-      for (int s = 0; s < S; ++s) {
-        if (armed & (1u << s)) {
-          const unsigned long long start = globaltimer();
-          while (!mbar_try_wait(full_bar(s), (armed_parity >> s) & 1u)) {
-            if (globaltimer() - start > p.wait_limit_ns) {
-              atomicOr(p.ws + 2, kErrTimeout);
-              atomicCAS(p.ws + 3, 0u, 10u);
-              break;
-            }
-          }
-        }
-      }
+      for (int s = 0; s < S; ++s)
+        if (armed & (1u << s)) drain_wait(full0 + 8u * s, (armed_parity >> s) & 1u, p, 10u);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
@@ -376,56 +414,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
+      // descriptors of stage 0; a stage or MMA step adds a constant to the
+      // 16-byte-granular start address in the low bits
+      const uint64_t adesc0 = desc_sw128(base + p.smem_a);
+      const uint64_t bdesc0 = desc_sw128(base + p.smem_b);
+      const uint64_t sfadesc0 = desc_atom(base + p.smem_sfa);
+      const uint64_t sfbdesc0 = desc_atom(base + p.smem_sfb);
+      const int last = p.k_stages - 1;
+      int last_nmma = (p.k_bytes - last * kStageKBytes + kMmaKBytes - 1) / kMmaKBytes;
+      if (last_nmma > kMmasPerStage) last_nmma = kMmasPerStage;
+      const int last_nch = p.t_k - last * KT::kChunks;
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         const Tile tc = tile_coords(p, t);
         int groups = p.t_n - tc.nt * G;
         if (groups > G) groups = G;
-        if (!wait_bar(acce_bar(acc), acc_phase ^ 1u, p, abort_flag, 2)) { ok = false; break; }
+        if (!BSG_WAIT(acce0 + 8u * acc, acc_phase ^ 1u, 2)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + acc * p.tile_n;
+        const uint32_t d_tmem = tmem + acc * TILE_N;
         for (int ks = 0; ks < p.k_stages; ++ks) {
-          if (!wait_bar(full_bar(stage), phase, p, abort_flag, 3)) { ok = false; break; }
+          if (!BSG_WAIT(full0 + 8u * stage, phase, 3)) { ok = false; break; }
           tc_fence_after();
-          const int chunk0 = ks * p.chunks_per_stage;
-          int nch = p.t_k - chunk0;
-          if (nch > p.chunks_per_stage) nch = p.chunks_per_stage;
-          const uint32_t sa = base + p.smem_sfa + stage * sfa_stage_bytes;
-          const uint32_t sb = base + p.smem_sfb + stage * sfb_stage_bytes;
-          for (int c = 0; c < nch; ++c) {
-            tc_cp_sf(tmem + sfa_col + 4 * c, desc_atom(sa + c * kAtomBytes));
-            for (int g = 0; g < groups; ++g)
-              tc_cp_sf(tmem + sfb_col + 4 * (c * G + g),
-                       desc_atom(sb + g * kMaxChunks * kAtomBytes + c * kAtomBytes));
+          const int nch = ks == last ? last_nch : KT::kChunks;
+          const int nmma = ks == last ? last_nmma : kMmasPerStage;
+          const uint32_t sfa_t = tmem + kSfCol0 + stage * kSfCols;
+          const uint32_t sfb_t = sfa_t + 4 * KT::kChunks;
+          const uint64_t sad = sfadesc0 + ((stage * kSfaStage) >> 4);
+          const uint64_t sbd = sfbdesc0 + ((stage * kSfbStage) >> 4);
+#pragma unroll
+          for (int c = 0; c < KT::kChunks; ++c) {
+            if (c < nch) {
+              tc_cp_sf(sfa_t + 4 * c, sad + ((c * kAtomBytes) >> 4));
+#pragma unroll
+              for (int g = 0; g < G; ++g)
+                if (g < groups)
+                  tc_cp_sf(sfb_t + 4 * (c * G + g), sbd + ((g * kSfaStage + c * kAtomBytes) >> 4));
+            }
           }
-          int nmma = (p.k_bytes - ks * kStageKBytes + kMmaKBytes - 1) / kMmaKBytes;
-          if (nmma > kStageKBytes / kMmaKBytes) nmma = kStageKBytes / kMmaKBytes;
-          const uint32_t a_tile = base + p.smem_a + stage * a_stage_bytes;
-          const uint32_t b_tile = base + p.smem_b + stage * b_stage_bytes;
-          for (int j = 0; j < nmma; ++j) {
-            const int c = j / p.mmas_per_chunk;
-            const uint32_t sf_id = static_cast<uint32_t>((j % p.mmas_per_chunk) * p.sf_id_step);
-            const uint32_t idesc = p.idesc | (sf_id << 29) | (sf_id << 4);
-            tc_mma(p.kind, d_tmem, desc_sw128(a_tile + j * kMmaKBytes),
-                   desc_sw128(b_tile + j * kMmaKBytes), idesc, tmem + sfa_col + 4 * c,
-                   tmem + sfb_col + 4 * G * c, (ks > 0 || j > 0) ? 1u : 0u);
+          const uint64_t ad = adesc0 + ((stage * kAStage) >> 4);
+          const uint64_t bd = bdesc0 + ((stage * kBStage) >> 4);
+#pragma unroll
+          for (int j = 0; j < kMmasPerStage; ++j) {
+            if (j < nmma) {
+              const int c = j / KT::kMmasPerChunk;
+              const uint32_t sf_id = static_cast<uint32_t>((j % KT::kMmasPerChunk) * KT::kSfIdStep);
+              tc_mma(KIND, d_tmem, ad + ((j * kMmaKBytes) >> 4), bd + ((j * kMmaKBytes) >> 4),
+                     p.idesc | (sf_id << 29) | (sf_id << 4), sfa_t + 4 * c, sfb_t + 4 * G * c,
+                     (ks | j) != 0 ? 1u : 0u);
+            }
           }
-          tc_commit(empty_bar(stage));  // frees the smem stage once these MMAs finish
+          tc_commit(empty0 + 8u * stage);  // frees the smem stage once these MMAs finish
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        tc_commit(accf_bar(acc));  // accumulator ready for the epilogue
-        if (++acc == kNumAcc) { acc = 0; acc_phase ^= 1u; }
+        tc_commit(accf0 + 8u * acc);  // accumulator ready for the epilogue
+        if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1u; }
       }
       // drain: all MMAs and copies issued by this thread complete before exit
       tc_commit(drain_bar);
-      const unsigned long long start = globaltimer();
-      while (!mbar_try_wait(drain_bar, 0)) {
-        if (globaltimer() - start > p.wait_limit_ns) {
-          atomicOr(p.ws + 2, kErrTimeout);
-          atomicCAS(p.ws + 3, 0u, 11u);
-          break;
-        }
-      }
+      drain_wait(drain_bar, 0, p, 11u);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -437,17 +483,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Tile tc = tile_coords(p, t);
       // one lane waits, the warp follows its verdict (tcgen05.ld is warp-collective)
       int ready = 0;
-      if (lane == 0) ready = wait_bar(accf_bar(acc), acc_phase, p, abort_flag, 4) ? 1 : 0;
+      if (lane == 0) ready = BSG_WAIT(accf0 + 8u * acc, acc_phase, 4) ? 1 : 0;
       ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
       if (!ready) break;
       tc_fence_after();
       const int row = tc.mt * kTileM + q * 32 + lane;
       const bool row_ok = row < p.M;
       const size_t batch_off = static_cast<size_t>(tc.l) * p.M * p.N;
-      for (int cc = 0; cc < p.tile_n; cc += 32) {
+#pragma unroll 1
+      for (int cc = 0; cc < TILE_N; cc += 32) {
         uint32_t r[32];
-        tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * p.tile_n + cc, r);
-        const int n0 = tc.nt * p.tile_n + cc;
+        tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * TILE_N + cc, r);
+        const int n0 = tc.nt * TILE_N + cc;
         if (p.c_major == 0) {
           // n-major: this thread owns 32 consecutive elements of row `row`
           if (p.c_dtype == BSG_F32) {
@@ -463,7 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           } else {
-            uint16_t* dst = static_cast<uint16_t*>(p.c) + batch_off + static_cast<size_t>(row) * p.N + n0;
+            uint16_t* dst =
+                static_cast<uint16_t*>(p.c) + batch_off + static_cast<size_t>(row) * p.N + n0;
 #pragma unroll
             for (int i = 0; i < 32; i += 8) {
               if (row_ok && n0 + i < p.N) {
@@ -518,8 +566,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce_bar(acc));
-      if (++acc == kNumAcc) { acc = 0; acc_phase ^= 1u; }
+      if (lane == 0) mbar_arrive(acce0 + 8u * acc);
+      if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1u; }
     }
     vmax = __reduce_max_sync(0xFFFFFFFFu, vmax);
     if (lane == 0) atomicMax(cta_amax, vmax);
@@ -547,6 +595,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       atomicExch(p.ws + 1, 0u);
     }
   }
+}
+#undef BSG_WAIT
+
+// Kernel variants: MMA kind x (TILE_N, accumulator buffers in tensor memory)
+struct Variant {
+  int kind, tile_n, num_acc;
+  const void* fn;
+};
+
+template <int KIND, int TN, int NACC>
+Variant make_variant() {
+  return Variant{KIND, TN, NACC, reinterpret_cast<const void*>(&bsg_gemm_amax_kernel<KIND, TN, NACC>)};
+}
+
+const Variant* find_variant(int kind, int tile_n, int num_acc) {
+  static const Variant table[] = {
+      make_variant<kKindF8F6F4, 128, 2>(), make_variant<kKindF8F6F4, 256, 1>(),
+      make_variant<kKindF4x4X, 128, 2>(),  make_variant<kKindF4x4X, 256, 1>(),
+      make_variant<kKindF4x2X, 128, 2>(),  make_variant<kKindF4x2X, 256, 1>(),
+  };
+  for (const Variant& v : table)
+    if (v.kind == kind && v.tile_n == tile_n && v.num_acc == num_acc) return &v;
+  return nullptr;
 }
 
 // ------------------------------------------------------------------ host
@@ -583,6 +654,9 @@ struct bsg_plan {
   int device;
   int sm_count;
   Params base;           // everything but the pointers
+  const void* kernel;    // the chosen kernel variant
+  int kind;
+  int num_acc;
   int grid;
   int smem_bytes;
   // tensor maps for the last A/B pointers seen
@@ -676,7 +750,20 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   k.N = static_cast<int>(prob->N);
   k.K = static_cast<int>(prob->K);
   k.L = static_cast<int>(prob->L);
-  k.tile_n = 128;
+  int kind;
+  if (!fp4) kind = kKindF8F6F4;          // one scale (block 32) per MMA: byte j of the column
+  else if (sfv == 16) kind = kKindF4x4X;  // four block-16 scales per MMA: the whole column
+  else kind = kKindF4x2X;                 // two block-32 scales per MMA: bytes 0-1 or 2-3
+  const int chunks = kind == kKindF8F6F4 ? 1 : (kind == kKindF4x4X ? 4 : 2);
+  // 128 x 256 tiles halve the issue work and the L2 traffic per flop; a
+  // hint of 128 (or N <= 128) keeps the double-buffered 128 x 128 variant
+  k.tile_n = prob->tile_n == 128 || (prob->tile_n == 0 && prob->N <= 128) ? 128 : 256;
+  const int num_acc = k.tile_n == 256 ? 1 : 2;
+  const Variant* var = find_variant(kind, k.tile_n, num_acc);
+  if (!var) { delete plan; return BSG_ERR_UNSUPPORTED; }
+  plan->kernel = var->fn;
+  plan->kind = kind;
+  plan->num_acc = num_acc;
   k.tiles_m = static_cast<int>(cdiv(prob->M, kTileM));
   k.tiles_n = static_cast<int>(cdiv(prob->N, k.tile_n));
   k.num_tiles = k.tiles_m * k.tiles_n * k.L;
@@ -685,24 +772,6 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   k.t_m = static_cast<int>(cdiv(prob->M, 128));
   k.t_n = static_cast<int>(cdiv(prob->N, 128));
   k.t_k = static_cast<int>(cdiv(prob->K, 4 * sfv));
-  // elements of K per stage: 128 (FP8) or 256 (FP4); one atom spans 4*sfv
-  const int k_elems_stage = fp4 ? 2 * kStageKBytes : kStageKBytes;
-  k.chunks_per_stage = k_elems_stage / (4 * sfv);
-  const int k_elems_mma = fp4 ? 2 * kMmaKBytes : kMmaKBytes;
-  if (!fp4) {
-    k.kind = kKindF8F6F4;  // one scale (block 32) per MMA: byte j of the column
-    k.mmas_per_chunk = 4;
-    k.sf_id_step = 1;
-  } else if (sfv == 16) {
-    k.kind = kKindF4x4X;   // four block-16 scales per MMA: the whole column
-    k.mmas_per_chunk = 1;
-    k.sf_id_step = 0;
-  } else {
-    k.kind = kKindF4x2X;   // two block-32 scales per MMA: bytes 0-1 or 2-3
-    k.mmas_per_chunk = 2;
-    k.sf_id_step = 2;
-  }
-  (void)k_elems_mma;
   uint32_t a_fmt, b_fmt;
   if (fp4) {
     a_fmt = b_fmt = 1;  // E2M1 in kind::mxf4nvf4
@@ -716,19 +785,24 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   k.c_major = prob->c_major == 'm' ? 1 : 0;
 
   const int G = k.tile_n / 128;
-  const int per_stage = kTileM * kStageKBytes + k.tile_n * kStageKBytes +
-                        kMaxChunks * kAtomBytes * (1 + G);
+  const int sfa_stage = chunks * kAtomBytes, sfb_stage = chunks * kAtomBytes * G;
+  const int per_stage = kTileM * kStageKBytes + k.tile_n * kStageKBytes + sfa_stage + sfb_stage;
   const int reserve = 1024 /* alignment slack */ + 512 /* barriers and flags */;
   int stages = (max_smem - reserve) / per_stage;
   if (stages > 8) stages = 8;
-  if (stages < 2) { delete plan; return BSG_ERR_UNSUPPORTED; }
+  const int sf_cols = 4 * chunks * (1 + G);
+  while (stages > 2 && num_acc * k.tile_n + stages * sf_cols > static_cast<int>(kTmemCols)) --stages;
+  if (stages < 2 || num_acc * k.tile_n + stages * sf_cols > static_cast<int>(kTmemCols)) {
+    delete plan;
+    return BSG_ERR_UNSUPPORTED;
+  }
   k.stages = stages;
   k.smem_a = 0;
   k.smem_b = k.smem_a + stages * kTileM * kStageKBytes;
   k.smem_sfa = k.smem_b + stages * k.tile_n * kStageKBytes;
-  k.smem_sfb = k.smem_sfa + stages * kMaxChunks * kAtomBytes;
-  k.smem_bar = k.smem_sfb + stages * kMaxChunks * kAtomBytes * G;
-  plan->smem_bytes = static_cast<int>(k.smem_bar) + 8 * (2 * stages + 2 * kNumAcc + 1) + 16 + 1024;
+  k.smem_sfb = k.smem_sfa + stages * sfa_stage;
+  k.smem_bar = k.smem_sfb + stages * sfb_stage;
+  plan->smem_bytes = static_cast<int>(k.smem_bar) + 16 * stages + 16 * num_acc + 8 + 16 + 1024;
   k.wait_limit_ns = 1000000000ull;  // one second per wait
   if (const char* e = std::getenv("BSG_WAIT_LIMIT_NS")) {
     const unsigned long long v = std::strtoull(e, nullptr, 10);
@@ -739,7 +813,7 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   int prev = 0;
   cudaGetDevice(&prev);
   if (prev != device) cudaSetDevice(device);
-  const cudaError_t e = cudaFuncSetAttribute(bsg_gemm_amax_kernel,
+  const cudaError_t e = cudaFuncSetAttribute(plan->kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              plan->smem_bytes);
   if (prev != device) cudaSetDevice(prev);
@@ -753,7 +827,7 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
                  "[bsgemm] M=%lld N=%lld K=%lld L=%lld tile=128x%d stages=%d grid=%d smem=%d "
                  "kind=%d tiles=%d\n",
                  (long long)prob->M, (long long)prob->N, (long long)prob->K, (long long)prob->L,
-                 k.tile_n, stages, plan->grid, plan->smem_bytes, k.kind, k.num_tiles);
+                 k.tile_n, stages, plan->grid, plan->smem_bytes, kind, k.num_tiles);
   *out = plan;
   return BSG_OK;
 }
@@ -829,9 +903,13 @@ bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const vo
     ma = plan->map_a;
     mb = plan->map_b;
   }
-  bsg_gemm_amax_kernel<<<plan->grid, kThreads, plan->smem_bytes,
-                         static_cast<cudaStream_t>(stream)>>>(ma, mb, k);
-  if (cudaGetLastError() != cudaSuccess) return BSG_ERR_CUDA;
+  void* args[3] = {&ma, &mb, &k};
+  if (cudaLaunchKernel(plan->kernel, dim3(plan->grid), dim3(kThreads), args,
+                       static_cast<size_t>(plan->smem_bytes),
+                       static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return BSG_ERR_CUDA;
+  }
   return BSG_OK;
 }
 
@@ -897,7 +975,7 @@ bsg_status bsg_plan_describe(const bsg_plan* plan, bsg_plan_info* info) {
   info->threads = kThreads;
   info->smem_bytes = plan->smem_bytes;
   info->num_tiles = plan->base.num_tiles;
-  info->mma_kind = plan->base.kind;
+  info->mma_kind = plan->kind;
   std::snprintf(info->kernel_name, sizeof(info->kernel_name), "bsg_gemm_amax_kernel");
   return BSG_OK;
 }

@@ -221,3 +221,26 @@ def test_workload_full_size_sampled(number):
     # the GPU's maximum element is itself within tolerance of the oracle
     i_arg = len(pts) - 3
     assert abs(amax - abs(cref[i_arg])) <= tau[i_arg]
+
+
+# ------------------------------------------------- tile-shape variants
+
+TILE_CASES = [
+    P(256, 512, 512), P(200, 520, 160, 2, c="bf16"), P(136, 1000, 96, major="m"),
+    P(128, 264, 64, a="e2m1", b="e2m1", sfv=16),
+    P(260, 384, 640, a="e2m1", b="e2m1", sfv=16, c="bf16"),
+    P(132, 392, 384, 2, a="e2m1", b="e2m1", sfv=32, major="m"),
+    P(384, 1100, 256, a="e5m2", b="e4m3"),
+]
+
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("p", TILE_CASES, ids=[f"{p.M}x{p.N}x{p.K}L{p.L}{p.a_dtype}sfv{p.sfv}{p.c_major}" for p in TILE_CASES])
+def test_tile_variants(p, tile_n):
+    """Both CTA tile widths (the 128 x 256 tile reads two 128-row scale
+    groups of B per K-chunk) against the oracle, ragged N included."""
+    inp = synth.uniform_codes(p, p.M * 5 + p.N + p.K + tile_n, 123, 131)
+    c, amax, _, op, guard_ok = run_gpu(inp, guard=4096, tile_n=tile_n)
+    assert op.describe()["tile_n"] == tile_n
+    assert guard_ok
+    assert_parity(inp, c, amax)
