@@ -92,11 +92,13 @@ def library() -> ctypes.CDLL:
     lib.bsg_run_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(bsg_device_buffers),
                                  vp]
     lib.bsg_check_device_status.argtypes = [vp, vp, vp]
+    lib.bsg_run_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
     lib.bsg_plan_describe.argtypes = [vp, ctypes.POINTER(bsg_plan_info)]
     lib.bsg_plan_destroy.argtypes = [vp]
     lib.bsg_plan_destroy.restype = None
     for name in ("bsg_problem_check", "bsg_plan_create", "bsg_plan_workspace_size",
                  "bsg_workspace_init", "bsg_run", "bsg_run_host", "bsg_check_device_status",
+                 "bsg_run_noalloc",
                  "bsg_plan_describe"):
         getattr(lib, name).restype = i32
     _lib = lib
@@ -150,6 +152,14 @@ def bsg_run_host(plan, hA: int, hB: int, hSFA: int, hSFB: int, hC: int, h_amax: 
     v = ctypes.c_void_p
     return library().bsg_run_host(plan, v(hA), v(hB), v(hSFA), v(hSFB), v(hC), v(h_amax),
                                   ctypes.byref(dev), v(stream))
+
+
+def bsg_run_noalloc(plan, A: int, B: int, SFA: int, SFB: int, C: int, amax: int,
+                    stream: int = 0) -> int:
+    """bsg_run for callers that cannot allocate: the workspace is a fixed
+    array inside the library (see include/bsgemm.h)."""
+    v = ctypes.c_void_p
+    return library().bsg_run_noalloc(plan, v(A), v(B), v(SFA), v(SFB), v(C), v(amax), v(stream))
 
 
 def bsg_check_device_status(plan, workspace: int, stream: int = 0) -> int:

@@ -913,6 +913,68 @@ bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const vo
   return BSG_OK;
 }
 
+// ---------------------------------------------------------------------------
+// bsg_run_noalloc: the same launch as bsg_run, with the workspace taken from a
+// fixed device array of this library instead of caller memory.  For callers
+// that cannot allocate device memory at all (no allocator of their own, or a
+// context in which cudaMalloc is not allowed).
+
+// Largest workspace the fixed array can stand in for; a plan needing more is
+// rejected with BSG_ERR_WORKSPACE.
+static constexpr size_t kNoAllocScratchBytes = 4096;
+
+// Loaded (zero-filled) on every GPU that loads this library, held until exit.
+// Host code must not hand this name to a kernel: on the host it is only a
+// stand-in; the device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+static constexpr int kNoAllocMaxDevices = 64;
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the array on the current device, looked up once per
+// device (the first call on a device; it also zero-fills the array,
+// synchronously).
+static bsg_status noalloc_scratch(int device, void** out) {
+  if (device < 0 || device >= kNoAllocMaxDevices) return BSG_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[device]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+      cudaGetLastError();
+      return BSG_ERR_CUDA;
+    }
+    if (cudaMemset(ptr, 0, kNoAllocScratchBytes) != cudaSuccess) {
+      cudaGetLastError();
+      return BSG_ERR_CUDA;
+    }
+    g_noalloc_ptr[device] = ptr;
+  }
+  *out = g_noalloc_ptr[device];
+  return BSG_OK;
+}
+
+bsg_status bsg_run_noalloc(const bsg_plan* plan, const void* A, const void* B, const void* SFA,
+                           const void* SFB, void* C, float* amax, void* stream) {
+  if (!plan) return BSG_ERR_INVALID_ARG;
+  size_t need = 0;
+  bsg_status st = bsg_plan_workspace_size(plan, &need);
+  if (st != BSG_OK) return st;
+  if (need > kNoAllocScratchBytes) return BSG_ERR_WORKSPACE;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return BSG_ERR_CUDA; }
+  void* scratch = nullptr;
+  st = noalloc_scratch(dev, &scratch);
+  if (st != BSG_OK) return st;
+  // the array keeps the previous call's words: clear the Amax slot, the
+  // arrival counter and the error word before this launch
+  if (cudaMemsetAsync(scratch, 0, 16, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return BSG_ERR_CUDA;
+  }
+  return bsg_run(plan, A, B, SFA, SFB, C, amax, scratch, kNoAllocScratchBytes, stream);
+}
+
 bsg_status bsg_run_host(const bsg_plan* plan, const void* hA, const void* hB, const void* hSFA,
                         const void* hSFB, void* hC, float* h_amax, const bsg_device_buffers* dev,
                         void* stream) {

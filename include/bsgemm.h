@@ -134,6 +134,22 @@ bsg_status bsg_run(const bsg_plan *plan, const void *A, const void *B, const voi
                    const void *SFB, void *C, float *amax, void *workspace, size_t ws_bytes,
                    void *stream);
 
+/* bsg_run without a caller workspace, for callers that cannot allocate
+ * device memory (no allocator to draw from, or code running where
+ * cudaMalloc is not permitted).  The paper has no counterpart: it is a
+ * convenience of this library.  The workspace comes from a fixed array
+ * inside the library (4096 bytes on every GPU that loads it, kept until the
+ * process exits); a plan needing more returns BSG_ERR_WORKSPACE.  The first
+ * call on a device looks the array up and zero-fills it synchronously, so
+ * make that first call before any stream capture.  Each call clears the
+ * array's first 16 bytes on `stream`, then launches exactly as bsg_run.  All
+ * calls share the one array: calls that overlap on the device race and
+ * give wrong results.  A device-side wait timeout is not reported here (use
+ * bsg_run with a workspace and bsg_check_device_status for that).  Nothing
+ * is allocated. */
+bsg_status bsg_run_noalloc(const bsg_plan *plan, const void *A, const void *B, const void *SFA,
+                           const void *SFB, void *C, float *amax, void *stream);
+
 /* Device buffers for bsg_run_host: caller-allocated, sized for the plan. */
 typedef struct {
     void *A, *B, *SFA, *SFB, *C;
