@@ -58,7 +58,7 @@ class bsg_plan_info(ctypes.Structure):
                 ("tile_k_bytes", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("threads", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("num_tiles", ctypes.c_int32),
-                ("mma_kind", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("mma_kind", ctypes.c_int32), ("cluster_m", ctypes.c_int32),
                 ("kernel_name", ctypes.c_char * 64)]
 
 
@@ -170,7 +170,7 @@ def bsg_check_device_status(plan, workspace: int, stream: int = 0) -> int:
 def bsg_plan_describe(plan):
     info = bsg_plan_info()
     st = library().bsg_plan_describe(plan, ctypes.byref(info))
-    out = {f: getattr(info, f) for f, _ in bsg_plan_info._fields_ if f != "reserved"}
+    out = {f: getattr(info, f) for f, _ in bsg_plan_info._fields_}
     out["kernel_name"] = info.kernel_name.decode()
     return st, out
 

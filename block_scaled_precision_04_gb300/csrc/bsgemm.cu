@@ -4,19 +4,20 @@
 //   C[m,n,l] = sum_k dec(A[m,k,l]) 2^(SFA[m,k/sfv,l]-127) * dec(B[n,k,l]) 2^(SFB[n,k/sfv,l]-127)
 //   Amax     = max |C|  (over the values as stored in C's dtype)
 //
-// Kernel design (one persistent CTA per SM, 6 warps):
+// Kernel design (one persistent CTA per SM, 14 warps):
 //   warp 0      TMA producer: per K stage, the 128 x 128-byte A tile and the
 //               TILE_N x 128-byte B tile (128-byte swizzle, 3-D tensor maps
 //               over (K bytes, rows, L), out-of-range rows/columns zero
 //               filled), plus the 512-byte scale atoms of those rows (bulk
 //               copies straight from the page's physical atom layout).
-//   warp 1      MMA issuer: copies the stage's scale atoms shared -> tensor
-//               memory (tcgen05.cp 32x128b.warpx4), then issues block-scaled
-//               tcgen05.mma (kind::mxf8f6f4 scale_vec::1X for FP8,
+//   warp 1      MMA issuer: once a stage's operands are in shared memory and
+//               its scales in tensor memory, issues block-scaled tcgen05.mma (kind::mxf8f6f4 scale_vec::1X for FP8,
 //               kind::mxf4nvf4 scale_vec::4X / 2X for packed FP4) into a
 //               double-buffered fp32 accumulator in tensor memory; commits
 //               free the smem stage and publish a finished accumulator.
-//   warps 2..5  epilogue: tcgen05.ld the accumulator (one row per thread),
+//   warps 2..5  scale warps: tcgen05.st of each stage's scale atoms from
+//               shared into tensor memory (one warp per lane quarter).
+//   warps 6..13 epilogue: tcgen05.ld the accumulator (one row per thread),
 //               round to C's dtype, store, and keep max |stored value| as an
 //               integer max of the float bits; at exit one atomicMax per CTA.
 //   The last CTA to finish writes Amax and re-zeroes the workspace slots.
@@ -44,7 +45,12 @@ namespace {
 constexpr int kTileM = 128;
 constexpr int kStageKBytes = 128;  // bytes of K per operand row per stage (one swizzle row)
 constexpr int kMmaKBytes = 32;     // bytes of K per tcgen05.mma (32 FP8 or 64 FP4 elements)
-constexpr int kThreads = 192;
+// Warp roles: 0 TMA producer, 1 MMA issuer, 2-5 scale warps (tensor-memory
+// lane quarters 2, 3, 0, 1), 6-13 epilogue (two warps per lane quarter).
+constexpr int kSfWarp0 = 2;
+constexpr int kEpiWarp0 = 6;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr int kAtomBytes = 512;    // one scale atom: 128 rows x 4 K-blocks
 constexpr uint32_t kTmemCols = 512;
 
@@ -56,6 +62,8 @@ enum MmaKind : int { kKindF8F6F4 = 0, kKindF4x4X = 1, kKindF4x2X = 2 };
 struct Params {
   int M, N, K, L;
   int tiles_m, tiles_n, num_tiles;
+  int tiles_mc;           // groups of cluster_m consecutive M tiles: ceil(tiles_m / cluster_m)
+  int num_units;          // scheduling units (one per cluster): L * tiles_mc * tiles_n
   int k_bytes;            // bytes per operand row
   int k_stages;           // ceil(k_bytes / 128)
   int t_m, t_n, t_k;      // scale atoms: ceil(M/128), ceil(N/128), ceil(K/(4 sfv))
@@ -119,6 +127,37 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// The same box into the same smem offset of every CTA in `mask`; each
+// destination CTA's mbarrier at `bar`'s offset receives the bytes it got.
+__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                               int z, uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar) {
   asm volatile(
@@ -141,10 +180,16 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
       : "memory");
 }
 
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-               : "memory");
+// Arrive on the mbarrier at `bar`'s offset in every CTA of `mask` once
+// this thread's earlier tcgen05 operations complete.
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
 }
+
 
 __device__ __forceinline__ void tc_mma(int kind, uint32_t d, uint64_t adesc, uint64_t bdesc,
                                        uint32_t idesc, uint32_t sfa, uint32_t sfb,
@@ -174,7 +219,8 @@ __device__ __forceinline__ void tc_mma(int kind, uint32_t d, uint64_t adesc, uin
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base + i).
-__device__ __forceinline__ void tc_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+// No wait: follow with tc_wait_ld() before reading r.
+__device__ __forceinline__ void tc_ld_32x32b_x32(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%"
       "14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -184,8 +230,33 @@ __device__ __forceinline__ void tc_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[3
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
+}
+
+__device__ __forceinline__ void tc_ld_32x32b_x16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%"
+      "14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tc_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+
+// 32 lanes x 4 consecutive 32-bit columns from registers: thread i writes lane (base + i).
+__device__ __forceinline__ void tc_st_32x32b_x4(uint32_t taddr, uint4 v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 
 // Shared-memory matrix descriptor, K-major operand tile with 128-byte
 // swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
@@ -199,16 +270,6 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
   return d;
 }
 
-// Descriptor of one 512-byte scale atom as the source of a 32x128b copy:
-// 32 rows of 16 bytes, no swizzle, 8-row core matrices 128 bytes apart.
-__device__ __forceinline__ uint64_t desc_atom(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(128 >> 4) << 16;
-  d |= static_cast<uint64_t>(128 >> 4) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  return d;
-}
 
 // ------------------------------------------------------------- helpers
 
@@ -233,13 +294,17 @@ struct Tile {
   int l, mt, nt;
 };
 
-__device__ __forceinline__ Tile tile_coords(const Params& p, int t) {
+// Unit u (one per cluster) -> (l, group of cluster_m M tiles, N tile); the
+// CTA of rank `rank` takes M tile group * cm + rank (past tiles_m: a ghost
+// tile whose rows are all masked, kept so the cluster stays in lockstep).
+__device__ __forceinline__ Tile tile_coords(const Params& p, int u, int cm, int rank) {
   Tile r;
-  int per_batch = p.tiles_m * p.tiles_n;
-  r.l = t / per_batch;
-  int rem = t - r.l * per_batch;
-  r.mt = rem / p.tiles_n;
-  r.nt = rem - r.mt * p.tiles_n;
+  const int per_batch = p.tiles_mc * p.tiles_n;
+  r.l = u / per_batch;
+  const int rem = u - r.l * per_batch;
+  const int mg = rem / p.tiles_n;
+  r.nt = rem - mg * p.tiles_n;
+  r.mt = mg * cm + rank;
   return r;
 }
 
@@ -256,9 +321,26 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded slow path of a wait.  Returns false when the pipeline is abandoned.
+// `spin`: poll without suspending first (the producer and MMA threads, whose
+// waits are short and whose wake-up latency is on the critical path).
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Params& p,
-                                       volatile uint32_t* abort_flag, uint32_t where) {
+                                       volatile uint32_t* abort_flag, uint32_t where, bool spin) {
+  if (spin)
+    for (int i = 0; i < 2048; ++i)
+      if (mbar_test_wait(bar, parity)) return true;
   const unsigned long long start = globaltimer();
   while (true) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
@@ -274,7 +356,9 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Para
 
 // Fast path inline: one try_wait; the bounded loop only when the phase is open.
 #define BSG_WAIT(bar, parity, site) \
-  (mbar_try_wait((bar), (parity)) || wait_slow((bar), (parity), p, abort_flag, (site)))
+  (mbar_try_wait((bar), (parity)) || wait_slow((bar), (parity), p, abort_flag, (site), true))
+#define BSG_WAIT_SLEEP(bar, parity, site) \
+  (mbar_try_wait((bar), (parity)) || wait_slow((bar), (parity), p, abort_flag, (site), false))
 
 __device__ __forceinline__ uint32_t abs_bits_f32(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
 
@@ -293,7 +377,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 
 // --------------------------------------------------------------- kernel
 
-template <int KIND, int TILE_N, int NUM_ACC>
+template <int KIND, int TILE_N, int NUM_ACC, int CM>
 __global__ void __launch_bounds__(kThreads, 1)
     bsg_gemm_amax_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ Params p) {
@@ -308,6 +392,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kSfCols = 4 * KT::kChunks * (1 + G);
   constexpr uint32_t kSfCol0 = NUM_ACC * TILE_N;
   constexpr int kMmasPerStage = kStageKBytes / kMmaKBytes;
+  // B tile shared by the cluster's CM CTAs: each loads TILE_N / CM rows and
+  // multicasts them to all
+  constexpr int kBPartRows = TILE_N / CM;
+  constexpr uint32_t kBPart = kBPartRows * kStageKBytes;
+  constexpr uint16_t kMask = static_cast<uint16_t>((1u << CM) - 1u);
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // align the dynamic window to 1024 bytes (128-byte swizzle atoms)
@@ -318,13 +407,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int S = p.stages;
+  const int crank = CM > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int unit0 = CM > 1 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int unit_step = CM > 1 ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
 
   const uint32_t bar0 = base + p.smem_bar;
-  const uint32_t full0 = bar0, empty0 = bar0 + 8u * S;
-  const uint32_t accf0 = bar0 + 16u * S, acce0 = accf0 + 8u * NUM_ACC;
+  const uint32_t full0 = bar0, empty0 = bar0 + 8u * S, sfr0 = bar0 + 16u * S;
+  const uint32_t accf0 = bar0 + 24u * S, acce0 = accf0 + 8u * NUM_ACC;
   const uint32_t drain_bar = acce0 + 8u * NUM_ACC;
   uint32_t* const misc =
-      reinterpret_cast<uint32_t*>(smem + p.smem_bar + 16u * S + 16u * NUM_ACC + 8u);
+      reinterpret_cast<uint32_t*>(smem + p.smem_bar + 24u * S + 16u * NUM_ACC + 8u);
   uint32_t* const tmem_holder = misc + 0;
   volatile uint32_t* const abort_flag = misc + 1;
   uint32_t* const cta_amax = misc + 2;
@@ -332,11 +424,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8u * s, 1);
-      mbar_init(empty0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, CM);  // every CTA's MMA commit frees the stage
+      mbar_init(sfr0 + 8u * s, 4);     // the four scale warps: scales in tensor memory
     }
     for (int b = 0; b < NUM_ACC; ++b) {
       mbar_init(accf0 + 8u * b, 1);
-      mbar_init(acce0 + 8u * b, 4);  // one arrival per epilogue warp
+      mbar_init(acce0 + 8u * b, kEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0u;
@@ -357,6 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (CM > 1) cluster_sync();  // peers' barriers initialised before any multicast
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
@@ -371,12 +465,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t a_dst0 = base + p.smem_a, b_dst0 = base + p.smem_b;
       const uint32_t sfa_dst0 = base + p.smem_sfa, sfb_dst0 = base + p.smem_sfb;
       const size_t sf_group_stride = static_cast<size_t>(p.t_k) * kAtomBytes;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-        const Tile tc = tile_coords(p, t);
+      for (int u = unit0; u < p.num_units && ok; u += unit_step) {
+        const Tile tc = tile_coords(p, u, CM, crank);
         int groups = p.t_n - tc.nt * G;
         if (groups > G) groups = G;
+        const bool ghost = tc.mt >= p.tiles_m;  // no rows of A: skip its scales
         const uint8_t* sfa_src =
-            p.sfa + (static_cast<size_t>(tc.l) * p.t_m + tc.mt) * sf_group_stride;
+            p.sfa + (static_cast<size_t>(tc.l) * p.t_m + (ghost ? 0 : tc.mt)) * sf_group_stride;
         const uint8_t* sfb_src =
             p.sfb + (static_cast<size_t>(tc.l) * p.t_n + static_cast<size_t>(tc.nt) * G) *
                         sf_group_stride;
@@ -387,13 +482,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (nch > KT::kChunks) nch = KT::kChunks;
           const uint32_t sf_bytes = static_cast<uint32_t>(nch) * kAtomBytes;
           const uint32_t fb = full0 + 8u * stage;
-          mbar_arrive_expect_tx(fb, kAStage + kBStage + sf_bytes * (1u + groups));
+          mbar_arrive_expect_tx(fb, kAStage + kBStage + sf_bytes * ((ghost ? 0u : 1u) + groups));
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           tma_load_3d(a_dst0 + stage * kAStage, &tmap_a, ks * kStageKBytes, m0, tc.l, fb);
-          tma_load_3d(b_dst0 + stage * kBStage, &tmap_b, ks * kStageKBytes, n0, tc.l, fb);
+          if (CM == 1)
+            tma_load_3d(b_dst0 + stage * kBStage, &tmap_b, ks * kStageKBytes, n0, tc.l, fb);
+          else
+            tma_load_3d_mc(b_dst0 + stage * kBStage + crank * kBPart, &tmap_b, ks * kStageKBytes,
+                           n0 + crank * kBPartRows, tc.l, fb, kMask);
           const size_t sf_off = static_cast<size_t>(ks) * KT::kChunks * kAtomBytes;
-          bulk_load(sfa_dst0 + stage * kSfaStage, sfa_src + sf_off, sf_bytes, fb);
+          if (!ghost) bulk_load(sfa_dst0 + stage * kSfaStage, sfa_src + sf_off, sf_bytes, fb);
 #pragma unroll
           for (int g = 0; g < G; ++g)
             if (g < groups)
@@ -418,90 +517,212 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 16-byte-granular start address in the low bits
       const uint64_t adesc0 = desc_sw128(base + p.smem_a);
       const uint64_t bdesc0 = desc_sw128(base + p.smem_b);
-      const uint64_t sfadesc0 = desc_atom(base + p.smem_sfa);
-      const uint64_t sfbdesc0 = desc_atom(base + p.smem_sfb);
+      const uint32_t sf_t0 = tmem + kSfCol0;
+      const uint32_t idesc = p.idesc;
+      // running addresses of the current stage
+      uint64_t ad = adesc0, bd = bdesc0;
+      uint32_t sfa_t = sf_t0;
       const int last = p.k_stages - 1;
       int last_nmma = (p.k_bytes - last * kStageKBytes + kMmaKBytes - 1) / kMmaKBytes;
       if (last_nmma > kMmasPerStage) last_nmma = kMmasPerStage;
-      const int last_nch = p.t_k - last * KT::kChunks;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-        const Tile tc = tile_coords(p, t);
-        int groups = p.t_n - tc.nt * G;
-        if (groups > G) groups = G;
+      for (int u = unit0; u < p.num_units && ok; u += unit_step) {
         if (!BSG_WAIT(acce0 + 8u * acc, acc_phase ^ 1u, 2)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * TILE_N;
         for (int ks = 0; ks < p.k_stages; ++ks) {
-          if (!BSG_WAIT(full0 + 8u * stage, phase, 3)) { ok = false; break; }
+          // operands in smem and this stage's scales in tensor memory
+          if (!BSG_WAIT(sfr0 + 8u * stage, phase, 3)) { ok = false; break; }
           tc_fence_after();
-          const int nch = ks == last ? last_nch : KT::kChunks;
-          const int nmma = ks == last ? last_nmma : kMmasPerStage;
-          const uint32_t sfa_t = tmem + kSfCol0 + stage * kSfCols;
           const uint32_t sfb_t = sfa_t + 4 * KT::kChunks;
-          const uint64_t sad = sfadesc0 + ((stage * kSfaStage) >> 4);
-          const uint64_t sbd = sfbdesc0 + ((stage * kSfbStage) >> 4);
+          if (ks != last) {
 #pragma unroll
-          for (int c = 0; c < KT::kChunks; ++c) {
-            if (c < nch) {
-              tc_cp_sf(sfa_t + 4 * c, sad + ((c * kAtomBytes) >> 4));
-#pragma unroll
-              for (int g = 0; g < G; ++g)
-                if (g < groups)
-                  tc_cp_sf(sfb_t + 4 * (c * G + g), sbd + ((g * kSfaStage + c * kAtomBytes) >> 4));
-            }
-          }
-          const uint64_t ad = adesc0 + ((stage * kAStage) >> 4);
-          const uint64_t bd = bdesc0 + ((stage * kBStage) >> 4);
-#pragma unroll
-          for (int j = 0; j < kMmasPerStage; ++j) {
-            if (j < nmma) {
+            for (int j = 0; j < kMmasPerStage; ++j) {
               const int c = j / KT::kMmasPerChunk;
               const uint32_t sf_id = static_cast<uint32_t>((j % KT::kMmasPerChunk) * KT::kSfIdStep);
               tc_mma(KIND, d_tmem, ad + ((j * kMmaKBytes) >> 4), bd + ((j * kMmaKBytes) >> 4),
-                     p.idesc | (sf_id << 29) | (sf_id << 4), sfa_t + 4 * c, sfb_t + 4 * G * c,
-                     (ks | j) != 0 ? 1u : 0u);
+                     idesc | (sf_id << 29) | (sf_id << 4), sfa_t + 4 * c, sfb_t + 4 * G * c,
+                     (j != 0 || ks != 0) ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < kMmasPerStage; ++j) {
+              if (j < last_nmma) {
+                const int c = j / KT::kMmasPerChunk;
+                const uint32_t sf_id = static_cast<uint32_t>((j % KT::kMmasPerChunk) * KT::kSfIdStep);
+                tc_mma(KIND, d_tmem, ad + ((j * kMmaKBytes) >> 4), bd + ((j * kMmaKBytes) >> 4),
+                       idesc | (sf_id << 29) | (sf_id << 4), sfa_t + 4 * c, sfb_t + 4 * G * c,
+                       (j != 0 || ks != 0) ? 1u : 0u);
+              }
             }
           }
-          tc_commit(empty0 + 8u * stage);  // frees the smem stage once these MMAs finish
-          if (++stage == S) { stage = 0; phase ^= 1u; }
+          // frees the smem stage (in every CTA of the cluster) once these MMAs finish
+          if (CM == 1) tc_commit(empty0 + 8u * stage);
+          else tc_commit_mc(empty0 + 8u * stage, kMask);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+            ad = adesc0;
+            bd = bdesc0;
+            sfa_t = sf_t0;
+          } else {
+            ad += kAStage >> 4;
+            bd += kBStage >> 4;
+            sfa_t += kSfCols;
+          }
         }
         if (!ok) break;
         tc_commit(accf0 + 8u * acc);  // accumulator ready for the epilogue
         if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1u; }
       }
-      // drain: all MMAs and copies issued by this thread complete before exit
+      // drain: all MMAs issued by this thread complete before exit
       tc_commit(drain_bar);
       drain_wait(drain_bar, 0, p, 11u);
     }
-  } else {
+  } else if (warp >= kSfWarp0 && warp < kSfWarp0 + 4) {
+    // --------------------------------------------------------- scale warps
+    // Per stage, once its bytes have landed, lane i of warp q = w % 4 moves
+    // row i of every scale atom of the stage (16 bytes: rows i, 32+i, 64+i,
+    // 96+i of a 128-row group, 4 K-blocks each) into tensor-memory lane
+    // 32q + i of the stage's scale columns, which gives each lane quarter the
+    // atom layout the block-scaled MMA reads.  Scale copies thus never sit in
+    // the MMA thread's issue stream.
+    const int q = warp & 3;
+    int stage = 0;
+    uint32_t phase = 0;
+    const uint32_t lane_off = static_cast<uint32_t>(lane) * 16u;
+    const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16) + kSfCol0;
+    bool ok = true;
+    for (int u = unit0; u < p.num_units && ok; u += unit_step) {
+      for (int ks = 0; ks < p.k_stages; ++ks) {
+        // one lane polls the barrier (the scales gate the MMAs: no sleeping);
+        // then every lane observes the completed phase itself before reading
+        // the bytes
+        int landed = 1;
+        if (lane == 0) landed = BSG_WAIT(full0 + 8u * stage, phase, 5) ? 1 : 0;
+        if (!__shfl_sync(0xFFFFFFFFu, landed, 0)) { ok = false; break; }
+        mbar_try_wait(full0 + 8u * stage, phase);
+        const uint8_t* sa = smem + p.smem_sfa + stage * kSfaStage + lane_off;
+        const uint8_t* sb = smem + p.smem_sfb + stage * kSfbStage + lane_off;
+        const uint32_t tcol = t_row + stage * kSfCols;
+#pragma unroll
+        for (int c = 0; c < KT::kChunks; ++c) {
+          tc_st_32x32b_x4(tcol + 4 * c, *reinterpret_cast<const uint4*>(sa + c * kAtomBytes));
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+            tc_st_32x32b_x4(tcol + 4 * KT::kChunks + 4 * (c * G + g),
+                            *reinterpret_cast<const uint4*>(sb + g * kSfaStage + c * kAtomBytes));
+        }
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sfr0 + 8u * stage);
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+      }
+    }
+  } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // tensor-memory lane quarter this warp may read
+    // Warp w reads lane quarter q = w % 4 and column half h of the tile (one
+    // row per thread, TILE_N/2 columns).  16-bit C: each 16-column chunk is
+    // rounded and packed as it leaves tensor memory, the accumulator is
+    // released after the last chunk, and the stores overlap the next tile's
+    // MMAs.  fp32 C: two passes of TILE_N/4 columns, released after the
+    // second pass's loads.
+    constexpr int kCols = TILE_N / 2;
+    const int q = warp & 3;
+    const int h = (warp - kEpiWarp0) >> 2;
     uint32_t vmax = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-      const Tile tc = tile_coords(p, t);
+    for (int u = unit0; u < p.num_units; u += unit_step) {
+      const Tile tc = tile_coords(p, u, CM, crank);
       // one lane waits, the warp follows its verdict (tcgen05.ld is warp-collective)
       int ready = 0;
-      if (lane == 0) ready = BSG_WAIT(accf0 + 8u * acc, acc_phase, 4) ? 1 : 0;
+      if (lane == 0) ready = BSG_WAIT_SLEEP(accf0 + 8u * acc, acc_phase, 4) ? 1 : 0;
       ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
       if (!ready) break;
       tc_fence_after();
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * TILE_N + h * kCols;
       const int row = tc.mt * kTileM + q * 32 + lane;
       const bool row_ok = row < p.M;
       const size_t batch_off = static_cast<size_t>(tc.l) * p.M * p.N;
-#pragma unroll 1
-      for (int cc = 0; cc < TILE_N; cc += 32) {
-        uint32_t r[32];
-        tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * TILE_N + cc, r);
-        const int n0 = tc.nt * TILE_N + cc;
-        if (p.c_major == 0) {
-          // n-major: this thread owns 32 consecutive elements of row `row`
-          if (p.c_dtype == BSG_F32) {
-            float* dst = static_cast<float*>(p.c) + batch_off + static_cast<size_t>(row) * p.N + n0;
+      const int n0 = tc.nt * TILE_N + h * kCols;
+      const uint32_t release_bar = acce0 + 8u * acc;
+      if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1u; }
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(release_bar);
+      };
+      if (p.c_dtype != BSG_F32) {
+        const bool bf = p.c_dtype == BSG_BF16;
+        uint32_t pk[kCols / 2];  // two rounded 16-bit values per register
+        uint32_t rb[2][16];      // chunk c converts while chunk c + 1 loads
+        tc_ld_32x32b_x16(taddr, rb[0]);
+        tc_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              if (row_ok && n0 + i < p.N) {
+        for (int cc = 0; cc < kCols; cc += 16) {
+          uint32_t* r = rb[(cc / 16) & 1];
+          if (cc + 16 < kCols) tc_ld_32x32b_x16(taddr + cc + 16, rb[((cc / 16) + 1) & 1]);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float f0 = __uint_as_float(r[2 * j]), f1 = __uint_as_float(r[2 * j + 1]);
+            uint32_t h0, h1, b0, b1;
+            if (bf) {
+              h0 = __bfloat16_as_ushort(__float2bfloat16_rn(f0));
+              h1 = __bfloat16_as_ushort(__float2bfloat16_rn(f1));
+              b0 = (h0 << 16) & 0x7FFFFFFFu;
+              b1 = (h1 << 16) & 0x7FFFFFFFu;
+            } else {
+              const __half x0 = __float2half_rn(f0), x1 = __float2half_rn(f1);
+              h0 = __half_as_ushort(x0);
+              h1 = __half_as_ushort(x1);
+              b0 = abs_bits_f32(__half2float(x0));
+              b1 = abs_bits_f32(__half2float(x1));
+            }
+            // only stored elements count toward Amax
+            const int n = n0 + cc + 2 * j;
+            if (row_ok && n < p.N) vmax = max(vmax, b0);
+            if (row_ok && n + 1 < p.N) vmax = max(vmax, b1);
+            pk[cc / 2 + j] = h0 | (h1 << 16);
+          }
+          tc_wait_ld();
+        }
+        release();
+        uint16_t* const cbase = static_cast<uint16_t*>(p.c) + batch_off;
+        if (p.c_major == 0) {
+          uint16_t* dst = cbase + static_cast<size_t>(row) * p.N + n0;
+#pragma unroll
+          for (int i = 0; i < kCols; i += 8)
+            if (row_ok && n0 + i < p.N)
+              *reinterpret_cast<uint4*>(dst + i) =
+                  make_uint4(pk[i / 2], pk[i / 2 + 1], pk[i / 2 + 2], pk[i / 2 + 3]);
+        } else {
+          // m-major: column by column, the 32 lanes write 32 consecutive rows
+          uint16_t* dst = cbase + static_cast<size_t>(n0) * p.M + row;
+          const int ncols = row_ok ? min(kCols, p.N - n0) : 0;
+#pragma unroll
+          for (int j = 0; j < kCols; ++j) {
+            if (j < ncols)
+              *dst = static_cast<uint16_t>((j & 1) ? (pk[j / 2] >> 16) : (pk[j / 2] & 0xFFFFu));
+            dst += p.M;
+          }
+        }
+      } else {
+        float* const cbase = static_cast<float*>(p.c) + batch_off;
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+          constexpr int kHalf = kCols / 2;
+          uint32_t r[kHalf];
+#pragma unroll
+          for (int cc = 0; cc < kHalf; cc += 32) tc_ld_32x32b_x32(taddr + pass * kHalf + cc, r + cc);
+          tc_wait_ld();
+          if (pass == 1) release();
+          const int nb = n0 + pass * kHalf;
+          if (p.c_major == 0) {
+            float* dst = cbase + static_cast<size_t>(row) * p.N + nb;
+#pragma unroll
+            for (int i = 0; i < kHalf; i += 4) {
+              if (row_ok && nb + i < p.N) {
                 float4 v = make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
                                        __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
                 vmax = max(vmax, max(max(abs_bits_f32(v.x), abs_bits_f32(v.y)),
@@ -510,64 +731,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           } else {
-            uint16_t* dst =
-                static_cast<uint16_t*>(p.c) + batch_off + static_cast<size_t>(row) * p.N + n0;
+            float* dst = cbase + static_cast<size_t>(nb) * p.M + row;
+            const int ncols = row_ok ? min(kHalf, p.N - nb) : 0;
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              if (row_ok && n0 + i < p.N) {
-                uint32_t w[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  const float f0 = __uint_as_float(r[i + 2 * j]);
-                  const float f1 = __uint_as_float(r[i + 2 * j + 1]);
-                  uint32_t h0, h1, b0, b1;
-                  if (p.c_dtype == BSG_BF16) {
-                    h0 = __bfloat16_as_ushort(__float2bfloat16_rn(f0));
-                    h1 = __bfloat16_as_ushort(__float2bfloat16_rn(f1));
-                    b0 = (h0 << 16) & 0x7FFFFFFFu;
-                    b1 = (h1 << 16) & 0x7FFFFFFFu;
-                  } else {
-                    const __half x0 = __float2half_rn(f0), x1 = __float2half_rn(f1);
-                    h0 = __half_as_ushort(x0);
-                    h1 = __half_as_ushort(x1);
-                    b0 = abs_bits_f32(__half2float(x0));
-                    b1 = abs_bits_f32(__half2float(x1));
-                  }
-                  vmax = max(vmax, max(b0, b1));
-                  w[j] = h0 | (h1 << 16);
-                }
-                *reinterpret_cast<uint4*>(dst + i) = make_uint4(w[0], w[1], w[2], w[3]);
-              }
-            }
-          }
-        } else {
-          // m-major: for each column the 32 lanes write 32 consecutive rows
-          const size_t colstride = static_cast<size_t>(p.M);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (row_ok && n0 + j < p.N) {
-              const size_t idx = batch_off + static_cast<size_t>(n0 + j) * colstride + row;
-              const float f = __uint_as_float(r[j]);
-              if (p.c_dtype == BSG_F32) {
-                static_cast<float*>(p.c)[idx] = f;
+            for (int j = 0; j < kHalf; ++j) {
+              if (j < ncols) {
+                const float f = __uint_as_float(r[j]);
+                *dst = f;
                 vmax = max(vmax, abs_bits_f32(f));
-              } else if (p.c_dtype == BSG_BF16) {
-                const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(f));
-                static_cast<uint16_t*>(p.c)[idx] = static_cast<uint16_t>(h);
-                vmax = max(vmax, (h << 16) & 0x7FFFFFFFu);
-              } else {
-                const __half x = __float2half_rn(f);
-                static_cast<uint16_t*>(p.c)[idx] = __half_as_ushort(x);
-                vmax = max(vmax, abs_bits_f32(__half2float(x)));
               }
+              dst += p.M;
             }
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acce0 + 8u * acc);
-      if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1u; }
     }
     vmax = __reduce_max_sync(0xFFFFFFFFu, vmax);
     if (lane == 0) atomicMax(cta_amax, vmax);
@@ -575,6 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (CM > 1) cluster_sync();  // no peer multicasts or arrives into this CTA any more
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
@@ -597,26 +775,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 #undef BSG_WAIT
+#undef BSG_WAIT_SLEEP
 
-// Kernel variants: MMA kind x (TILE_N, accumulator buffers in tensor memory)
+// Kernel variants: MMA kind x (TILE_N, accumulator buffers) x cluster size along M
 struct Variant {
-  int kind, tile_n, num_acc;
+  int kind, tile_n, num_acc, cm;
   const void* fn;
 };
 
-template <int KIND, int TN, int NACC>
+template <int KIND, int TN, int NACC, int CM>
 Variant make_variant() {
-  return Variant{KIND, TN, NACC, reinterpret_cast<const void*>(&bsg_gemm_amax_kernel<KIND, TN, NACC>)};
+  return Variant{KIND, TN, NACC, CM,
+                 reinterpret_cast<const void*>(&bsg_gemm_amax_kernel<KIND, TN, NACC, CM>)};
 }
 
-const Variant* find_variant(int kind, int tile_n, int num_acc) {
+const Variant* find_variant(int kind, int tile_n, int num_acc, int cm) {
   static const Variant table[] = {
-      make_variant<kKindF8F6F4, 128, 2>(), make_variant<kKindF8F6F4, 256, 1>(),
-      make_variant<kKindF4x4X, 128, 2>(),  make_variant<kKindF4x4X, 256, 1>(),
-      make_variant<kKindF4x2X, 128, 2>(),  make_variant<kKindF4x2X, 256, 1>(),
+      make_variant<kKindF8F6F4, 128, 2, 1>(), make_variant<kKindF8F6F4, 256, 1, 1>(),
+      make_variant<kKindF8F6F4, 256, 1, 2>(), make_variant<kKindF8F6F4, 256, 1, 4>(),
+      make_variant<kKindF4x4X, 128, 2, 1>(),  make_variant<kKindF4x4X, 256, 1, 1>(),
+      make_variant<kKindF4x4X, 256, 1, 2>(),  make_variant<kKindF4x4X, 256, 1, 4>(),
+      make_variant<kKindF4x2X, 128, 2, 1>(),  make_variant<kKindF4x2X, 256, 1, 1>(),
+      make_variant<kKindF4x2X, 256, 1, 2>(),  make_variant<kKindF4x2X, 256, 1, 4>(),
   };
   for (const Variant& v : table)
-    if (v.kind == kind && v.tile_n == tile_n && v.num_acc == num_acc) return &v;
+    if (v.kind == kind && v.tile_n == tile_n && v.num_acc == num_acc && v.cm == cm) return &v;
   return nullptr;
 }
 
@@ -657,6 +840,7 @@ struct bsg_plan {
   const void* kernel;    // the chosen kernel variant
   int kind;
   int num_acc;
+  int cluster_m;         // CTAs per cluster along M sharing (multicasting) the B tile
   int grid;
   int smem_bytes;
   // tensor maps for the last A/B pointers seen
@@ -759,14 +943,20 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   // hint of 128 (or N <= 128) keeps the double-buffered 128 x 128 variant
   k.tile_n = prob->tile_n == 128 || (prob->tile_n == 0 && prob->N <= 128) ? 128 : 256;
   const int num_acc = k.tile_n == 256 ? 1 : 2;
-  const Variant* var = find_variant(kind, k.tile_n, num_acc);
+  // clusters along M multicast the 256-row B tile; the 128-wide variant runs alone
+  int cm = k.tile_n == 256 && prob->cluster_m > 1 ? prob->cluster_m : 1;
+  k.tiles_m = static_cast<int>(cdiv(prob->M, kTileM));
+  if (cm > k.tiles_m) cm = k.tiles_m >= 2 ? 2 : 1;
+  const Variant* var = find_variant(kind, k.tile_n, num_acc, cm);
   if (!var) { delete plan; return BSG_ERR_UNSUPPORTED; }
   plan->kernel = var->fn;
   plan->kind = kind;
   plan->num_acc = num_acc;
-  k.tiles_m = static_cast<int>(cdiv(prob->M, kTileM));
+  plan->cluster_m = cm;
   k.tiles_n = static_cast<int>(cdiv(prob->N, k.tile_n));
   k.num_tiles = k.tiles_m * k.tiles_n * k.L;
+  k.tiles_mc = static_cast<int>(cdiv(k.tiles_m, cm));
+  k.num_units = k.tiles_mc * k.tiles_n * k.L;
   k.k_bytes = static_cast<int>(fp4 ? prob->K / 2 : prob->K);
   k.k_stages = static_cast<int>(cdiv(k.k_bytes, kStageKBytes));
   k.t_m = static_cast<int>(cdiv(prob->M, 128));
@@ -802,13 +992,13 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   k.smem_sfa = k.smem_b + stages * k.tile_n * kStageKBytes;
   k.smem_sfb = k.smem_sfa + stages * sfa_stage;
   k.smem_bar = k.smem_sfb + stages * sfb_stage;
-  plan->smem_bytes = static_cast<int>(k.smem_bar) + 16 * stages + 16 * num_acc + 8 + 16 + 1024;
+  plan->smem_bytes = static_cast<int>(k.smem_bar) + 24 * stages + 16 * num_acc + 8 + 16 + 1024;
   k.wait_limit_ns = 1000000000ull;  // one second per wait
   if (const char* e = std::getenv("BSG_WAIT_LIMIT_NS")) {
     const unsigned long long v = std::strtoull(e, nullptr, 10);
     if (v > 0) k.wait_limit_ns = v;
   }
-  plan->grid = k.num_tiles < sms ? k.num_tiles : sms;
+  plan->grid = k.num_units < sms ? k.num_units : sms;
 
   int prev = 0;
   cudaGetDevice(&prev);
@@ -822,12 +1012,37 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
     delete plan;
     return BSG_ERR_CUDA;
   }
+  if (cm > 1) {
+    // persistent clusters: as many as can be resident at once
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cm;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(cm * (sms / cm));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = plan->smem_bytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int max_clusters = 0;
+    if (prev != device) cudaSetDevice(device);
+    const cudaError_t oe = cudaOccupancyMaxActiveClusters(&max_clusters, plan->kernel, &cfg);
+    if (prev != device) cudaSetDevice(prev);
+    if (oe != cudaSuccess || max_clusters < 1) {
+      cudaGetLastError();
+      delete plan;
+      return BSG_ERR_CUDA;
+    }
+    const int clusters = k.num_units < max_clusters ? k.num_units : max_clusters;
+    plan->grid = cm * clusters;
+  }
   if (std::getenv("BSG_LOG"))
     std::fprintf(stderr,
                  "[bsgemm] M=%lld N=%lld K=%lld L=%lld tile=128x%d stages=%d grid=%d smem=%d "
-                 "kind=%d tiles=%d\n",
+                 "kind=%d tiles=%d cluster_m=%d\n",
                  (long long)prob->M, (long long)prob->N, (long long)prob->K, (long long)prob->L,
-                 k.tile_n, stages, plan->grid, plan->smem_bytes, kind, k.num_tiles);
+                 k.tile_n, stages, plan->grid, plan->smem_bytes, kind, k.num_tiles, cm);
   *out = plan;
   return BSG_OK;
 }
@@ -894,7 +1109,7 @@ bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const vo
       plan->map_a_ptr = A;
     }
     if (plan->map_b_ptr != B) {
-      if (!encode_operand(&plan->map_b, B, row_bytes, pr.N, pr.L, k.tile_n)) {
+      if (!encode_operand(&plan->map_b, B, row_bytes, pr.N, pr.L, k.tile_n / plan->cluster_m)) {
         plan->map_b_ptr = nullptr;
         return BSG_ERR_CUDA;
       }
@@ -904,9 +1119,21 @@ bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const vo
     mb = plan->map_b;
   }
   void* args[3] = {&ma, &mb, &k};
-  if (cudaLaunchKernel(plan->kernel, dim3(plan->grid), dim3(kThreads), args,
-                       static_cast<size_t>(plan->smem_bytes),
-                       static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(plan->grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(plan->smem_bytes);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  if (plan->cluster_m > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = plan->cluster_m;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  if (cudaLaunchKernelExC(&cfg, plan->kernel, args) != cudaSuccess) {
     cudaGetLastError();
     return BSG_ERR_CUDA;
   }
@@ -1038,6 +1265,7 @@ bsg_status bsg_plan_describe(const bsg_plan* plan, bsg_plan_info* info) {
   info->smem_bytes = plan->smem_bytes;
   info->num_tiles = plan->base.num_tiles;
   info->mma_kind = plan->kind;
+  info->cluster_m = plan->cluster_m;
   std::snprintf(info->kernel_name, sizeof(info->kernel_name), "bsg_gemm_amax_kernel");
   return BSG_OK;
 }

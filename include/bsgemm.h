@@ -101,7 +101,7 @@ typedef struct {
     int32_t smem_bytes;                    /* dynamic shared memory per CTA */
     int32_t num_tiles;                     /* output tiles per launch */
     int32_t mma_kind;                      /* 0 mxf8f6f4 1X, 1 mxf4nvf4 4X, 2 mxf4nvf4 2X */
-    int32_t reserved;
+    int32_t cluster_m;                     /* CTAs per cluster sharing one B tile */
     char kernel_name[64];
 } bsg_plan_info;
 

@@ -244,3 +244,24 @@ def test_tile_variants(p, tile_n):
     assert op.describe()["tile_n"] == tile_n
     assert guard_ok
     assert_parity(inp, c, amax)
+
+
+CLUSTER_CASES = [
+    P(640, 512, 512), P(200, 520, 160, 2, c="bf16"), P(392, 1000, 96, major="m"),
+    P(260, 384, 640, a="e2m1", b="e2m1", sfv=16, c="bf16"),
+    P(132, 392, 384, 2, a="e2m1", b="e2m1", sfv=32, major="m"),
+    P(1000, 264, 256, 3, a="e5m2", b="e4m3"),
+]
+
+
+@pytest.mark.parametrize("cluster_m", [2, 4])
+@pytest.mark.parametrize("p", CLUSTER_CASES, ids=[f"{p.M}x{p.N}x{p.K}L{p.L}{p.a_dtype}sfv{p.sfv}{p.c_major}" for p in CLUSTER_CASES])
+def test_cluster_multicast(p, cluster_m):
+    """Clusters of 2 or 4 CTAs along M share each B tile by TMA multicast;
+    M-tile counts that do not divide by the cluster give ghost tiles."""
+    inp = synth.uniform_codes(p, p.M * 3 + p.N + p.K + cluster_m, 123, 131)
+    c, amax, _, op, guard_ok = run_gpu(inp, guard=4096, tile_n=256, cluster_m=cluster_m)
+    info = op.describe()
+    assert info["tile_n"] == 256 and info["cluster_m"] >= 1
+    assert guard_ok
+    assert_parity(inp, c, amax)
