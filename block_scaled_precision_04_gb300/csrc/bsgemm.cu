@@ -191,6 +191,72 @@ __device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
 }
 
 
+// cta_group::2 forms: issued by the leader CTA of a pair, acting on both CTAs
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier anywhere in the cluster (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void tc_mma_pair(int kind, uint32_t d, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                            uint32_t accumulate) {
+  if (kind == kKindF8F6F4) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+        " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        : "memory");
+  } else if (kind == kKindF4x4X) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::2X"
+        " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        : "memory");
+  }
+}
+
 __device__ __forceinline__ void tc_mma(int kind, uint32_t d, uint64_t adesc, uint64_t bdesc,
                                        uint32_t idesc, uint32_t sfa, uint32_t sfb,
                                        uint32_t accumulate) {
@@ -357,6 +423,11 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Para
 // Fast path inline: one try_wait; the bounded loop only when the phase is open.
 #define BSG_WAIT(bar, parity, site) \
   (mbar_try_wait((bar), (parity)) || wait_slow((bar), (parity), p, abort_flag, (site), true))
+// Cluster-scope acquire for barriers that receive arrivals from the peer CTA.
+#define BSG_WAIT_CL(bar, parity, site)                                                 \
+  (mbar_try_wait_cluster((bar), (parity)) ||                                           \
+   (wait_slow((bar), (parity), p, abort_flag, (site), true) &&                         \
+    mbar_try_wait_cluster((bar), (parity))))
 #define BSG_WAIT_SLEEP(bar, parity, site) \
   (mbar_try_wait((bar), (parity)) || wait_slow((bar), (parity), p, abort_flag, (site), false))
 
@@ -377,14 +448,18 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 
 // --------------------------------------------------------------- kernel
 
-template <int KIND, int TILE_N, int NUM_ACC, int CM>
+template <int KIND, int TILE_N, int NUM_ACC, int CM, int PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     bsg_gemm_amax_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ Params p) {
   using KT = KindTraits<KIND>;
   constexpr int G = TILE_N / 128;                       // 128-row scale groups of B per tile
   constexpr uint32_t kAStage = kTileM * kStageKBytes;   // smem bytes per stage
-  constexpr uint32_t kBStage = TILE_N * kStageKBytes;
+  // PAIR: a 2-CTA pair runs 256 x TILE_N MMAs (cta_group::2); each CTA holds
+  // its 128 rows of A and half (TILE_N/2 rows) of the B tile
+  static_assert(!PAIR || CM == 2, "a CTA pair is a cluster of two");
+  constexpr int kBRows = PAIR ? TILE_N / 2 : TILE_N;
+  constexpr uint32_t kBStage = kBRows * kStageKBytes;
   constexpr uint32_t kSfaStage = KT::kChunks * kAtomBytes;
   constexpr uint32_t kSfbStage = KT::kChunks * kAtomBytes * G;
   // scale columns follow the accumulators, one set per smem stage, so that a
@@ -394,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kMmasPerStage = kStageKBytes / kMmaKBytes;
   // B tile shared by the cluster's CM CTAs: each loads TILE_N / CM rows and
   // multicasts them to all
-  constexpr int kBPartRows = TILE_N / CM;
+  constexpr int kBPartRows = PAIR ? kBRows : TILE_N / CM;
   constexpr uint32_t kBPart = kBPartRows * kStageKBytes;
   constexpr uint16_t kMask = static_cast<uint16_t>((1u << CM) - 1u);
 
@@ -424,12 +499,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8u * s, 1);
-      mbar_init(empty0 + 8u * s, CM);  // every CTA's MMA commit frees the stage
-      mbar_init(sfr0 + 8u * s, 4);     // the four scale warps: scales in tensor memory
+      // freed by the MMA commit of every CTA of a multicast cluster, or by the
+      // single (multicast) commit of a pair's leader
+      mbar_init(empty0 + 8u * s, PAIR ? 1 : CM);
+      // the four scale warps (of both CTAs of a pair): scales in tensor memory
+      mbar_init(sfr0 + 8u * s, PAIR ? 8 : 4);
     }
     for (int b = 0; b < NUM_ACC; ++b) {
       mbar_init(accf0 + 8u * b, 1);
-      mbar_init(acce0 + 8u * b, kEpiWarps);  // one arrival per epilogue warp
+      mbar_init(acce0 + 8u * b, PAIR ? 2 * kEpiWarps : kEpiWarps);  // one per epilogue warp
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0u;
@@ -442,11 +520,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(tmem_holder)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if (PAIR) {  // one warp of each CTA of the pair allocates collectively
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_holder)),
+                   "r"(kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_holder)),
+                   "r"(kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -488,6 +574,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(a_dst0 + stage * kAStage, &tmap_a, ks * kStageKBytes, m0, tc.l, fb);
           if (CM == 1)
             tma_load_3d(b_dst0 + stage * kBStage, &tmap_b, ks * kStageKBytes, n0, tc.l, fb);
+          else if (PAIR)
+            tma_load_3d(b_dst0 + stage * kBStage, &tmap_b, ks * kStageKBytes, n0 + crank * kBRows,
+                        tc.l, fb);
           else
             tma_load_3d_mc(b_dst0 + stage * kBStage + crank * kBPart, &tmap_b, ks * kStageKBytes,
                            n0 + crank * kBPartRows, tc.l, fb, kMask);
@@ -507,7 +596,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
-    if (lane == 0) {
+    // (in a CTA pair only the leader issues, for both CTAs)
+    if (lane == 0 && (!PAIR || crank == 0)) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -519,6 +609,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t bdesc0 = desc_sw128(base + p.smem_b);
       const uint32_t sf_t0 = tmem + kSfCol0;
       const uint32_t idesc = p.idesc;
+      auto mma_issue = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t sa,
+                           uint32_t sb, uint32_t accumulate) {
+        if (PAIR) tc_mma_pair(KIND, d, a, b, id, sa, sb, accumulate);
+        else tc_mma(KIND, d, a, b, id, sa, sb, accumulate);
+      };
       // running addresses of the current stage
       uint64_t ad = adesc0, bd = bdesc0;
       uint32_t sfa_t = sf_t0;
@@ -526,12 +621,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       int last_nmma = (p.k_bytes - last * kStageKBytes + kMmaKBytes - 1) / kMmaKBytes;
       if (last_nmma > kMmasPerStage) last_nmma = kMmasPerStage;
       for (int u = unit0; u < p.num_units && ok; u += unit_step) {
-        if (!BSG_WAIT(acce0 + 8u * acc, acc_phase ^ 1u, 2)) { ok = false; break; }
+        if (!(PAIR ? BSG_WAIT_CL(acce0 + 8u * acc, acc_phase ^ 1u, 2)
+                   : BSG_WAIT(acce0 + 8u * acc, acc_phase ^ 1u, 2))) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * TILE_N;
         for (int ks = 0; ks < p.k_stages; ++ks) {
           // operands in smem and this stage's scales in tensor memory
-          if (!BSG_WAIT(sfr0 + 8u * stage, phase, 3)) { ok = false; break; }
+          if (!(PAIR ? BSG_WAIT_CL(sfr0 + 8u * stage, phase, 3)
+                     : BSG_WAIT(sfr0 + 8u * stage, phase, 3))) { ok = false; break; }
           tc_fence_after();
           const uint32_t sfb_t = sfa_t + 4 * KT::kChunks;
           if (ks != last) {
@@ -539,9 +636,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < kMmasPerStage; ++j) {
               const int c = j / KT::kMmasPerChunk;
               const uint32_t sf_id = static_cast<uint32_t>((j % KT::kMmasPerChunk) * KT::kSfIdStep);
-              tc_mma(KIND, d_tmem, ad + ((j * kMmaKBytes) >> 4), bd + ((j * kMmaKBytes) >> 4),
-                     idesc | (sf_id << 29) | (sf_id << 4), sfa_t + 4 * c, sfb_t + 4 * G * c,
-                     (j != 0 || ks != 0) ? 1u : 0u);
+              mma_issue(d_tmem, ad + ((j * kMmaKBytes) >> 4), bd + ((j * kMmaKBytes) >> 4),
+                        idesc | (sf_id << 29) | (sf_id << 4), sfa_t + 4 * c, sfb_t + 4 * G * c,
+                        (j != 0 || ks != 0) ? 1u : 0u);
             }
           } else {
 #pragma unroll
@@ -549,14 +646,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (j < last_nmma) {
                 const int c = j / KT::kMmasPerChunk;
                 const uint32_t sf_id = static_cast<uint32_t>((j % KT::kMmasPerChunk) * KT::kSfIdStep);
-                tc_mma(KIND, d_tmem, ad + ((j * kMmaKBytes) >> 4), bd + ((j * kMmaKBytes) >> 4),
-                       idesc | (sf_id << 29) | (sf_id << 4), sfa_t + 4 * c, sfb_t + 4 * G * c,
-                       (j != 0 || ks != 0) ? 1u : 0u);
+                mma_issue(d_tmem, ad + ((j * kMmaKBytes) >> 4), bd + ((j * kMmaKBytes) >> 4),
+                          idesc | (sf_id << 29) | (sf_id << 4), sfa_t + 4 * c, sfb_t + 4 * G * c,
+                          (j != 0 || ks != 0) ? 1u : 0u);
               }
             }
           }
           // frees the smem stage (in every CTA of the cluster) once these MMAs finish
-          if (CM == 1) tc_commit(empty0 + 8u * stage);
+          if (PAIR) tc_commit_pair_mc(empty0 + 8u * stage, kMask);
+          else if (CM == 1) tc_commit(empty0 + 8u * stage);
           else tc_commit_mc(empty0 + 8u * stage, kMask);
           if (++stage == S) {
             stage = 0;
@@ -571,11 +669,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        tc_commit(accf0 + 8u * acc);  // accumulator ready for the epilogue
+        // accumulator ready for the epilogue (of both CTAs of a pair)
+        if (PAIR) tc_commit_pair_mc(accf0 + 8u * acc, kMask);
+        else tc_commit(accf0 + 8u * acc);
         if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1u; }
       }
       // drain: all MMAs issued by this thread complete before exit
-      tc_commit(drain_bar);
+      if (PAIR) tc_commit_pair(drain_bar);
+      else tc_commit(drain_bar);
       drain_wait(drain_bar, 0, p, 11u);
     }
   } else if (warp >= kSfWarp0 && warp < kSfWarp0 + 4) {
@@ -615,7 +716,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(sfr0 + 8u * stage);
+        if (lane == 0) {
+          if (PAIR) mbar_arrive_cluster(mapa_shared(sfr0 + 8u * stage, 0));
+          else mbar_arrive(sfr0 + 8u * stage);
+        }
         if (++stage == S) { stage = 0; phase ^= 1u; }
       }
     }
@@ -651,7 +755,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto release = [&]() {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(release_bar);
+        if (lane == 0) {
+          if (PAIR) mbar_arrive_cluster(mapa_shared(release_bar, 0));
+          else mbar_arrive(release_bar);
+        }
       };
       if (p.c_dtype != BSG_F32) {
         const bool bf = p.c_dtype == BSG_BF16;
@@ -756,9 +863,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(kTmemCols)
-                 : "memory");
+    if (PAIR)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                   "r"(kTmemCols)
+                   : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                   "r"(kTmemCols)
+                   : "memory");
   }
   if (threadIdx.x == 0) {
     // global Amax: max over CTAs, written by the last CTA to arrive, which
@@ -776,30 +888,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 #undef BSG_WAIT
 #undef BSG_WAIT_SLEEP
+#undef BSG_WAIT_CL
 
-// Kernel variants: MMA kind x (TILE_N, accumulator buffers) x cluster size along M
+// Kernel variants: MMA kind x (TILE_N, accumulator buffers) x cluster along M
+// (cm 1 alone, 2 a cta_group::2 pair, 4 a quad multicasting the B tile)
 struct Variant {
-  int kind, tile_n, num_acc, cm;
+  int kind, tile_n, num_acc, cm, pair;
   const void* fn;
 };
 
-template <int KIND, int TN, int NACC, int CM>
+template <int KIND, int TN, int NACC, int CM, int PAIR>
 Variant make_variant() {
-  return Variant{KIND, TN, NACC, CM,
-                 reinterpret_cast<const void*>(&bsg_gemm_amax_kernel<KIND, TN, NACC, CM>)};
+  return Variant{KIND, TN, NACC, CM, PAIR,
+                 reinterpret_cast<const void*>(&bsg_gemm_amax_kernel<KIND, TN, NACC, CM, PAIR>)};
+}
+
+template <int KIND>
+void add_kind(Variant* out, int& n) {
+  out[n++] = make_variant<KIND, 128, 2, 1, 0>();
+  out[n++] = make_variant<KIND, 256, 1, 1, 0>();
+  out[n++] = make_variant<KIND, 256, 1, 2, 1>();
+  out[n++] = make_variant<KIND, 256, 1, 4, 0>();
 }
 
 const Variant* find_variant(int kind, int tile_n, int num_acc, int cm) {
-  static const Variant table[] = {
-      make_variant<kKindF8F6F4, 128, 2, 1>(), make_variant<kKindF8F6F4, 256, 1, 1>(),
-      make_variant<kKindF8F6F4, 256, 1, 2>(), make_variant<kKindF8F6F4, 256, 1, 4>(),
-      make_variant<kKindF4x4X, 128, 2, 1>(),  make_variant<kKindF4x4X, 256, 1, 1>(),
-      make_variant<kKindF4x4X, 256, 1, 2>(),  make_variant<kKindF4x4X, 256, 1, 4>(),
-      make_variant<kKindF4x2X, 128, 2, 1>(),  make_variant<kKindF4x2X, 256, 1, 1>(),
-      make_variant<kKindF4x2X, 256, 1, 2>(),  make_variant<kKindF4x2X, 256, 1, 4>(),
-  };
-  for (const Variant& v : table)
+  static Variant table[12];
+  static int n = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    add_kind<kKindF8F6F4>(table, n);
+    add_kind<kKindF4x4X>(table, n);
+    add_kind<kKindF4x2X>(table, n);
+  });
+  for (int i = 0; i < n; ++i) {
+    const Variant& v = table[i];
     if (v.kind == kind && v.tile_n == tile_n && v.num_acc == num_acc && v.cm == cm) return &v;
+  }
   return nullptr;
 }
 
@@ -840,7 +964,8 @@ struct bsg_plan {
   const void* kernel;    // the chosen kernel variant
   int kind;
   int num_acc;
-  int cluster_m;         // CTAs per cluster along M sharing (multicasting) the B tile
+  int cluster_m;         // CTAs per cluster along M sharing the B tile
+  int pair;              // 1: the cluster is a cta_group::2 pair (256-row MMAs)
   int grid;
   int smem_bytes;
   // tensor maps for the last A/B pointers seen
@@ -953,6 +1078,7 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   plan->kind = kind;
   plan->num_acc = num_acc;
   plan->cluster_m = cm;
+  plan->pair = var->pair;
   k.tiles_n = static_cast<int>(cdiv(prob->N, k.tile_n));
   k.num_tiles = k.tiles_m * k.tiles_n * k.L;
   k.tiles_mc = static_cast<int>(cdiv(k.tiles_m, cm));
@@ -969,14 +1095,16 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
     a_fmt = prob->a_dtype == BSG_E5M2 ? 1 : 0;  // kind::mxf8f6f4: E4M3 0, E5M2 1
     b_fmt = prob->b_dtype == BSG_E5M2 ? 1 : 0;
   }
+  const int mma_m = plan->pair ? 2 * kTileM : kTileM;
   k.idesc = (a_fmt << 7) | (b_fmt << 10) | (static_cast<uint32_t>(k.tile_n >> 3) << 17) |
-            (1u << 23) /* E8M0 scales */ | (static_cast<uint32_t>(kTileM >> 4) << 24);
+            (1u << 23) /* E8M0 scales */ | (static_cast<uint32_t>(mma_m >> 4) << 24);
   k.c_dtype = prob->c_dtype;
   k.c_major = prob->c_major == 'm' ? 1 : 0;
 
   const int G = k.tile_n / 128;
   const int sfa_stage = chunks * kAtomBytes, sfb_stage = chunks * kAtomBytes * G;
-  const int per_stage = kTileM * kStageKBytes + k.tile_n * kStageKBytes + sfa_stage + sfb_stage;
+  const int b_rows = plan->pair ? k.tile_n / 2 : k.tile_n;  // B rows held per CTA
+  const int per_stage = kTileM * kStageKBytes + b_rows * kStageKBytes + sfa_stage + sfb_stage;
   const int reserve = 1024 /* alignment slack */ + 512 /* barriers and flags */;
   int stages = (max_smem - reserve) / per_stage;
   if (stages > 8) stages = 8;
@@ -989,7 +1117,7 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   k.stages = stages;
   k.smem_a = 0;
   k.smem_b = k.smem_a + stages * kTileM * kStageKBytes;
-  k.smem_sfa = k.smem_b + stages * k.tile_n * kStageKBytes;
+  k.smem_sfa = k.smem_b + stages * b_rows * kStageKBytes;
   k.smem_sfb = k.smem_sfa + stages * sfa_stage;
   k.smem_bar = k.smem_sfb + stages * sfb_stage;
   plan->smem_bytes = static_cast<int>(k.smem_bar) + 24 * stages + 16 * num_acc + 8 + 16 + 1024;

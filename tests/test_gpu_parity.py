@@ -251,13 +251,18 @@ CLUSTER_CASES = [
     P(260, 384, 640, a="e2m1", b="e2m1", sfv=16, c="bf16"),
     P(132, 392, 384, 2, a="e2m1", b="e2m1", sfv=32, major="m"),
     P(1000, 264, 256, 3, a="e5m2", b="e4m3"),
+    # more units than resident clusters and more K stages than the smem ring:
+    # the ring and the accumulator hand-off wrap
+    P(2048, 2560, 1024, c="bf16"),
+    P(1536, 2304, 2048, a="e2m1", b="e2m1", sfv=16, c="bf16"),
 ]
 
 
 @pytest.mark.parametrize("cluster_m", [2, 4])
 @pytest.mark.parametrize("p", CLUSTER_CASES, ids=[f"{p.M}x{p.N}x{p.K}L{p.L}{p.a_dtype}sfv{p.sfv}{p.c_major}" for p in CLUSTER_CASES])
 def test_cluster_multicast(p, cluster_m):
-    """Clusters of 2 or 4 CTAs along M share each B tile by TMA multicast;
+    """A cta_group::2 pair (cluster 2: 256-row MMAs, each CTA holding half the
+    B tile) or a cluster of 4 CTAs sharing each B tile by TMA multicast;
     M-tile counts that do not divide by the cluster give ghost tiles."""
     inp = synth.uniform_codes(p, p.M * 3 + p.N + p.K + cluster_m, 123, 131)
     c, amax, _, op, guard_ok = run_gpu(inp, guard=4096, tile_n=256, cluster_m=cluster_m)
