@@ -212,23 +212,11 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   return r;
 }
 
-// Arrive on an mbarrier anywhere in the cluster (release at cluster scope).
+// Arrive on an mbarrier anywhere in the cluster (default semantics).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 
 __device__ __forceinline__ void tc_mma_pair(int kind, uint32_t d, uint64_t adesc, uint64_t bdesc,
                                             uint32_t idesc, uint32_t sfa, uint32_t sfb,
@@ -423,11 +411,6 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Para
 // Fast path inline: one try_wait; the bounded loop only when the phase is open.
 #define BSG_WAIT(bar, parity, site) \
   (mbar_try_wait((bar), (parity)) || wait_slow((bar), (parity), p, abort_flag, (site), true))
-// Cluster-scope acquire for barriers that receive arrivals from the peer CTA.
-#define BSG_WAIT_CL(bar, parity, site)                                                 \
-  (mbar_try_wait_cluster((bar), (parity)) ||                                           \
-   (wait_slow((bar), (parity), p, abort_flag, (site), true) &&                         \
-    mbar_try_wait_cluster((bar), (parity))))
 #define BSG_WAIT_SLEEP(bar, parity, site) \
   (mbar_try_wait((bar), (parity)) || wait_slow((bar), (parity), p, abort_flag, (site), false))
 
@@ -621,14 +604,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int last_nmma = (p.k_bytes - last * kStageKBytes + kMmaKBytes - 1) / kMmaKBytes;
       if (last_nmma > kMmasPerStage) last_nmma = kMmasPerStage;
       for (int u = unit0; u < p.num_units && ok; u += unit_step) {
-        if (!(PAIR ? BSG_WAIT_CL(acce0 + 8u * acc, acc_phase ^ 1u, 2)
-                   : BSG_WAIT(acce0 + 8u * acc, acc_phase ^ 1u, 2))) { ok = false; break; }
+        if (!BSG_WAIT(acce0 + 8u * acc, acc_phase ^ 1u, 2)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * TILE_N;
         for (int ks = 0; ks < p.k_stages; ++ks) {
           // operands in smem and this stage's scales in tensor memory
-          if (!(PAIR ? BSG_WAIT_CL(sfr0 + 8u * stage, phase, 3)
-                     : BSG_WAIT(sfr0 + 8u * stage, phase, 3))) { ok = false; break; }
+          if (!BSG_WAIT(sfr0 + 8u * stage, phase, 3)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sfb_t = sfa_t + 4 * KT::kChunks;
           if (ks != last) {
@@ -888,7 +869,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 #undef BSG_WAIT
 #undef BSG_WAIT_SLEEP
-#undef BSG_WAIT_CL
 
 // Kernel variants: MMA kind x (TILE_N, accumulator buffers) x cluster along M
 // (cm 1 alone, 2 a cta_group::2 pair, 4 a quad multicasting the B tile)
@@ -1068,8 +1048,10 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   // hint of 128 (or N <= 128) keeps the double-buffered 128 x 128 variant
   k.tile_n = prob->tile_n == 128 || (prob->tile_n == 0 && prob->N <= 128) ? 128 : 256;
   const int num_acc = k.tile_n == 256 ? 1 : 2;
-  // clusters along M multicast the 256-row B tile; the 128-wide variant runs alone
-  int cm = k.tile_n == 256 && prob->cluster_m > 1 ? prob->cluster_m : 1;
+  // 256-wide tiles run as cta_group::2 pairs by default (hint 1: single CTAs,
+  // 4: clusters of four multicasting the B tile); the 128-wide variant runs alone
+  int cm = 1;
+  if (k.tile_n == 256) cm = prob->cluster_m == 0 ? 2 : prob->cluster_m;
   k.tiles_m = static_cast<int>(cdiv(prob->M, kTileM));
   if (cm > k.tiles_m) cm = k.tiles_m >= 2 ? 2 : 1;
   const Variant* var = find_variant(kind, k.tile_n, num_acc, cm);

@@ -258,10 +258,11 @@ CLUSTER_CASES = [
 ]
 
 
-@pytest.mark.parametrize("cluster_m", [2, 4])
+@pytest.mark.parametrize("cluster_m", [1, 2, 4])
 @pytest.mark.parametrize("p", CLUSTER_CASES, ids=[f"{p.M}x{p.N}x{p.K}L{p.L}{p.a_dtype}sfv{p.sfv}{p.c_major}" for p in CLUSTER_CASES])
 def test_cluster_multicast(p, cluster_m):
-    """A cta_group::2 pair (cluster 2: 256-row MMAs, each CTA holding half the
+    """Single CTAs (cluster 1), a cta_group::2 pair (cluster 2, the default:
+    256-row MMAs, each CTA holding half the
     B tile) or a cluster of 4 CTAs sharing each B tile by TMA multicast;
     M-tile counts that do not divide by the cluster give ghost tiles."""
     inp = synth.uniform_codes(p, p.M * 3 + p.N + p.K + cluster_m, 123, 131)
