@@ -37,13 +37,32 @@ NOMINAL_RATIO = {"fp8": 4.5 / 2.25, "fp4": 13.5 / 2.25}  # dense tensor peak vs 
 FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM bytes per launch of the GEMM kernel from an ncu capture, keyed by the
 # kernel source it was taken on (sha256 prefix of csrc/bsgemm.cu) and workload.
-TRAFFIC = {}
+TRAFFIC = {
+    ("e53f75cda7bacd9f", 2): 35592192,
+    ("e53f75cda7bacd9f", 3): 405918464,
+    ("e53f75cda7bacd9f", 4): 186805760,
+}
 
 
 def kernel_source_hash() -> str:
     path = os.path.join(ROOT, "block_scaled_precision_04_gb300", "csrc", "bsgemm.cu")
     with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The largest `value` over all ranks (the slowest rank sets the time)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, world: int, total_ms: float) -> float:
+    """Work of every replica (one per rank) over the slowest rank's time."""
+    return world * flops_per_step * steps / (total_ms / 1e3) / 1e12
 
 
 def workload_numbers(p: synth.Problem):
@@ -115,7 +134,7 @@ class ClockSampler:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.file, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
@@ -213,13 +232,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         dist.barrier()
     bsg.check(op.device_status(), "device status")
     times_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
-    total_ms = sum(times_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(times_ms), dist, dev)
     ms = total_ms / args.steps
-    value = world * nums["flops"] * args.steps / (total_ms / 1e3) / 1e12
+    value = whole_job_tflops(nums["flops"], args.steps, world, total_ms)
 
     # end to end through the C ABI with host buffers (pinned), copies included
     e2e = None
@@ -242,11 +257,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             run_host()
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = e0.elapsed_time(e1) / args.steps
-        if dist is not None:
-            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
         e2e = {"value": world * nums["flops"] / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": nums["h2d"],
                "d2h_bytes_per_step": nums["d2h"]}
