@@ -45,12 +45,14 @@ namespace {
 constexpr int kTileM = 128;
 constexpr int kStageKBytes = 128;  // bytes of K per operand row per stage (one swizzle row)
 constexpr int kMmaKBytes = 32;     // bytes of K per tcgen05.mma (32 FP8 or 64 FP4 elements)
-// Warp roles: 0 TMA producer, 1 MMA issuer, 2-5 scale warps (tensor-memory
-// lane quarters 2, 3, 0, 1), 6-13 epilogue (two warps per lane quarter).
+// Warp roles: 0 operand producer (A/B tiles), 1 MMA issuer, 2-5 scale warps
+// (tensor-memory lane quarters 2, 3, 0, 1), 6-13 epilogue (two warps per lane
+// quarter), 14 scale producer (bulk copies of the scale atoms).
 constexpr int kSfWarp0 = 2;
 constexpr int kEpiWarp0 = 6;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+constexpr int kSfProdWarp = kEpiWarp0 + kEpiWarps;
+constexpr int kThreads = 32 * (kSfProdWarp + 1);
 constexpr int kAtomBytes = 512;    // one scale atom: 128 rows x 4 K-blocks
 constexpr uint32_t kTmemCols = 512;
 
@@ -272,20 +274,8 @@ __device__ __forceinline__ void tc_mma(int kind, uint32_t d, uint64_t adesc, uin
   }
 }
 
-// 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base + i).
+// 32 lanes x 16 consecutive 32-bit columns: thread i gets lane (base + i).
 // No wait: follow with tc_wait_ld() before reading r.
-__device__ __forceinline__ void tc_ld_32x32b_x32(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%"
-      "14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-
 __device__ __forceinline__ void tc_ld_32x32b_x16(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%"
@@ -436,7 +426,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     bsg_gemm_amax_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ Params p) {
   using KT = KindTraits<KIND>;
-  constexpr int G = TILE_N / 128;                       // 128-row scale groups of B per tile
+  // 128-row scale groups of B the MMA reads (tile rows 128g .. 128g+127 at
+  // columns +4g); a tile width that is not a multiple of 128 (224) starts at
+  // any multiple of 32 inside a scale atom, so its scales span one atom more
+  constexpr int G = (TILE_N + 127) / 128;
+  constexpr bool kAlignedN = TILE_N % 128 == 0;
+  constexpr int kSfbAtoms = kAlignedN ? G : G + 1;  // B scale atoms per chunk in smem
   constexpr uint32_t kAStage = kTileM * kStageKBytes;   // smem bytes per stage
   // PAIR: a 2-CTA pair runs 256 x TILE_N MMAs (cta_group::2); each CTA holds
   // its 128 rows of A and half (TILE_N/2 rows) of the B tile
@@ -444,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kBRows = PAIR ? TILE_N / 2 : TILE_N;
   constexpr uint32_t kBStage = kBRows * kStageKBytes;
   constexpr uint32_t kSfaStage = KT::kChunks * kAtomBytes;
-  constexpr uint32_t kSfbStage = KT::kChunks * kAtomBytes * G;
+  constexpr uint32_t kSfbStage = KT::kChunks * kAtomBytes * kSfbAtoms;
   // scale columns follow the accumulators, one set per smem stage, so that a
   // stage's tcgen05.cp never rewrites columns an in-flight MMA still reads
   constexpr uint32_t kSfCols = 4 * KT::kChunks * (1 + G);
@@ -470,11 +465,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int unit_step = CM > 1 ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
 
   const uint32_t bar0 = base + p.smem_bar;
+  // per stage: full (A/B bytes landed), empty (stage free), sfr (scales in
+  // tensor memory), sff (scale bytes landed; issued first, off the A/B path)
   const uint32_t full0 = bar0, empty0 = bar0 + 8u * S, sfr0 = bar0 + 16u * S;
-  const uint32_t accf0 = bar0 + 24u * S, acce0 = accf0 + 8u * NUM_ACC;
+  const uint32_t sff0 = bar0 + 24u * S;
+  const uint32_t accf0 = bar0 + 32u * S, acce0 = accf0 + 8u * NUM_ACC;
   const uint32_t drain_bar = acce0 + 8u * NUM_ACC;
   uint32_t* const misc =
-      reinterpret_cast<uint32_t*>(smem + p.smem_bar + 24u * S + 16u * NUM_ACC + 8u);
+      reinterpret_cast<uint32_t*>(smem + p.smem_bar + 32u * S + 16u * NUM_ACC + 8u);
   uint32_t* const tmem_holder = misc + 0;
   volatile uint32_t* const abort_flag = misc + 1;
   uint32_t* const cta_amax = misc + 2;
@@ -487,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(empty0 + 8u * s, PAIR ? 1 : CM);
       // the four scale warps (of both CTAs of a pair): scales in tensor memory
       mbar_init(sfr0 + 8u * s, PAIR ? 8 : 4);
+      mbar_init(sff0 + 8u * s, 1);
     }
     for (int b = 0; b < NUM_ACC; ++b) {
       mbar_init(accf0 + 8u * b, 1);
@@ -523,8 +522,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == kSfProdWarp) {
+    // ----------------------------------------------------- producers
+    // warp 0 issues the operand tiles (first thing once a stage frees);
+    // warp kSfProdWarp issues the stage's small scale copies on their own
+    // barrier.  Both wait on the same stage-free barrier.
+    const bool scales = warp == kSfProdWarp;
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -534,48 +537,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t a_dst0 = base + p.smem_a, b_dst0 = base + p.smem_b;
       const uint32_t sfa_dst0 = base + p.smem_sfa, sfb_dst0 = base + p.smem_sfb;
       const size_t sf_group_stride = static_cast<size_t>(p.t_k) * kAtomBytes;
+      const uint32_t bar_base = scales ? sff0 : full0;
       for (int u = unit0; u < p.num_units && ok; u += unit_step) {
         const Tile tc = tile_coords(p, u, CM, crank);
-        int groups = p.t_n - tc.nt * G;
-        if (groups > G) groups = G;
+        const int m0 = tc.mt * kTileM, n0 = tc.nt * TILE_N;
+        const int atom0 = n0 / 128;  // first scale atom of B covering this tile
+        int natoms = p.t_n - atom0;
+        if (natoms > kSfbAtoms) natoms = kSfbAtoms;
         const bool ghost = tc.mt >= p.tiles_m;  // no rows of A: skip its scales
         const uint8_t* sfa_src =
             p.sfa + (static_cast<size_t>(tc.l) * p.t_m + (ghost ? 0 : tc.mt)) * sf_group_stride;
         const uint8_t* sfb_src =
-            p.sfb + (static_cast<size_t>(tc.l) * p.t_n + static_cast<size_t>(tc.nt) * G) *
-                        sf_group_stride;
-        const int m0 = tc.mt * kTileM, n0 = tc.nt * TILE_N;
+            p.sfb + (static_cast<size_t>(tc.l) * p.t_n + atom0) * sf_group_stride;
         for (int ks = 0; ks < p.k_stages; ++ks) {
-          if (!BSG_WAIT(empty0 + 8u * stage, phase ^ 1u, 1)) { ok = false; break; }
-          int nch = p.t_k - ks * KT::kChunks;
-          if (nch > KT::kChunks) nch = KT::kChunks;
-          const uint32_t sf_bytes = static_cast<uint32_t>(nch) * kAtomBytes;
-          const uint32_t fb = full0 + 8u * stage;
-          mbar_arrive_expect_tx(fb, kAStage + kBStage + sf_bytes * ((ghost ? 0u : 1u) + groups));
+          if (!BSG_WAIT(empty0 + 8u * stage, phase ^ 1u, scales ? 12 : 1)) { ok = false; break; }
+          const uint32_t bar = bar_base + 8u * stage;
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          tma_load_3d(a_dst0 + stage * kAStage, &tmap_a, ks * kStageKBytes, m0, tc.l, fb);
-          if (CM == 1)
-            tma_load_3d(b_dst0 + stage * kBStage, &tmap_b, ks * kStageKBytes, n0, tc.l, fb);
-          else if (PAIR)
-            tma_load_3d(b_dst0 + stage * kBStage, &tmap_b, ks * kStageKBytes, n0 + crank * kBRows,
-                        tc.l, fb);
-          else
-            tma_load_3d_mc(b_dst0 + stage * kBStage + crank * kBPart, &tmap_b, ks * kStageKBytes,
-                           n0 + crank * kBPartRows, tc.l, fb, kMask);
-          const size_t sf_off = static_cast<size_t>(ks) * KT::kChunks * kAtomBytes;
-          if (!ghost) bulk_load(sfa_dst0 + stage * kSfaStage, sfa_src + sf_off, sf_bytes, fb);
+          if (scales) {
+            int nch = p.t_k - ks * KT::kChunks;
+            if (nch > KT::kChunks) nch = KT::kChunks;
+            const uint32_t sf_bytes = static_cast<uint32_t>(nch) * kAtomBytes;
+            mbar_arrive_expect_tx(bar, sf_bytes * ((ghost ? 0u : 1u) + natoms));
+            const size_t sf_off = static_cast<size_t>(ks) * KT::kChunks * kAtomBytes;
+            if (!ghost) bulk_load(sfa_dst0 + stage * kSfaStage, sfa_src + sf_off, sf_bytes, bar);
 #pragma unroll
-          for (int g = 0; g < G; ++g)
-            if (g < groups)
-              bulk_load(sfb_dst0 + stage * kSfbStage + g * kSfaStage,
-                        sfb_src + g * sf_group_stride + sf_off, sf_bytes, fb);
+            for (int g = 0; g < kSfbAtoms; ++g)
+              if (g < natoms)
+                bulk_load(sfb_dst0 + stage * kSfbStage + g * kSfaStage,
+                          sfb_src + g * sf_group_stride + sf_off, sf_bytes, bar);
+          } else {
+            mbar_arrive_expect_tx(bar, kAStage + kBStage);
+            tma_load_3d(a_dst0 + stage * kAStage, &tmap_a, ks * kStageKBytes, m0, tc.l, bar);
+            if (CM == 1)
+              tma_load_3d(b_dst0 + stage * kBStage, &tmap_b, ks * kStageKBytes, n0, tc.l, bar);
+            else if (PAIR)
+              tma_load_3d(b_dst0 + stage * kBStage, &tmap_b, ks * kStageKBytes,
+                          n0 + crank * kBRows, tc.l, bar);
+            else
+              tma_load_3d_mc(b_dst0 + stage * kBStage + crank * kBPart, &tmap_b,
+                             ks * kStageKBytes, n0 + crank * kBPartRows, tc.l, bar, kMask);
+          }
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
       }
       // drain: every issued load must have landed before the CTA may exit
       for (int s = 0; s < S; ++s)
-        if (armed & (1u << s)) drain_wait(full0 + 8u * s, (armed_parity >> s) & 1u, p, 10u);
+        if (armed & (1u << s)) drain_wait(bar_base + 8u * s, (armed_parity >> s) & 1u, p, scales ? 13u : 10u);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
@@ -609,7 +617,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tmem + acc * TILE_N;
         for (int ks = 0; ks < p.k_stages; ++ks) {
           // operands in smem and this stage's scales in tensor memory
-          if (!BSG_WAIT(sfr0 + 8u * stage, phase, 3)) { ok = false; break; }
+          if (!BSG_WAIT(full0 + 8u * stage, phase, 3) || !BSG_WAIT(sfr0 + 8u * stage, phase, 6)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t sfb_t = sfa_t + 4 * KT::kChunks;
           if (ks != last) {
@@ -675,32 +686,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16) + kSfCol0;
     bool ok = true;
     for (int u = unit0; u < p.num_units && ok; u += unit_step) {
+      // row offset of the tile's first B row inside its first scale atom
+      const int n_off = (tile_coords(p, u, CM, crank).nt * TILE_N) % 128;
       for (int ks = 0; ks < p.k_stages; ++ks) {
-        // one lane polls the barrier (the scales gate the MMAs: no sleeping);
-        // then every lane observes the completed phase itself before reading
-        // the bytes
+        // one lane sleeps on the barrier (the scale bytes are issued ahead of
+        // the operand tiles, so there is slack; a polling warp would steal
+        // issue slots from the MMA warp, which shares a sub-partition with
+        // the quarter-1 scale warp); then every lane observes the completed
+        // phase itself before reading the bytes
         int landed = 1;
-        if (lane == 0) landed = BSG_WAIT(full0 + 8u * stage, phase, 5) ? 1 : 0;
+        if (lane == 0) landed = BSG_WAIT_SLEEP(sff0 + 8u * stage, phase, 5) ? 1 : 0;
         if (!__shfl_sync(0xFFFFFFFFu, landed, 0)) { ok = false; break; }
-        mbar_try_wait(full0 + 8u * stage, phase);
+        mbar_try_wait(sff0 + 8u * stage, phase);
         const uint8_t* sa = smem + p.smem_sfa + stage * kSfaStage + lane_off;
         const uint8_t* sb = smem + p.smem_sfb + stage * kSfbStage + lane_off;
         const uint32_t tcol = t_row + stage * kSfCols;
 #pragma unroll
         for (int c = 0; c < KT::kChunks; ++c) {
           tc_st_32x32b_x4(tcol + 4 * c, *reinterpret_cast<const uint4*>(sa + c * kAtomBytes));
+          if (kAlignedN) {
 #pragma unroll
-          for (int g = 0; g < G; ++g)
-            tc_st_32x32b_x4(tcol + 4 * KT::kChunks + 4 * (c * G + g),
-                            *reinterpret_cast<const uint4*>(sb + g * kSfaStage + c * kAtomBytes));
+            for (int g = 0; g < G; ++g)
+              tc_st_32x32b_x4(tcol + 4 * KT::kChunks + 4 * (c * G + g),
+                              *reinterpret_cast<const uint4*>(sb + g * kSfaStage + c * kAtomBytes));
+          } else {
+            // gather: tile row 128g + 32m1 + lane is row lane of the atom
+            // holding B row n0 + that row (n_off is a multiple of 32)
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              uint32_t w[4];
+#pragma unroll
+              for (int m1 = 0; m1 < 4; ++m1) {
+                const int t = 128 * g + 32 * m1;
+                const int rr = n_off + t;
+                w[m1] = t < TILE_N ? *reinterpret_cast<const uint32_t*>(
+                                         sb + (rr >> 7) * kSfaStage + c * kAtomBytes + ((rr >> 5) & 3) * 4)
+                                   : 0x7F7F7F7Fu;  // rows past the tile: scale 1
+              }
+              tc_st_32x32b_x4(tcol + 4 * KT::kChunks + 4 * (c * G + g), make_uint4(w[0], w[1], w[2], w[3]));
+            }
+          }
         }
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if (PAIR) mbar_arrive_cluster(mapa_shared(sfr0 + 8u * stage, 0));
-          else mbar_arrive(sfr0 + 8u * stage);
+          if (PAIR) {
+            // the leader waits for its own A/B halves; the peer's halves are
+            // reported through this arrival, so it also waits for them
+            if (crank != 0 && !BSG_WAIT_SLEEP(full0 + 8u * stage, phase, 7)) ok = false;
+            mbar_arrive_cluster(mapa_shared(sfr0 + 8u * stage, 0));
+          } else {
+            mbar_arrive(sfr0 + 8u * stage);
+          }
         }
+        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;  // the warp follows lane 0
+        if (!ok) break;
         if (++stage == S) { stage = 0; phase ^= 1u; }
       }
     }
@@ -797,20 +838,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         float* const cbase = static_cast<float*>(p.c) + batch_off;
+        constexpr int kCh = kCols / 16;        // 16-column chunks of this warp
+        constexpr int kP1 = (kCh + 1) / 2;     // chunks of the first pass
 #pragma unroll
         for (int pass = 0; pass < 2; ++pass) {
-          constexpr int kHalf = kCols / 2;
-          uint32_t r[kHalf];
+          const int c0 = pass ? kP1 : 0;
+          const int cn = pass ? kCh - kP1 : kP1;
+          uint32_t r[kP1 * 16];
 #pragma unroll
-          for (int cc = 0; cc < kHalf; cc += 32) tc_ld_32x32b_x32(taddr + pass * kHalf + cc, r + cc);
+          for (int i = 0; i < kP1; ++i)
+            if (i < cn) tc_ld_32x32b_x16(taddr + (c0 + i) * 16, r + 16 * i);
           tc_wait_ld();
           if (pass == 1) release();
-          const int nb = n0 + pass * kHalf;
+          const int nb = n0 + c0 * 16;
           if (p.c_major == 0) {
             float* dst = cbase + static_cast<size_t>(row) * p.N + nb;
 #pragma unroll
-            for (int i = 0; i < kHalf; i += 4) {
-              if (row_ok && nb + i < p.N) {
+            for (int i = 0; i < kP1 * 16; i += 4) {
+              if (i < cn * 16 && row_ok && nb + i < p.N) {
                 float4 v = make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
                                        __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
                 vmax = max(vmax, max(max(abs_bits_f32(v.x), abs_bits_f32(v.y)),
@@ -820,9 +865,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {
             float* dst = cbase + static_cast<size_t>(nb) * p.M + row;
-            const int ncols = row_ok ? min(kHalf, p.N - nb) : 0;
+            const int ncols = row_ok ? min(cn * 16, p.N - nb) : 0;
 #pragma unroll
-            for (int j = 0; j < kHalf; ++j) {
+            for (int j = 0; j < kP1 * 16; ++j) {
               if (j < ncols) {
                 const float f = __uint_as_float(r[j]);
                 *dst = f;
@@ -892,11 +937,12 @@ void add_kind(Variant* out, int& n) {
 }
 
 const Variant* find_variant(int kind, int tile_n, int num_acc, int cm) {
-  static Variant table[12];
+  static Variant table[13];
   static int n = 0;
   static std::once_flag once;
   std::call_once(once, [] {
     add_kind<kKindF8F6F4>(table, n);
+    table[n++] = make_variant<kKindF8F6F4, 224, 2, 2, 1>();  // 256 x 224 pairs, two accumulators
     add_kind<kKindF4x4X>(table, n);
     add_kind<kKindF4x2X>(table, n);
   });
@@ -997,7 +1043,8 @@ bsg_status bsg_problem_check(const bsg_problem* p) {
   }
   if (p->c_major != 'n' && p->c_major != 'm') return BSG_ERR_INVALID_ARG;
   if (p->tile_m != 0 && p->tile_m != 128) return BSG_ERR_INVALID_ARG;
-  if (p->tile_n != 0 && p->tile_n != 128 && p->tile_n != 256) return BSG_ERR_INVALID_ARG;
+  if (p->tile_n != 0 && p->tile_n != 128 && p->tile_n != 224 && p->tile_n != 256)
+    return BSG_ERR_INVALID_ARG;
   const int cl[2] = {p->cluster_m, p->cluster_n};
   for (int c : cl)
     if (c != 0 && c != 1 && c != 2 && c != 4) return BSG_ERR_INVALID_ARG;
@@ -1044,15 +1091,46 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   else if (sfv == 16) kind = kKindF4x4X;  // four block-16 scales per MMA: the whole column
   else kind = kKindF4x2X;                 // two block-32 scales per MMA: bytes 0-1 or 2-3
   const int chunks = kind == kKindF8F6F4 ? 1 : (kind == kKindF4x4X ? 4 : 2);
-  // 128 x 256 tiles halve the issue work and the L2 traffic per flop; a
-  // hint of 128 (or N <= 128) keeps the double-buffered 128 x 128 variant
-  k.tile_n = prob->tile_n == 128 || (prob->tile_n == 0 && prob->N <= 128) ? 128 : 256;
+  k.tiles_m = static_cast<int>(cdiv(prob->M, kTileM));
+  k.k_bytes = static_cast<int>(fp4 ? prob->K / 2 : prob->K);
+  k.k_stages = static_cast<int>(cdiv(k.k_bytes, kStageKBytes));
+  // Tile width.  256 (one accumulator) halves the issue work and the L2
+  // traffic per flop against 128; 224 (FP8, CTA pairs only) keeps two
+  // accumulators in tensor memory so the epilogue overlaps the next tile,
+  // and changes how the tiles fill the last wave.  With no hint the cheaper
+  // of 224 and 256 is taken by a model counted in 128-byte K stages of MMA
+  // work: every cluster runs ceil(units / clusters) tiles, and a tile with
+  // one accumulator also waits for its epilogue (about four stages).
+  const bool pair_ok = k.tiles_m >= 2 && (prob->cluster_m == 0 || prob->cluster_m == 2);
+  const bool n224_ok = kind == kKindF8F6F4 && pair_ok;
+  if (prob->tile_n == 128) {
+    k.tile_n = 128;
+  } else if (prob->tile_n == 256) {
+    k.tile_n = 256;
+  } else if (prob->tile_n == 224) {
+    if (!n224_ok) { delete plan; return BSG_ERR_UNSUPPORTED; }
+    k.tile_n = 224;
+  } else if (prob->N <= 128) {
+    k.tile_n = 128;
+  } else {
+    k.tile_n = 256;
+    if (n224_ok) {
+      const int64_t clusters = sms / 2 > 0 ? sms / 2 : 1;
+      auto estimate = [&](int tn, bool overlapped) {
+        const int64_t units = prob->L * cdiv(k.tiles_m, 2) * cdiv(prob->N, tn);
+        return static_cast<double>(cdiv(units, clusters)) *
+               (k.k_stages * tn / 256.0 + (overlapped ? 0.0 : 4.0));
+      };
+      if (estimate(224, true) < estimate(256, false)) k.tile_n = 224;
+    }
+  }
   const int num_acc = k.tile_n == 256 ? 1 : 2;
-  // 256-wide tiles run as cta_group::2 pairs by default (hint 1: single CTAs,
-  // 4: clusters of four multicasting the B tile); the 128-wide variant runs alone
+  // 224- and 256-wide tiles run as cta_group::2 pairs by default (hint 1:
+  // single CTAs, 4: clusters of four multicasting the B tile; 224 is pairs
+  // only); the 128-wide variant runs alone
   int cm = 1;
   if (k.tile_n == 256) cm = prob->cluster_m == 0 ? 2 : prob->cluster_m;
-  k.tiles_m = static_cast<int>(cdiv(prob->M, kTileM));
+  if (k.tile_n == 224) cm = 2;
   if (cm > k.tiles_m) cm = k.tiles_m >= 2 ? 2 : 1;
   const Variant* var = find_variant(kind, k.tile_n, num_acc, cm);
   if (!var) { delete plan; return BSG_ERR_UNSUPPORTED; }
@@ -1065,8 +1143,6 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   k.num_tiles = k.tiles_m * k.tiles_n * k.L;
   k.tiles_mc = static_cast<int>(cdiv(k.tiles_m, cm));
   k.num_units = k.tiles_mc * k.tiles_n * k.L;
-  k.k_bytes = static_cast<int>(fp4 ? prob->K / 2 : prob->K);
-  k.k_stages = static_cast<int>(cdiv(k.k_bytes, kStageKBytes));
   k.t_m = static_cast<int>(cdiv(prob->M, 128));
   k.t_n = static_cast<int>(cdiv(prob->N, 128));
   k.t_k = static_cast<int>(cdiv(prob->K, 4 * sfv));
@@ -1083,8 +1159,9 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   k.c_dtype = prob->c_dtype;
   k.c_major = prob->c_major == 'm' ? 1 : 0;
 
-  const int G = k.tile_n / 128;
-  const int sfa_stage = chunks * kAtomBytes, sfb_stage = chunks * kAtomBytes * G;
+  const int G = (k.tile_n + 127) / 128;                       // scale groups the MMA reads
+  const int sfb_atoms = k.tile_n % 128 == 0 ? G : G + 1;      // B scale atoms per chunk
+  const int sfa_stage = chunks * kAtomBytes, sfb_stage = chunks * kAtomBytes * sfb_atoms;
   const int b_rows = plan->pair ? k.tile_n / 2 : k.tile_n;  // B rows held per CTA
   const int per_stage = kTileM * kStageKBytes + b_rows * kStageKBytes + sfa_stage + sfb_stage;
   const int reserve = 1024 /* alignment slack */ + 512 /* barriers and flags */;
@@ -1102,7 +1179,7 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   k.smem_sfa = k.smem_b + stages * b_rows * kStageKBytes;
   k.smem_sfb = k.smem_sfa + stages * sfa_stage;
   k.smem_bar = k.smem_sfb + stages * sfb_stage;
-  plan->smem_bytes = static_cast<int>(k.smem_bar) + 24 * stages + 16 * num_acc + 8 + 16 + 1024;
+  plan->smem_bytes = static_cast<int>(k.smem_bar) + 32 * stages + 16 * num_acc + 8 + 16 + 1024;
   k.wait_limit_ns = 1000000000ull;  // one second per wait
   if (const char* e = std::getenv("BSG_WAIT_LIMIT_NS")) {
     const unsigned long long v = std::strtoull(e, nullptr, 10);

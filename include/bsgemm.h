@@ -76,7 +76,9 @@ typedef enum {
 /* Problem statement, after the page's constructor arguments ("Common
  * parameters", "Class-specific parameters").  tile_* and cluster_* are
  * hints only: 0 lets the library choose; otherwise tile_m must be 128,
- * tile_n 128 or 256, cluster_* 1, 2 or 4. */
+ * tile_n 128, 224 or 256 (224: FP8 operands and M > 128 only, else
+ * BSG_ERR_UNSUPPORTED), cluster_* 1, 2 or 4 (cluster_m 2 is a pair of CTAs
+ * running 256-row MMAs, the default for tile_n 224 and 256). */
 typedef struct {
     int64_t M, N, K, L;
     int32_t a_dtype, b_dtype;   /* bsg_dtype */

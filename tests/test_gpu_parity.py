@@ -227,6 +227,8 @@ def test_workload_full_size_sampled(number):
 
 TILE_CASES = [
     P(256, 512, 512), P(200, 520, 160, 2, c="bf16"), P(136, 1000, 96, major="m"),
+    P(640, 1352, 1024, c="bf16"), P(392, 904, 512, 2, major="m"),
+    P(1000, 1576, 384, a="e5m2", b="e4m3", c="f16"),
     P(128, 264, 64, a="e2m1", b="e2m1", sfv=16),
     P(260, 384, 640, a="e2m1", b="e2m1", sfv=16, c="bf16"),
     P(132, 392, 384, 2, a="e2m1", b="e2m1", sfv=32, major="m"),
@@ -234,11 +236,17 @@ TILE_CASES = [
 ]
 
 
-@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("tile_n", [128, 224, 256])
 @pytest.mark.parametrize("p", TILE_CASES, ids=[f"{p.M}x{p.N}x{p.K}L{p.L}{p.a_dtype}sfv{p.sfv}{p.c_major}" for p in TILE_CASES])
 def test_tile_variants(p, tile_n):
-    """Both CTA tile widths (the 128 x 256 tile reads two 128-row scale
-    groups of B per K-chunk) against the oracle, ragged N included."""
+    """Every tile width against the oracle, ragged N included.  256 reads two
+    128-row scale groups of B per K-chunk; 224 (FP8 pairs, two accumulators)
+    starts each tile at a multiple of 32 inside a scale atom, so its scales
+    are gathered across up to three atoms."""
+    if tile_n == 224 and (p.a_dtype == "e2m1" or p.M <= 128):
+        st, _ = bsg.bsg_plan_create(problem_of(p, tile_n=224), 0)
+        assert st == bsg.BSG_ERR_UNSUPPORTED
+        return
     inp = synth.uniform_codes(p, p.M * 5 + p.N + p.K + tile_n, 123, 131)
     c, amax, _, op, guard_ok = run_gpu(inp, guard=4096, tile_n=tile_n)
     assert op.describe()["tile_n"] == tile_n
