@@ -617,10 +617,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tmem + acc * TILE_N;
         for (int ks = 0; ks < p.k_stages; ++ks) {
           // operands in smem and this stage's scales in tensor memory
-          if (!BSG_WAIT(full0 + 8u * stage, phase, 3) || !BSG_WAIT(sfr0 + 8u * stage, phase, 6)) {
-            ok = false;
-            break;
-          }
+          // one barrier per stage: its arrivals come after the scales are in
+          // tensor memory and (through the quarter-0 scale warp of each CTA)
+          // after the A/B tiles have landed
+          if (!BSG_WAIT(sfr0 + 8u * stage, phase, 3)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sfb_t = sfa_t + 4 * KT::kChunks;
           if (ks != last) {
@@ -731,14 +731,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if (PAIR) {
-            // the leader waits for its own A/B halves; the peer's halves are
-            // reported through this arrival, so it also waits for them
-            if (crank != 0 && !BSG_WAIT_SLEEP(full0 + 8u * stage, phase, 7)) ok = false;
-            mbar_arrive_cluster(mapa_shared(sfr0 + 8u * stage, 0));
-          } else {
-            mbar_arrive(sfr0 + 8u * stage);
-          }
+          // the quarter-0 warp also reports this CTA's A/B tiles landed, so
+          // the MMA issuer needs only this barrier (it polls on sub-partition
+          // 0, away from the MMA warp)
+          if (q == 0 && !BSG_WAIT(full0 + 8u * stage, phase, 7)) ok = false;
+          if (PAIR) mbar_arrive_cluster(mapa_shared(sfr0 + 8u * stage, 0));
+          else mbar_arrive(sfr0 + 8u * stage);
         }
         ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;  // the warp follows lane 0
         if (!ok) break;
