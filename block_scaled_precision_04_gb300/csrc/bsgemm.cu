@@ -421,7 +421,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 
 // --------------------------------------------------------------- kernel
 
-template <int KIND, int TILE_N, int NUM_ACC, int CM, int PAIR>
+template <int KIND, int TILE_N, int NUM_ACC, int CM, int PAIR, int KSL>
 __global__ void __launch_bounds__(kThreads, 1)
     bsg_gemm_amax_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ Params p) {
@@ -432,19 +432,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int G = (TILE_N + 127) / 128;
   constexpr bool kAlignedN = TILE_N % 128 == 0;
   constexpr int kSfbAtoms = kAlignedN ? G : G + 1;  // B scale atoms per chunk in smem
-  constexpr uint32_t kAStage = kTileM * kStageKBytes;   // smem bytes per stage
+  // a stage holds KSL 128-byte K slices (each its own 128-byte swizzle block)
+  constexpr int kSB = kStageKBytes * KSL;                // K bytes per stage
+  constexpr int kCps = KT::kChunks * KSL;                // scale atoms along K per stage
+  constexpr uint32_t kASlice = kTileM * kStageKBytes;
+  constexpr uint32_t kAStage = kASlice * KSL;            // smem bytes per stage
   // PAIR: a 2-CTA pair runs 256 x TILE_N MMAs (cta_group::2); each CTA holds
   // its 128 rows of A and half (TILE_N/2 rows) of the B tile
   static_assert(!PAIR || CM == 2, "a CTA pair is a cluster of two");
   constexpr int kBRows = PAIR ? TILE_N / 2 : TILE_N;
-  constexpr uint32_t kBStage = kBRows * kStageKBytes;
-  constexpr uint32_t kSfaStage = KT::kChunks * kAtomBytes;
-  constexpr uint32_t kSfbStage = KT::kChunks * kAtomBytes * kSfbAtoms;
+  constexpr uint32_t kBSlice = kBRows * kStageKBytes;
+  constexpr uint32_t kBStage = kBSlice * KSL;
+  constexpr uint32_t kSfaStage = kCps * kAtomBytes;
+  constexpr uint32_t kSfbStage = kCps * kAtomBytes * kSfbAtoms;
   // scale columns follow the accumulators, one set per smem stage, so that a
   // stage's tcgen05.cp never rewrites columns an in-flight MMA still reads
-  constexpr uint32_t kSfCols = 4 * KT::kChunks * (1 + G);
+  constexpr uint32_t kSfCols = 4 * kCps * (1 + G);
   constexpr uint32_t kSfCol0 = NUM_ACC * TILE_N;
-  constexpr int kMmasPerStage = kStageKBytes / kMmaKBytes;
+  constexpr int kMmasPerStage = kSB / kMmaKBytes;
+  constexpr int kMmasPerSlice = kStageKBytes / kMmaKBytes;
   // B tile shared by the cluster's CM CTAs: each loads TILE_N / CM rows and
   // multicasts them to all
   constexpr int kBPartRows = PAIR ? kBRows : TILE_N / CM;
@@ -555,11 +561,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (scales) {
-            int nch = p.t_k - ks * KT::kChunks;
-            if (nch > KT::kChunks) nch = KT::kChunks;
+            int nch = p.t_k - ks * kCps;
+            if (nch > kCps) nch = kCps;
             const uint32_t sf_bytes = static_cast<uint32_t>(nch) * kAtomBytes;
             mbar_arrive_expect_tx(bar, sf_bytes * ((ghost ? 0u : 1u) + natoms));
-            const size_t sf_off = static_cast<size_t>(ks) * KT::kChunks * kAtomBytes;
+            const size_t sf_off = static_cast<size_t>(ks) * kCps * kAtomBytes;
             if (!ghost) bulk_load(sfa_dst0 + stage * kSfaStage, sfa_src + sf_off, sf_bytes, bar);
 #pragma unroll
             for (int g = 0; g < kSfbAtoms; ++g)
@@ -568,15 +574,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                           sfb_src + g * sf_group_stride + sf_off, sf_bytes, bar);
           } else {
             mbar_arrive_expect_tx(bar, kAStage + kBStage);
-            tma_load_3d(a_dst0 + stage * kAStage, &tmap_a, ks * kStageKBytes, m0, tc.l, bar);
-            if (CM == 1)
-              tma_load_3d(b_dst0 + stage * kBStage, &tmap_b, ks * kStageKBytes, n0, tc.l, bar);
-            else if (PAIR)
-              tma_load_3d(b_dst0 + stage * kBStage, &tmap_b, ks * kStageKBytes,
-                          n0 + crank * kBRows, tc.l, bar);
-            else
-              tma_load_3d_mc(b_dst0 + stage * kBStage + crank * kBPart, &tmap_b,
-                             ks * kStageKBytes, n0 + crank * kBPartRows, tc.l, bar, kMask);
+#pragma unroll
+            for (int sl = 0; sl < KSL; ++sl) {
+              const int kx = ks * kSB + sl * kStageKBytes;
+              tma_load_3d(a_dst0 + stage * kAStage + sl * kASlice, &tmap_a, kx, m0, tc.l, bar);
+              const uint32_t bdst = b_dst0 + stage * kBStage + sl * kBSlice;
+              if (CM == 1)
+                tma_load_3d(bdst, &tmap_b, kx, n0, tc.l, bar);
+              else if (PAIR)
+                tma_load_3d(bdst, &tmap_b, kx, n0 + crank * kBRows, tc.l, bar);
+              else
+                tma_load_3d_mc(bdst + crank * kBPart, &tmap_b, kx, n0 + crank * kBPartRows, tc.l,
+                               bar, kMask);
+            }
           }
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
@@ -609,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t ad = adesc0, bd = bdesc0;
       uint32_t sfa_t = sf_t0;
       const int last = p.k_stages - 1;
-      int last_nmma = (p.k_bytes - last * kStageKBytes + kMmaKBytes - 1) / kMmaKBytes;
+      int last_nmma = (p.k_bytes - last * kSB + kMmaKBytes - 1) / kMmaKBytes;
       if (last_nmma > kMmasPerStage) last_nmma = kMmasPerStage;
       for (int u = unit0; u < p.num_units && ok; u += unit_step) {
         if (!BSG_WAIT(acce0 + 8u * acc, acc_phase ^ 1u, 2)) { ok = false; break; }
@@ -622,13 +632,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           // after the A/B tiles have landed
           if (!BSG_WAIT(sfr0 + 8u * stage, phase, 3)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sfb_t = sfa_t + 4 * KT::kChunks;
+          const uint32_t sfb_t = sfa_t + 4 * kCps;
           if (ks != last) {
 #pragma unroll
             for (int j = 0; j < kMmasPerStage; ++j) {
               const int c = j / KT::kMmasPerChunk;
               const uint32_t sf_id = static_cast<uint32_t>((j % KT::kMmasPerChunk) * KT::kSfIdStep);
-              mma_issue(d_tmem, ad + ((j * kMmaKBytes) >> 4), bd + ((j * kMmaKBytes) >> 4),
+              const int sl = j / kMmasPerSlice, jj = j % kMmasPerSlice;
+              mma_issue(d_tmem, ad + ((sl * kASlice + jj * kMmaKBytes) >> 4),
+                        bd + ((sl * kBSlice + jj * kMmaKBytes) >> 4),
                         idesc | (sf_id << 29) | (sf_id << 4), sfa_t + 4 * c, sfb_t + 4 * G * c,
                         (j != 0 || ks != 0) ? 1u : 0u);
             }
@@ -638,7 +650,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (j < last_nmma) {
                 const int c = j / KT::kMmasPerChunk;
                 const uint32_t sf_id = static_cast<uint32_t>((j % KT::kMmasPerChunk) * KT::kSfIdStep);
-                mma_issue(d_tmem, ad + ((j * kMmaKBytes) >> 4), bd + ((j * kMmaKBytes) >> 4),
+                const int sl = j / kMmasPerSlice, jj = j % kMmasPerSlice;
+                mma_issue(d_tmem, ad + ((sl * kASlice + jj * kMmaKBytes) >> 4),
+                          bd + ((sl * kBSlice + jj * kMmaKBytes) >> 4),
                           idesc | (sf_id << 29) | (sf_id << 4), sfa_t + 4 * c, sfb_t + 4 * G * c,
                           (j != 0 || ks != 0) ? 1u : 0u);
               }
@@ -702,12 +716,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* sb = smem + p.smem_sfb + stage * kSfbStage + lane_off;
         const uint32_t tcol = t_row + stage * kSfCols;
 #pragma unroll
-        for (int c = 0; c < KT::kChunks; ++c) {
+        for (int c = 0; c < kCps; ++c) {
           tc_st_32x32b_x4(tcol + 4 * c, *reinterpret_cast<const uint4*>(sa + c * kAtomBytes));
           if (kAlignedN) {
 #pragma unroll
             for (int g = 0; g < G; ++g)
-              tc_st_32x32b_x4(tcol + 4 * KT::kChunks + 4 * (c * G + g),
+              tc_st_32x32b_x4(tcol + 4 * kCps + 4 * (c * G + g),
                               *reinterpret_cast<const uint4*>(sb + g * kSfaStage + c * kAtomBytes));
           } else {
             // gather: tile row 128g + 32m1 + lane is row lane of the atom
@@ -723,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          sb + (rr >> 7) * kSfaStage + c * kAtomBytes + ((rr >> 5) & 3) * 4)
                                    : 0x7F7F7F7Fu;  // rows past the tile: scale 1
               }
-              tc_st_32x32b_x4(tcol + 4 * KT::kChunks + 4 * (c * G + g), make_uint4(w[0], w[1], w[2], w[3]));
+              tc_st_32x32b_x4(tcol + 4 * kCps + 4 * (c * G + g), make_uint4(w[0], w[1], w[2], w[3]));
             }
           }
         }
@@ -916,14 +930,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Kernel variants: MMA kind x (TILE_N, accumulator buffers) x cluster along M
 // (cm 1 alone, 2 a cta_group::2 pair, 4 a quad multicasting the B tile)
 struct Variant {
-  int kind, tile_n, num_acc, cm, pair;
+  int kind, tile_n, num_acc, cm, pair, kslices;
   const void* fn;
 };
 
-template <int KIND, int TN, int NACC, int CM, int PAIR>
+template <int KIND, int TN, int NACC, int CM, int PAIR, int KSL = 1>
 Variant make_variant() {
-  return Variant{KIND, TN, NACC, CM, PAIR,
-                 reinterpret_cast<const void*>(&bsg_gemm_amax_kernel<KIND, TN, NACC, CM, PAIR>)};
+  return Variant{KIND, TN, NACC, CM, PAIR, KSL,
+                 reinterpret_cast<const void*>(&bsg_gemm_amax_kernel<KIND, TN, NACC, CM, PAIR, KSL>)};
 }
 
 template <int KIND>
@@ -934,19 +948,22 @@ void add_kind(Variant* out, int& n) {
   out[n++] = make_variant<KIND, 256, 1, 4, 0>();
 }
 
-const Variant* find_variant(int kind, int tile_n, int num_acc, int cm) {
-  static Variant table[13];
+const Variant* find_variant(int kind, int tile_n, int num_acc, int cm, int kslices) {
+  static Variant table[14];
   static int n = 0;
   static std::once_flag once;
   std::call_once(once, [] {
     add_kind<kKindF8F6F4>(table, n);
     table[n++] = make_variant<kKindF8F6F4, 224, 2, 2, 1>();  // 256 x 224 pairs, two accumulators
+    table[n++] = make_variant<kKindF8F6F4, 256, 1, 2, 1, 2>();  // pairs, 256-byte K stages
     add_kind<kKindF4x4X>(table, n);
     add_kind<kKindF4x2X>(table, n);
   });
   for (int i = 0; i < n; ++i) {
     const Variant& v = table[i];
-    if (v.kind == kind && v.tile_n == tile_n && v.num_acc == num_acc && v.cm == cm) return &v;
+    if (v.kind == kind && v.tile_n == tile_n && v.num_acc == num_acc && v.cm == cm &&
+        v.kslices == kslices)
+      return &v;
   }
   return nullptr;
 }
@@ -989,6 +1006,7 @@ struct bsg_plan {
   int kind;
   int num_acc;
   int cluster_m;         // CTAs per cluster along M sharing the B tile
+  int kslices;           // 128-byte K slices per pipeline stage
   int pair;              // 1: the cluster is a cta_group::2 pair (256-row MMAs)
   int grid;
   int smem_bytes;
@@ -1130,8 +1148,14 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   if (k.tile_n == 256) cm = prob->cluster_m == 0 ? 2 : prob->cluster_m;
   if (k.tile_n == 224) cm = 2;
   if (cm > k.tiles_m) cm = k.tiles_m >= 2 ? 2 : 1;
-  const Variant* var = find_variant(kind, k.tile_n, num_acc, cm);
+  // FP8 pairs with 256-wide tiles take 256-byte K stages (8 MMAs per
+  // barrier check); each CTA's half tiles keep three such stages in smem
+  const int ksl = kind == kKindF8F6F4 && k.tile_n == 256 && cm == 2 ? 2 : 1;
+  const int stage_k_bytes = kStageKBytes * ksl;
+  k.k_stages = static_cast<int>(cdiv(k.k_bytes, stage_k_bytes));
+  const Variant* var = find_variant(kind, k.tile_n, num_acc, cm, ksl);
   if (!var) { delete plan; return BSG_ERR_UNSUPPORTED; }
+  plan->kslices = ksl;
   plan->kernel = var->fn;
   plan->kind = kind;
   plan->num_acc = num_acc;
@@ -1159,13 +1183,13 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
 
   const int G = (k.tile_n + 127) / 128;                       // scale groups the MMA reads
   const int sfb_atoms = k.tile_n % 128 == 0 ? G : G + 1;      // B scale atoms per chunk
-  const int sfa_stage = chunks * kAtomBytes, sfb_stage = chunks * kAtomBytes * sfb_atoms;
+  const int sfa_stage = chunks * ksl * kAtomBytes, sfb_stage = chunks * ksl * kAtomBytes * sfb_atoms;
   const int b_rows = plan->pair ? k.tile_n / 2 : k.tile_n;  // B rows held per CTA
-  const int per_stage = kTileM * kStageKBytes + b_rows * kStageKBytes + sfa_stage + sfb_stage;
+  const int per_stage = kTileM * stage_k_bytes + b_rows * stage_k_bytes + sfa_stage + sfb_stage;
   const int reserve = 1024 /* alignment slack */ + 512 /* barriers and flags */;
   int stages = (max_smem - reserve) / per_stage;
   if (stages > 8) stages = 8;
-  const int sf_cols = 4 * chunks * (1 + G);
+  const int sf_cols = 4 * chunks * ksl * (1 + G);
   while (stages > 2 && num_acc * k.tile_n + stages * sf_cols > static_cast<int>(kTmemCols)) --stages;
   if (stages < 2 || num_acc * k.tile_n + stages * sf_cols > static_cast<int>(kTmemCols)) {
     delete plan;
@@ -1173,8 +1197,8 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   }
   k.stages = stages;
   k.smem_a = 0;
-  k.smem_b = k.smem_a + stages * kTileM * kStageKBytes;
-  k.smem_sfa = k.smem_b + stages * b_rows * kStageKBytes;
+  k.smem_b = k.smem_a + stages * kTileM * stage_k_bytes;
+  k.smem_sfa = k.smem_b + stages * b_rows * stage_k_bytes;
   k.smem_sfb = k.smem_sfa + stages * sfa_stage;
   k.smem_bar = k.smem_sfb + stages * sfb_stage;
   plan->smem_bytes = static_cast<int>(k.smem_bar) + 32 * stages + 16 * num_acc + 8 + 16 + 1024;
@@ -1443,7 +1467,7 @@ bsg_status bsg_plan_describe(const bsg_plan* plan, bsg_plan_info* info) {
   std::memset(info, 0, sizeof(*info));
   info->tile_m = kTileM;
   info->tile_n = plan->base.tile_n;
-  info->tile_k_bytes = kStageKBytes;
+  info->tile_k_bytes = kStageKBytes * plan->kslices;
   info->stages = plan->base.stages;
   info->grid = plan->grid;
   info->threads = kThreads;
