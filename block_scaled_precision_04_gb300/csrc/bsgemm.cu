@@ -406,12 +406,17 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Para
 
 __device__ __forceinline__ uint32_t abs_bits_f32(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
 
-// Bounded wait for the drains at exit (no abort flag: always runs).
+// Bounded wait for the drains at exit (no abort flag: always runs).  It
+// waits for this CTA's own copies and MMAs, which finish by themselves, so
+// its limit never drops below 200 ms even when the pipeline waits use a
+// shorter one.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const Params& p,
                                            uint32_t where) {
+  const unsigned long long limit =
+      p.wait_limit_ns > 200000000ull ? p.wait_limit_ns : 200000000ull;
   const unsigned long long start = globaltimer();
   while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
-    if (globaltimer() - start > p.wait_limit_ns) {
+    if (globaltimer() - start > limit) {
       atomicOr(p.ws + 2, kErrTimeout);
       atomicCAS(p.ws + 3, 0u, where);
       break;

@@ -1,0 +1,45 @@
+"""Failure detection on the GPU without a fault: every pipeline wait in the
+kernel is bounded.  With a wait limit far below a tile's running time the
+waits run out; the kernel records it in the workspace error word, abandons
+its pipeline, drains its own copies and MMAs, frees tensor memory and
+returns.  The host reads BSG_ERR_DEVICE_TIMEOUT, and the same context then
+runs a normal plan correctly."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_precision_04_gb300 as bsg
+import synth
+from gpu_util import assert_parity, problem_of, run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    bsg.build()
+    bsg.library()
+
+
+@pytest.mark.parametrize("tile_n", [0, 128])
+def test_wait_limit_reports_timeout_then_context_recovers(tile_n, monkeypatch):
+    inp = synth.workload(2, M=1024, N=1024, K=4096)
+    p = inp.problem
+    monkeypatch.setenv("BSG_WAIT_LIMIT_NS", "2000")  # 2 us: shorter than one tile
+    op = bsg.GemmAmax(problem_of(p, tile_n=tile_n))  # the plan reads the limit
+    monkeypatch.delenv("BSG_WAIT_LIMIT_NS")
+    A, B, SFA, SFB = to_device(inp)
+    C = torch.zeros(synth.c_shape(p), dtype=torch.bfloat16, device="cuda:0")
+    amax = torch.zeros(1, dtype=torch.float32, device="cuda:0")
+    op.run(A, B, SFA, SFB, C, amax)
+    torch.cuda.synchronize()  # the kernel returned (no hang, no fault)
+    assert op.device_status() == bsg.BSG_ERR_DEVICE_TIMEOUT
+    assert op.device_status() == bsg.BSG_OK  # reading clears the error word
+    op.close()
+    # a normal plan on the same context
+    c, a, *_ = run_gpu(inp, tile_n=tile_n)
+    assert_parity(inp, c, a)
