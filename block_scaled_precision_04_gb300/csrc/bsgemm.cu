@@ -129,6 +129,28 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// 4-D tiled copy (scale atoms: 64 x 8-byte words, K atoms, MN atoms, L).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, int w, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+
+// A pair's second CTA: the box lands in its own shared memory and the bytes
+// are counted on the mbarrier at `bar`, a shared::cluster address in the
+// pair's leader, so the leader's MMA issuer sees both halves on one barrier.
+__device__ __forceinline__ void tma_load_3d_to_leader(uint32_t dst, const CUtensorMap* map, int x,
+                                                      int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
 // The same box into the same smem offset of every CTA in `mask`; each
 // destination CTA's mbarrier at `bar`'s offset receives the bytes it got.
 __device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, int x, int y,
@@ -158,15 +180,6 @@ __device__ __forceinline__ uint32_t cluster_count_x() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -378,43 +391,45 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded slow path of a wait.  Returns false when the pipeline is abandoned.
-// `spin`: poll without suspending first (the producer and MMA threads, whose
-// waits are short and whose wake-up latency is on the critical path).
+// Polls with test_wait: warps parked in a blocking try_wait measurably slow
+// the MMA issuer sharing their SM.  `sleep_ns` > 0 (warps off the critical
+// path: epilogue, scale warps) naps between polls; 0 spins (producers and
+// the MMA issuer, whose wake-up latency is on the critical path).
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Params& p,
-                                       volatile uint32_t* abort_flag, uint32_t where, bool spin) {
-  if (spin)
-    for (int i = 0; i < 2048; ++i)
-      if (mbar_test_wait(bar, parity)) return true;
+                                       volatile uint32_t* abort_flag, uint32_t where,
+                                       uint32_t sleep_ns) {
   const unsigned long long start = globaltimer();
-  while (true) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer() - start > p.wait_limit_ns) {
-      atomicOr(p.ws + 2, kErrTimeout);
-      atomicCAS(p.ws + 3, 0u, where);
-      *abort_flag = 1u;
-      return false;
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if (sleep_ns) __nanosleep(sleep_ns);
+    if (sleep_ns || (i & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - start > p.wait_limit_ns) {
+        atomicOr(p.ws + 2, kErrTimeout);
+        atomicCAS(p.ws + 3, 0u, where);
+        *abort_flag = 1u;
+        return false;
+      }
     }
   }
 }
 
-// Fast path inline: one try_wait; the bounded loop only when the phase is open.
+// Fast path inline: one test_wait; the bounded loop only when the phase is open.
 #define BSG_WAIT(bar, parity, site) \
-  (mbar_try_wait((bar), (parity)) || wait_slow((bar), (parity), p, abort_flag, (site), true))
+  (mbar_test_wait((bar), (parity)) || wait_slow((bar), (parity), p, abort_flag, (site), 0u))
 #define BSG_WAIT_SLEEP(bar, parity, site) \
-  (mbar_try_wait((bar), (parity)) || wait_slow((bar), (parity), p, abort_flag, (site), false))
+  (mbar_test_wait((bar), (parity)) || wait_slow((bar), (parity), p, abort_flag, (site), 128u))
 
 __device__ __forceinline__ uint32_t abs_bits_f32(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
 
 // Bounded wait for the drains at exit (no abort flag: always runs).  It
 // waits for this CTA's own copies and MMAs, which finish by themselves, so
-// its limit never drops below 200 ms even when the pipeline waits use a
-// shorter one.
+// its limit, counted from `start` (one deadline for a whole drain), never
+// drops below 200 ms even when the pipeline waits use a shorter one.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const Params& p,
-                                           uint32_t where) {
+                                           uint32_t where, unsigned long long start) {
   const unsigned long long limit =
       p.wait_limit_ns > 200000000ull ? p.wait_limit_ns : 200000000ull;
-  const unsigned long long start = globaltimer();
   while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
     if (globaltimer() - start > limit) {
       atomicOr(p.ws + 2, kErrTimeout);
@@ -429,7 +444,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 template <int KIND, int TILE_N, int NUM_ACC, int CM, int PAIR, int KSL>
 __global__ void __launch_bounds__(kThreads, 1)
     bsg_gemm_amax_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                         const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ Params p) {
+                         const __grid_constant__ CUtensorMap tmap_b,
+                         const __grid_constant__ CUtensorMap tmap_sfa,
+                         const __grid_constant__ CUtensorMap tmap_sfb, const __grid_constant__ Params p) {
   using KT = KindTraits<KIND>;
   // 128-row scale groups of B the MMA reads (tile rows 128g .. 128g+127 at
   // columns +4g); a tile width that is not a multiple of 128 (224) starts at
@@ -446,7 +463,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // its 128 rows of A and half (TILE_N/2 rows) of the B tile
   static_assert(!PAIR || CM == 2, "a CTA pair is a cluster of two");
   constexpr int kBRows = PAIR ? TILE_N / 2 : TILE_N;
-  constexpr uint32_t kBSlice = kBRows * kStageKBytes;
+  // B is loaded in boxes of whole 128-row groups: a 112-row box (a 224-wide
+  // pair's half) streams markedly slower through the TMA unit, so the half
+  // is loaded as 128 rows and the MMA reads the first 112
+  constexpr int kBLoadRows = (kBRows + 127) / 128 * 128;
+  constexpr uint32_t kBSlice = kBLoadRows * kStageKBytes;
   constexpr uint32_t kBStage = kBSlice * KSL;
   constexpr uint32_t kSfaStage = kCps * kAtomBytes;
   constexpr uint32_t kSfbStage = kCps * kAtomBytes * kSfbAtoms;
@@ -476,26 +497,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int unit_step = CM > 1 ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
 
   const uint32_t bar0 = base + p.smem_bar;
-  // per stage: full (A/B bytes landed), empty (stage free), sfr (scales in
-  // tensor memory), sff (scale bytes landed; issued first, off the A/B path)
-  const uint32_t full0 = bar0, empty0 = bar0 + 8u * S, sfr0 = bar0 + 16u * S;
-  const uint32_t sff0 = bar0 + 24u * S;
-  const uint32_t accf0 = bar0 + 32u * S, acce0 = accf0 + 8u * NUM_ACC;
+  // per stage: full (the stage is ready for the MMA: its A/B bytes -- of
+  // both CTAs of a pair, counted in the leader -- have landed and every
+  // scale warp has put its scales in tensor memory), empty (stage free), sff
+  // (scale bytes landed; issued first, off the A/B path)
+  const uint32_t full0 = bar0, empty0 = bar0 + 8u * S, sff0 = bar0 + 16u * S;
+  const uint32_t accf0 = bar0 + 24u * S, acce0 = accf0 + 8u * NUM_ACC;
   const uint32_t drain_bar = acce0 + 8u * NUM_ACC;
   uint32_t* const misc =
-      reinterpret_cast<uint32_t*>(smem + p.smem_bar + 32u * S + 16u * NUM_ACC + 8u);
+      reinterpret_cast<uint32_t*>(smem + p.smem_bar + 24u * S + 16u * NUM_ACC + 8u);
   uint32_t* const tmem_holder = misc + 0;
   volatile uint32_t* const abort_flag = misc + 1;
   uint32_t* const cta_amax = misc + 2;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8u * s, 1);
+      // the producer's expect_tx and the four scale warps (of both CTAs of a
+      // pair; only the leader's barrier is used then)
+      mbar_init(full0 + 8u * s, 1 + (PAIR ? 8 : 4));
       // freed by the MMA commit of every CTA of a multicast cluster, or by the
       // single (multicast) commit of a pair's leader
       mbar_init(empty0 + 8u * s, PAIR ? 1 : CM);
-      // the four scale warps (of both CTAs of a pair): scales in tensor memory
-      mbar_init(sfr0 + 8u * s, PAIR ? 8 : 4);
       mbar_init(sff0 + 8u * s, 1);
     }
     for (int b = 0; b < NUM_ACC; ++b) {
@@ -511,6 +533,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
+  }
+  if (warp == kSfProdWarp && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_sfa)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_sfb)) : "memory");
   }
   if (warp == 1) {
     if (PAIR) {  // one warp of each CTA of the pair allocates collectively
@@ -547,47 +573,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       const uint32_t a_dst0 = base + p.smem_a, b_dst0 = base + p.smem_b;
       const uint32_t sfa_dst0 = base + p.smem_sfa, sfb_dst0 = base + p.smem_sfb;
-      const size_t sf_group_stride = static_cast<size_t>(p.t_k) * kAtomBytes;
       const uint32_t bar_base = scales ? sff0 : full0;
       for (int u = unit0; u < p.num_units && ok; u += unit_step) {
         const Tile tc = tile_coords(p, u, CM, crank);
         const int m0 = tc.mt * kTileM, n0 = tc.nt * TILE_N;
         const int atom0 = n0 / 128;  // first scale atom of B covering this tile
-        int natoms = p.t_n - atom0;
-        if (natoms > kSfbAtoms) natoms = kSfbAtoms;
-        const bool ghost = tc.mt >= p.tiles_m;  // no rows of A: skip its scales
-        const uint8_t* sfa_src =
-            p.sfa + (static_cast<size_t>(tc.l) * p.t_m + (ghost ? 0 : tc.mt)) * sf_group_stride;
-        const uint8_t* sfb_src =
-            p.sfb + (static_cast<size_t>(tc.l) * p.t_n + atom0) * sf_group_stride;
         for (int ks = 0; ks < p.k_stages; ++ks) {
           if (!BSG_WAIT(empty0 + 8u * stage, phase ^ 1u, scales ? 12 : 1)) { ok = false; break; }
           const uint32_t bar = bar_base + 8u * stage;
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (scales) {
-            int nch = p.t_k - ks * kCps;
-            if (nch > kCps) nch = kCps;
-            const uint32_t sf_bytes = static_cast<uint32_t>(nch) * kAtomBytes;
-            mbar_arrive_expect_tx(bar, sf_bytes * ((ghost ? 0u : 1u) + natoms));
-            const size_t sf_off = static_cast<size_t>(ks) * kCps * kAtomBytes;
-            if (!ghost) bulk_load(sfa_dst0 + stage * kSfaStage, sfa_src + sf_off, sf_bytes, bar);
+            // the stage's scale atoms in two tensor copies (the small copies
+            // share the TMA unit with the operand tiles, so fewer is faster):
+            // atoms past the tensor's end (a ghost M tile, N or K tails)
+            // arrive zero-filled and are never read for a stored element
+            mbar_arrive_expect_tx(bar, kSfaStage + kSfbStage);
+            tma_load_4d(sfa_dst0 + stage * kSfaStage, &tmap_sfa, 0, ks * kCps, tc.mt, tc.l, bar);
+            tma_load_4d(sfb_dst0 + stage * kSfbStage, &tmap_sfb, 0, ks * kCps, atom0, tc.l, bar);
+          } else if (PAIR && crank != 0) {
+            // the second CTA of a pair: its halves are counted in the leader
+            const uint32_t lbar = mapa_shared(bar, 0);
 #pragma unroll
-            for (int g = 0; g < kSfbAtoms; ++g)
-              if (g < natoms)
-                bulk_load(sfb_dst0 + stage * kSfbStage + g * kSfaStage,
-                          sfb_src + g * sf_group_stride + sf_off, sf_bytes, bar);
+            for (int sl = 0; sl < KSL; ++sl) {
+              const int kx = ks * kSB + sl * kStageKBytes;
+              tma_load_3d_to_leader(a_dst0 + stage * kAStage + sl * kASlice, &tmap_a, kx, m0, tc.l,
+                                    lbar);
+              tma_load_3d_to_leader(b_dst0 + stage * kBStage + sl * kBSlice, &tmap_b, kx,
+                                    n0 + kBRows, tc.l, lbar);
+            }
           } else {
-            mbar_arrive_expect_tx(bar, kAStage + kBStage);
+            // a pair's leader expects the bytes of both CTAs
+            mbar_arrive_expect_tx(bar, (PAIR ? 2u : 1u) * (kAStage + kBStage));
 #pragma unroll
             for (int sl = 0; sl < KSL; ++sl) {
               const int kx = ks * kSB + sl * kStageKBytes;
               tma_load_3d(a_dst0 + stage * kAStage + sl * kASlice, &tmap_a, kx, m0, tc.l, bar);
               const uint32_t bdst = b_dst0 + stage * kBStage + sl * kBSlice;
-              if (CM == 1)
+              if (CM == 1 || PAIR)
                 tma_load_3d(bdst, &tmap_b, kx, n0, tc.l, bar);
-              else if (PAIR)
-                tma_load_3d(bdst, &tmap_b, kx, n0 + crank * kBRows, tc.l, bar);
               else
                 tma_load_3d_mc(bdst + crank * kBPart, &tmap_b, kx, n0 + crank * kBPartRows, tc.l,
                                bar, kMask);
@@ -596,9 +620,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
       }
-      // drain: every issued load must have landed before the CTA may exit
+      // drain: every issued load must have landed before the CTA may exit.
+      // The scale copies complete on this CTA's own sff barrier.  The A/B
+      // barrier also counts the scale warps (and, in a pair, lives in the
+      // leader), so the operand producer instead waits until the MMAs have
+      // released each stage it loaded, which they do only after its bytes
+      // landed.
+      const unsigned long long t_drain = globaltimer();
       for (int s = 0; s < S; ++s)
-        if (armed & (1u << s)) drain_wait(bar_base + 8u * s, (armed_parity >> s) & 1u, p, scales ? 13u : 10u);
+        if (armed & (1u << s)) {
+          const uint32_t parity = (armed_parity >> s) & 1u;
+          if (scales) drain_wait(sff0 + 8u * s, parity, p, 13u, t_drain);
+          else drain_wait(empty0 + 8u * s, parity, p, 10u, t_drain);
+        }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
@@ -632,15 +666,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tmem + acc * TILE_N;
         for (int ks = 0; ks < p.k_stages; ++ks) {
           // operands in smem and this stage's scales in tensor memory
-          // one barrier per stage: its arrivals come after the scales are in
-          // tensor memory and (through the quarter-0 scale warp of each CTA)
-          // after the A/B tiles have landed
-          if (!BSG_WAIT(sfr0 + 8u * stage, phase, 3)) { ok = false; break; }
+          if (!BSG_WAIT(full0 + 8u * stage, phase, 3)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sfb_t = sfa_t + 4 * kCps;
-          if (ks != last) {
+          const int nm = ks == last ? last_nmma : kMmasPerStage;
 #pragma unroll
-            for (int j = 0; j < kMmasPerStage; ++j) {
+          for (int j = 0; j < kMmasPerStage; ++j) {
+            if (j < nm) {
               const int c = j / KT::kMmasPerChunk;
               const uint32_t sf_id = static_cast<uint32_t>((j % KT::kMmasPerChunk) * KT::kSfIdStep);
               const int sl = j / kMmasPerSlice, jj = j % kMmasPerSlice;
@@ -649,21 +681,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         idesc | (sf_id << 29) | (sf_id << 4), sfa_t + 4 * c, sfb_t + 4 * G * c,
                         (j != 0 || ks != 0) ? 1u : 0u);
             }
-          } else {
-#pragma unroll
-            for (int j = 0; j < kMmasPerStage; ++j) {
-              if (j < last_nmma) {
-                const int c = j / KT::kMmasPerChunk;
-                const uint32_t sf_id = static_cast<uint32_t>((j % KT::kMmasPerChunk) * KT::kSfIdStep);
-                const int sl = j / kMmasPerSlice, jj = j % kMmasPerSlice;
-                mma_issue(d_tmem, ad + ((sl * kASlice + jj * kMmaKBytes) >> 4),
-                          bd + ((sl * kBSlice + jj * kMmaKBytes) >> 4),
-                          idesc | (sf_id << 29) | (sf_id << 4), sfa_t + 4 * c, sfb_t + 4 * G * c,
-                          (j != 0 || ks != 0) ? 1u : 0u);
-              }
-            }
           }
-          // frees the smem stage (in every CTA of the cluster) once these MMAs finish
+          // frees the smem stage (in every CTA of the cluster) once these MMAs
+          // finish; issued at once, since the ring is latency-bound and every
+          // cycle of delay here delays the stage's refill
           if (PAIR) tc_commit_pair_mc(empty0 + 8u * stage, kMask);
           else if (CM == 1) tc_commit(empty0 + 8u * stage);
           else tc_commit_mc(empty0 + 8u * stage, kMask);
@@ -688,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // drain: all MMAs issued by this thread complete before exit
       if (PAIR) tc_commit_pair(drain_bar);
       else tc_commit(drain_bar);
-      drain_wait(drain_bar, 0, p, 11u);
+      drain_wait(drain_bar, 0, p, 11u, globaltimer());
     }
   } else if (warp >= kSfWarp0 && warp < kSfWarp0 + 4) {
     // --------------------------------------------------------- scale warps
@@ -716,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int landed = 1;
         if (lane == 0) landed = BSG_WAIT_SLEEP(sff0 + 8u * stage, phase, 5) ? 1 : 0;
         if (!__shfl_sync(0xFFFFFFFFu, landed, 0)) { ok = false; break; }
-        mbar_try_wait(sff0 + 8u * stage, phase);
+        mbar_test_wait(sff0 + 8u * stage, phase);
         const uint8_t* sa = smem + p.smem_sfa + stage * kSfaStage + lane_off;
         const uint8_t* sb = smem + p.smem_sfb + stage * kSfbStage + lane_off;
         const uint32_t tcol = t_row + stage * kSfCols;
@@ -749,16 +770,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
+        // one of the stage's arrivals (on the leader's barrier in a pair)
         if (lane == 0) {
-          // the quarter-0 warp also reports this CTA's A/B tiles landed, so
-          // the MMA issuer needs only this barrier (it polls on sub-partition
-          // 0, away from the MMA warp)
-          if (q == 0 && !BSG_WAIT(full0 + 8u * stage, phase, 7)) ok = false;
-          if (PAIR) mbar_arrive_cluster(mapa_shared(sfr0 + 8u * stage, 0));
-          else mbar_arrive(sfr0 + 8u * stage);
+          if (PAIR) mbar_arrive_cluster(mapa_shared(full0 + 8u * stage, 0));
+          else mbar_arrive(full0 + 8u * stage);
         }
-        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;  // the warp follows lane 0
-        if (!ok) break;
         if (++stage == S) { stage = 0; phase ^= 1u; }
       }
     }
@@ -1019,8 +1035,12 @@ struct bsg_plan {
   std::mutex mu;
   const void* map_a_ptr = nullptr;
   const void* map_b_ptr = nullptr;
+  const void* map_sfa_ptr = nullptr;
+  const void* map_sfb_ptr = nullptr;
   CUtensorMap map_a;
   CUtensorMap map_b;
+  CUtensorMap map_sfa;
+  CUtensorMap map_sfb;
 };
 
 extern "C" {
@@ -1189,7 +1209,8 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   const int G = (k.tile_n + 127) / 128;                       // scale groups the MMA reads
   const int sfb_atoms = k.tile_n % 128 == 0 ? G : G + 1;      // B scale atoms per chunk
   const int sfa_stage = chunks * ksl * kAtomBytes, sfb_stage = chunks * ksl * kAtomBytes * sfb_atoms;
-  const int b_rows = plan->pair ? k.tile_n / 2 : k.tile_n;  // B rows held per CTA
+  // B rows held per CTA: whole 128-row boxes (a 224-wide pair's half is loaded as 128 rows)
+  const int b_rows = plan->pair ? (k.tile_n / 2 + 127) / 128 * 128 : k.tile_n;
   const int per_stage = kTileM * stage_k_bytes + b_rows * stage_k_bytes + sfa_stage + sfb_stage;
   const int reserve = 1024 /* alignment slack */ + 512 /* barriers and flags */;
   int stages = (max_smem - reserve) / per_stage;
@@ -1206,7 +1227,7 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   k.smem_sfa = k.smem_b + stages * b_rows * stage_k_bytes;
   k.smem_sfb = k.smem_sfa + stages * sfa_stage;
   k.smem_bar = k.smem_sfb + stages * sfb_stage;
-  plan->smem_bytes = static_cast<int>(k.smem_bar) + 32 * stages + 16 * num_acc + 8 + 16 + 1024;
+  plan->smem_bytes = static_cast<int>(k.smem_bar) + 24 * stages + 16 * num_acc + 8 + 16 + 1024;
   k.wait_limit_ns = 1000000000ull;  // one second per wait
   if (const char* e = std::getenv("BSG_WAIT_LIMIT_NS")) {
     const unsigned long long v = std::strtoull(e, nullptr, 10);
@@ -1292,6 +1313,25 @@ static bool encode_operand(CUtensorMap* map, const void* ptr, int64_t row_bytes,
   return r == CUDA_SUCCESS;
 }
 
+// Scale atoms as a 4-D tensor of 8-byte words: (64 words of one 512-byte
+// atom, t_k atoms along K, t_mn atoms along M or N, L); the box is one
+// stage's `k_atoms` K atoms of `mn_atoms` consecutive MN atoms.
+static bool encode_scales(CUtensorMap* map, const void* ptr, int64_t t_k, int64_t t_mn, int64_t L,
+                          int k_atoms, int mn_atoms) {
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(t_k), static_cast<cuuint64_t>(t_mn),
+                        static_cast<cuuint64_t>(L)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(kAtomBytes),
+                           static_cast<cuuint64_t>(kAtomBytes * t_k),
+                           static_cast<cuuint64_t>(kAtomBytes * t_k * t_mn)};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(k_atoms), static_cast<cuuint32_t>(mn_atoms), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = get_encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, const_cast<void*>(ptr),
+                                     dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const void* SFA,
                    const void* SFB, void* C, float* amax, void* ws, size_t ws_bytes,
                    void* stream) {
@@ -1312,7 +1352,7 @@ bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const vo
   k.c = C;
   k.amax = amax;
   k.ws = static_cast<uint32_t*>(ws);
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, msfa, msfb;
   {
     std::lock_guard<std::mutex> lock(plan->mu);
     if (plan->map_a_ptr != A) {
@@ -1323,16 +1363,36 @@ bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const vo
       plan->map_a_ptr = A;
     }
     if (plan->map_b_ptr != B) {
-      if (!encode_operand(&plan->map_b, B, row_bytes, pr.N, pr.L, k.tile_n / plan->cluster_m)) {
+      const int b_box = plan->pair ? (k.tile_n / 2 + 127) / 128 * 128 : k.tile_n / plan->cluster_m;
+      if (!encode_operand(&plan->map_b, B, row_bytes, pr.N, pr.L, b_box)) {
         plan->map_b_ptr = nullptr;
         return BSG_ERR_CUDA;
       }
       plan->map_b_ptr = B;
     }
+    const int chunks = plan->kind == kKindF8F6F4 ? 1 : (plan->kind == kKindF4x4X ? 4 : 2);
+    const int k_atoms = chunks * plan->kslices;
+    const int sfb_atoms = k.tile_n % 128 == 0 ? (k.tile_n + 127) / 128 : (k.tile_n + 127) / 128 + 1;
+    if (plan->map_sfa_ptr != SFA) {
+      if (!encode_scales(&plan->map_sfa, SFA, k.t_k, k.t_m, pr.L, k_atoms, 1)) {
+        plan->map_sfa_ptr = nullptr;
+        return BSG_ERR_CUDA;
+      }
+      plan->map_sfa_ptr = SFA;
+    }
+    if (plan->map_sfb_ptr != SFB) {
+      if (!encode_scales(&plan->map_sfb, SFB, k.t_k, k.t_n, pr.L, k_atoms, sfb_atoms)) {
+        plan->map_sfb_ptr = nullptr;
+        return BSG_ERR_CUDA;
+      }
+      plan->map_sfb_ptr = SFB;
+    }
     ma = plan->map_a;
     mb = plan->map_b;
+    msfa = plan->map_sfa;
+    msfb = plan->map_sfb;
   }
-  void* args[3] = {&ma, &mb, &k};
+  void* args[5] = {&ma, &mb, &msfa, &msfb, &k};
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(plan->grid);
