@@ -54,6 +54,7 @@ constexpr int kEpiWarps = 8;
 constexpr int kSfProdWarp = kEpiWarp0 + kEpiWarps;
 constexpr int kThreads = 32 * (kSfProdWarp + 1);
 constexpr int kAtomBytes = 512;    // one scale atom: 128 rows x 4 K-blocks
+constexpr int kEpiStageBytes = 2048;  // per epilogue warp: 32 rows x 64 bytes of C
 constexpr uint32_t kTmemCols = 512;
 
 // error word bits (workspace word 2); word 3 keeps where the first wait gave up
@@ -74,7 +75,7 @@ struct Params {
   int c_dtype;            // bsg_dtype
   int c_major;            // 0 = n-major, 1 = m-major
   uint32_t idesc;         // instruction descriptor, scale ids zero
-  uint32_t smem_a, smem_b, smem_sfa, smem_sfb, smem_bar;  // offsets in dynamic smem
+  uint32_t smem_a, smem_b, smem_sfa, smem_sfb, smem_epi, smem_bar;  // offsets in dynamic smem
   const uint8_t* sfa;
   const uint8_t* sfb;
   void* c;
@@ -421,6 +422,36 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Para
   (mbar_test_wait((bar), (parity)) || wait_slow((bar), (parity), p, abort_flag, (site), 128u))
 
 __device__ __forceinline__ uint32_t abs_bits_f32(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
+
+// A warp's 32 rows of W 32-bit words (row t in lane t's v[0..W)) to global
+// memory, row-major with a pitch of `pitch` bytes from `g` (row 0, word 0),
+// through the warp's 2 KB staging buffer `stg`.  Each store instruction then
+// writes W/4 lanes x 16 contiguous bytes per row (8 rows x 64 bytes for
+// W = 16) instead of 32 scattered 16-byte pieces.  The 16-byte pieces of a
+// row sit XOR-swizzled by (row / 2) % 4, which keeps both the row-per-lane
+// writes and the piece-per-lane reads free of bank conflicts.  Rows from
+// `rows_valid` and bytes from `bytes_valid` (multiples of 16) on are not
+// written.
+template <int W>
+__device__ __forceinline__ void store_rows_coalesced(uint8_t* stg, const uint32_t* v, int lane, char* g,
+                                                     size_t pitch, int rows_valid, int bytes_valid) {
+  static_assert(W == 8 || W == 16, "a staged row chunk is 32 or 64 bytes");
+  constexpr int L = W / 4;    // lanes (16-byte pieces) per row
+  constexpr int RP = 32 / L;  // rows per store instruction
+  __syncwarp();               // the previous chunk's reads are done
+#pragma unroll
+  for (int pc = 0; pc < L; ++pc)
+    *reinterpret_cast<uint4*>(stg + lane * 64 + ((pc ^ ((lane >> 1) & 3)) * 16)) =
+        make_uint4(v[4 * pc], v[4 * pc + 1], v[4 * pc + 2], v[4 * pc + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < L; ++k) {
+    const int r = lane / L + RP * k, pc = lane % L;
+    const uint4 x = *reinterpret_cast<const uint4*>(stg + r * 64 + ((pc ^ ((r >> 1) & 3)) * 16));
+    if (r < rows_valid && pc * 16 < bytes_valid)
+      *reinterpret_cast<uint4*>(g + static_cast<size_t>(r) * pitch + pc * 16) = x;
+  }
+}
 
 // Bounded wait for the drains at exit (no abort flag: always runs).  It
 // waits for this CTA's own copies and MMAs, which finish by themselves, so
@@ -789,6 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kCols = TILE_N / 2;
     const int q = warp & 3;
     const int h = (warp - kEpiWarp0) >> 2;
+    uint8_t* const stg = smem + p.smem_epi + (warp - kEpiWarp0) * kEpiStageBytes;
     uint32_t vmax = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -852,12 +884,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         release();
         uint16_t* const cbase = static_cast<uint16_t*>(p.c) + batch_off;
         if (p.c_major == 0) {
-          uint16_t* dst = cbase + static_cast<size_t>(row) * p.N + n0;
+          // 32-column chunks (64 bytes per row) through the staging buffer;
+          // a 112-column half ends with a 16-column chunk
+          const int row0 = tc.mt * kTileM + q * 32;
+          char* const g0 = reinterpret_cast<char*>(cbase + static_cast<size_t>(row0) * p.N + n0);
+          const size_t pitch = static_cast<size_t>(p.N) * 2;
 #pragma unroll
-          for (int i = 0; i < kCols; i += 8)
-            if (row_ok && n0 + i < p.N)
-              *reinterpret_cast<uint4*>(dst + i) =
-                  make_uint4(pk[i / 2], pk[i / 2 + 1], pk[i / 2 + 2], pk[i / 2 + 3]);
+          for (int cc = 0; cc + 32 <= kCols; cc += 32)
+            store_rows_coalesced<16>(stg, pk + cc / 2, lane, g0 + cc * 2, pitch, p.M - row0,
+                                     (p.N - n0 - cc) * 2);
+          if (kCols % 32 == 16)
+            store_rows_coalesced<8>(stg, pk + (kCols - 16) / 2, lane, g0 + (kCols - 16) * 2, pitch,
+                                    p.M - row0, (p.N - n0 - (kCols - 16)) * 2);
         } else {
           // m-major: column by column, the 32 lanes write 32 consecutive rows
           uint16_t* dst = cbase + static_cast<size_t>(n0) * p.M + row;
@@ -885,15 +923,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (pass == 1) release();
           const int nb = n0 + c0 * 16;
           if (p.c_major == 0) {
-            float* dst = cbase + static_cast<size_t>(row) * p.N + nb;
+            // each 16-column chunk (64 bytes per row) through the staging buffer
+            const int row0 = tc.mt * kTileM + q * 32;
+            char* const g0 = reinterpret_cast<char*>(cbase + static_cast<size_t>(row0) * p.N + nb);
+            const size_t pitch = static_cast<size_t>(p.N) * 4;
 #pragma unroll
-            for (int i = 0; i < kP1 * 16; i += 4) {
-              if (i < cn * 16 && row_ok && nb + i < p.N) {
-                float4 v = make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
-                                       __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-                vmax = max(vmax, max(max(abs_bits_f32(v.x), abs_bits_f32(v.y)),
-                                     max(abs_bits_f32(v.z), abs_bits_f32(v.w))));
-                *reinterpret_cast<float4*>(dst + i) = v;
+            for (int i = 0; i < kP1; ++i) {
+              if (i < cn) {
+                // only stored elements count toward Amax
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  if (row_ok && nb + 16 * i + j < p.N)
+                    vmax = max(vmax, abs_bits_f32(__uint_as_float(r[16 * i + j])));
+                store_rows_coalesced<16>(stg, r + 16 * i, lane, g0 + 16 * i * 4, pitch, p.M - row0,
+                                         (p.N - nb - 16 * i) * 4);
               }
             }
           } else {
@@ -1212,7 +1255,8 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   // B rows held per CTA: whole 128-row boxes (a 224-wide pair's half is loaded as 128 rows)
   const int b_rows = plan->pair ? (k.tile_n / 2 + 127) / 128 * 128 : k.tile_n;
   const int per_stage = kTileM * stage_k_bytes + b_rows * stage_k_bytes + sfa_stage + sfb_stage;
-  const int reserve = 1024 /* alignment slack */ + 512 /* barriers and flags */;
+  const int reserve = 1024 /* alignment slack */ + 512 /* barriers and flags */ +
+                      kEpiWarps * kEpiStageBytes /* epilogue staging */;
   int stages = (max_smem - reserve) / per_stage;
   if (stages > 8) stages = 8;
   const int sf_cols = 4 * chunks * ksl * (1 + G);
@@ -1226,7 +1270,8 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   k.smem_b = k.smem_a + stages * kTileM * stage_k_bytes;
   k.smem_sfa = k.smem_b + stages * b_rows * stage_k_bytes;
   k.smem_sfb = k.smem_sfa + stages * sfa_stage;
-  k.smem_bar = k.smem_sfb + stages * sfb_stage;
+  k.smem_epi = k.smem_sfb + stages * sfb_stage;
+  k.smem_bar = k.smem_epi + kEpiWarps * kEpiStageBytes;
   plan->smem_bytes = static_cast<int>(k.smem_bar) + 24 * stages + 16 * num_acc + 8 + 16 + 1024;
   k.wait_limit_ns = 1000000000ull;  // one second per wait
   if (const char* e = std::getenv("BSG_WAIT_LIMIT_NS")) {
