@@ -821,7 +821,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int h = (warp - kEpiWarp0) >> 2;
     uint8_t* const stg = smem + p.smem_epi + (warp - kEpiWarp0) * kEpiStageBytes;
-    uint32_t vmax = 0;
+    uint32_t vmax = 0;  // max |stored value| as fp32 bits
+    // 16-bit C: the largest magnitudes kept as two packed 16-bit halves (the
+    // magnitude bits of a 16-bit float order like its value, so an unsigned
+    // SIMD max finds it), widened to fp32 bits once at the end
+    uint32_t vmax16 = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = unit0; u < p.num_units; u += unit_step) {
@@ -857,27 +861,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cc = 0; cc < kCols; cc += 16) {
           uint32_t* r = rb[(cc / 16) & 1];
           if (cc + 16 < kCols) tc_ld_32x32b_x16(taddr + cc + 16, rb[((cc / 16) + 1) & 1]);
+          // the whole chunk is stored (all but a ragged edge)
+          const bool whole = row_ok && n0 + cc + 16 <= p.N;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float f0 = __uint_as_float(r[2 * j]), f1 = __uint_as_float(r[2 * j + 1]);
-            uint32_t h0, h1, b0, b1;
+            // two round-to-nearest-even conversions in one: low half column
+            // cc + 2j, high half column cc + 2j + 1
+            uint32_t h;
             if (bf) {
-              h0 = __bfloat16_as_ushort(__float2bfloat16_rn(f0));
-              h1 = __bfloat16_as_ushort(__float2bfloat16_rn(f1));
-              b0 = (h0 << 16) & 0x7FFFFFFFu;
-              b1 = (h1 << 16) & 0x7FFFFFFFu;
+              const __nv_bfloat162 v = __floats2bfloat162_rn(f0, f1);
+              h = *reinterpret_cast<const uint32_t*>(&v);
             } else {
-              const __half x0 = __float2half_rn(f0), x1 = __float2half_rn(f1);
-              h0 = __half_as_ushort(x0);
-              h1 = __half_as_ushort(x1);
-              b0 = abs_bits_f32(__half2float(x0));
-              b1 = abs_bits_f32(__half2float(x1));
+              const __half2 v = __floats2half2_rn(f0, f1);
+              h = *reinterpret_cast<const uint32_t*>(&v);
             }
+            pk[cc / 2 + j] = h;
             // only stored elements count toward Amax
-            const int n = n0 + cc + 2 * j;
-            if (row_ok && n < p.N) vmax = max(vmax, b0);
-            if (row_ok && n + 1 < p.N) vmax = max(vmax, b1);
-            pk[cc / 2 + j] = h0 | (h1 << 16);
+            uint32_t m = h & 0x7FFF7FFFu;
+            if (!whole) {
+              const int n = n0 + cc + 2 * j;
+              if (!(row_ok && n < p.N)) m &= 0xFFFF0000u;
+              if (!(row_ok && n + 1 < p.N)) m &= 0x0000FFFFu;
+            }
+            vmax16 = __vmaxu2(vmax16, m);
           }
           tc_wait_ld();
         }
@@ -931,10 +938,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < kP1; ++i) {
               if (i < cn) {
                 // only stored elements count toward Amax
+                if (row_ok && nb + 16 * i + 16 <= p.N) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                  if (row_ok && nb + 16 * i + j < p.N)
-                    vmax = max(vmax, abs_bits_f32(__uint_as_float(r[16 * i + j])));
+                  for (int j = 0; j < 16; ++j) vmax = max(vmax, r[16 * i + j] & 0x7FFFFFFFu);
+                } else {
+#pragma unroll
+                  for (int j = 0; j < 16; ++j)
+                    if (row_ok && nb + 16 * i + j < p.N) vmax = max(vmax, r[16 * i + j] & 0x7FFFFFFFu);
+                }
                 store_rows_coalesced<16>(stg, r + 16 * i, lane, g0 + 16 * i * 4, pitch, p.M - row0,
                                          (p.N - nb - 16 * i) * 4);
               }
@@ -954,6 +965,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+    }
+    {
+      const uint32_t hmax = max(vmax16 & 0xFFFFu, vmax16 >> 16);
+      vmax = max(vmax, p.c_dtype == BSG_BF16
+                           ? hmax << 16
+                           : abs_bits_f32(__half2float(__ushort_as_half(static_cast<unsigned short>(hmax)))));
     }
     vmax = __reduce_max_sync(0xFFFFFFFFu, vmax);
     if (lane == 0) atomicMax(cta_amax, vmax);
