@@ -4,22 +4,26 @@
 //   C[m,n,l] = sum_k dec(A[m,k,l]) 2^(SFA[m,k/sfv,l]-127) * dec(B[n,k,l]) 2^(SFB[n,k/sfv,l]-127)
 //   Amax     = max |C|  (over the values as stored in C's dtype)
 //
-// Kernel design (one persistent CTA per SM, 14 warps):
-//   warp 0      TMA producer: per K stage, the 128 x 128-byte A tile and the
-//               TILE_N x 128-byte B tile (128-byte swizzle, 3-D tensor maps
-//               over (K bytes, rows, L), out-of-range rows/columns zero
-//               filled), plus the 512-byte scale atoms of those rows (bulk
-//               copies straight from the page's physical atom layout).
-//   warp 1      MMA issuer: once a stage's operands are in shared memory and
-//               its scales in tensor memory, issues block-scaled tcgen05.mma (kind::mxf8f6f4 scale_vec::1X for FP8,
-//               kind::mxf4nvf4 scale_vec::4X / 2X for packed FP4) into a
-//               double-buffered fp32 accumulator in tensor memory; commits
-//               free the smem stage and publish a finished accumulator.
+// Kernel design (one persistent CTA per SM, 15 warps; by default two CTAs
+// of a cluster form a cta_group::2 pair running 256-row MMAs):
+//   warp 0      operand producer: per K stage, the 128 x 128-byte A tile and
+//               the B tile (its half in a pair, always whole 128-row boxes)
+//               through 3-D tensor maps (128-byte swizzle, out-of-range rows
+//               and columns zero-filled).  In a pair both CTAs count their
+//               bytes on the leader's stage barrier.
+//   warp 1      MMA issuer (the leader's, in a pair): once a stage is ready,
+//               block-scaled tcgen05.mma (kind::mxf8f6f4 scale_vec::1X for
+//               FP8, kind::mxf4nvf4 scale_vec::4X / 2X for packed FP4) into
+//               fp32 accumulators in tensor memory; commits free the smem stage
+//               and publish a finished accumulator.
 //   warps 2..5  scale warps: tcgen05.st of each stage's scale atoms from
-//               shared into tensor memory (one warp per lane quarter).
+//               shared into tensor memory (one warp per lane quarter), then
+//               an arrival on the stage barrier.
 //   warps 6..13 epilogue: tcgen05.ld the accumulator (one row per thread),
-//               round to C's dtype, store, and keep max |stored value| as an
-//               integer max of the float bits; at exit one atomicMax per CTA.
+//               round to C's dtype, keep max |stored value| as an integer max
+//               of the float bits, store through a per-warp staging buffer.
+//   warp 14     scale producer: each stage's scale atoms in two 4-D tensor
+//               copies, on their own barrier, ahead of the operand tiles.
 //   The last CTA to finish writes Amax and re-zeroes the workspace slots.
 //
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
@@ -47,7 +51,7 @@ constexpr int kStageKBytes = 128;  // bytes of K per operand row per stage (one 
 constexpr int kMmaKBytes = 32;     // bytes of K per tcgen05.mma (32 FP8 or 64 FP4 elements)
 // Warp roles: 0 operand producer (A/B tiles), 1 MMA issuer, 2-5 scale warps
 // (tensor-memory lane quarters 2, 3, 0, 1), 6-13 epilogue (two warps per lane
-// quarter), 14 scale producer (bulk copies of the scale atoms).
+// quarter), 14 scale producer (tensor copies of the scale atoms).
 constexpr int kSfWarp0 = 2;
 constexpr int kEpiWarp0 = 6;
 constexpr int kEpiWarps = 8;
