@@ -40,9 +40,9 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # comments and whitespace removed, so only a code change invalidates an
 # entry) and workload.
 TRAFFIC = {
-    ("929ad3071d94734b", 2): 37115904,
-    ("929ad3071d94734b", 3): 417080320,
-    ("929ad3071d94734b", 4): 202603776,
+    ("52da3c12e74b3b92", 2): 37115904,
+    ("52da3c12e74b3b92", 3): 417080320,
+    ("52da3c12e74b3b92", 4): 202603776,
 }
 
 
