@@ -15,6 +15,10 @@ functions follow the page's section "Equations":
 * ``round_to``      -- C rounded to the output dtype (round-to-nearest-even)
 * ``ulp``, ``tolerance`` -- tau = 1e-5 * S + ulp_c(|C_ref|)
 * ``reference``     -- C_ref, S, tau and Amax = max |C_ref| for a whole problem
+* ``quantize``      -- the row upstream of the GEMM: real values -> element
+  codes + E8M0 scales in the atom layout ("GEMM + RoPE + MXFP8 Projection
+  (SM100)", "Equations"; the block-scale rule is the reading stated in
+  bsg_oracle.c); ``quantize_value`` rounds one scaled value
 
 Parity unpinned: the split of a row index mn = m0 + 32*m1 inside a 128-row
 scale atom is the column-major reading of the atom's shape (32, 4); the pages
@@ -87,6 +91,11 @@ def _load():
     lib.bsgo_round_array.restype = ctypes.c_int
     lib.bsgo_tolerance.argtypes = [dp, dp, ctypes.c_int64, ctypes.c_int, ctypes.c_double, dp]
     lib.bsgo_tolerance.restype = ctypes.c_int
+    lib.bsgo_quantize_value.argtypes = [ctypes.c_double, ctypes.c_int]
+    lib.bsgo_quantize_value.restype = ctypes.c_int
+    lib.bsgo_quantize.argtypes = [dp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                  ctypes.c_int, ctypes.c_int, u8p, u8p]
+    lib.bsgo_quantize.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -210,3 +219,40 @@ def reference(M, N, K, L, a_dtype, b_dtype, sfv, A, B, SFA, SFB, c_dtype, sf_dty
     cref = round_to(C, c_dtype)
     tau = tolerance(cref, S, c_dtype)
     return {"c": cref, "exact": C, "s": S, "tau": tau, "amax": float(np.max(np.abs(cref)))}
+
+
+def quant_sizes(rows: int, cols: int, L: int, out_dtype: str, sfv: int):
+    """(code bytes, scale bytes) of a quantized (rows, cols, L) tensor; the
+    scales cover whole (padded) atoms."""
+    t_r = -(-rows // 128)
+    t_k = -(-(cols // sfv) // 4)
+    code_bytes = L * rows * (cols // 2 if out_dtype == "e2m1" else cols)
+    return code_bytes, L * t_r * t_k * 512
+
+
+def quantize_value(y: float, out_dtype: str) -> int:
+    """Code of the out_dtype value nearest to y (ties to even, saturating)."""
+    c = _load().bsgo_quantize_value(float(y), DTYPES[out_dtype])
+    if c < 0:
+        raise ValueError(out_dtype)
+    return int(c)
+
+
+def quantize(X: np.ndarray, out_dtype: str, sfv: int):
+    """X (L, rows, cols) real values -> (codes uint8 (L, rows, cols or cols/2),
+    scales uint8 (L, t_r, t_k, 32, 4, 4))."""
+    X = np.ascontiguousarray(X, dtype=np.float64)
+    if X.ndim == 2:
+        X = X[None]
+    L, rows, cols = X.shape
+    code_bytes, sf_bytes = quant_sizes(rows, cols, L, out_dtype, sfv)
+    codes = np.zeros(code_bytes, dtype=np.uint8)
+    sf = np.zeros(sf_bytes, dtype=np.uint8)
+    rc = _load().bsgo_quantize(_ptr(X), int(rows), int(cols), int(L), DTYPES[out_dtype],
+                               int(sfv), _ptr(codes), _ptr(sf))
+    if rc != 0:
+        raise ValueError("unsupported quantize request")
+    t_r = -(-rows // 128)
+    t_k = -(-(cols // sfv) // 4)
+    return (codes.reshape(L, rows, -1), sf.reshape(L, t_r, t_k, 32, 4, 4))
+

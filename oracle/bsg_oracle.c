@@ -465,3 +465,133 @@ int bsgo_tolerance(const double *cref, const double *S, int64_t n, int c_dtype,
     for (i = 0; i < n; i++) tau[i] = rel * S[i] + bsgo_ulp(cref[i], c_dtype);
     return 0;
 }
+
+/* ----------------------------------------------------------- MX quantizer */
+/*
+ * The row upstream of the GEMM: real values X (rows, cols, L), cols
+ * contiguous, become element codes of out_dtype plus one E8M0 scale per
+ * sf_vec_size consecutive elements of a row, the scales written in the atom
+ * layout of bsgo_sf_offset.  "GEMM + RoPE + MXFP8 Projection (SM100)",
+ * section "Equations", names the operation (MXFP8 quantize: an E8M0 scale per
+ * block of 32, E4M3 data); "GEMM + Amax (SM100)" gives the scale layout and
+ * the E5M2 / packed E2M1 element formats the GEMM consumes.  The pages do not
+ * spell out how a block's scale is chosen.  The reading used here (and by the
+ * CUDA path) takes the block's largest magnitude to the top binade of the
+ * element format:
+ *   amax  = max |x| over the block
+ *   e     = floor(log2 amax) - emax(out_dtype)      (E4M3 8, E5M2 15, E2M1 2)
+ *   e     clamped to [-127, 127]; scale = 2^e; scale byte = e + 127
+ *   code  = the value of out_dtype nearest to x / scale, ties to the even
+ *           code; magnitudes past the largest finite value saturate to it;
+ *           the sign of x is kept (a negative value rounding to zero is -0)
+ * Special blocks: all zeros -> byte 127 (scale 1); any NaN or infinity ->
+ * byte 0xFF (E8M0 NaN) and every code of the block the format's NaN code
+ * (E4M3 0x7F, E5M2 0x7F; E2M1 has none, so its codes are 0).  Scale bytes of
+ * padding positions (rows past `rows`, blocks past cols/sfv inside the last
+ * atoms) are 127.
+ * Parity: pinned by hand-worked blocks, by torch's float8 conversions of the
+ * scaled values, by an exhaustive E2M1 grid, and by invariants (rounding
+ * error bound, scale invariance, sign symmetry, exact round trips).
+ */
+
+static int quant_format(int dtype, int *emax, unsigned *maxc, unsigned *sign, unsigned *nanc)
+{
+    switch (dtype) {
+    case BSGO_E4M3: *emax = 8;  *maxc = 0x7Eu; *sign = 0x80u; *nanc = 0x7Fu; return 0;
+    case BSGO_E5M2: *emax = 15; *maxc = 0x7Bu; *sign = 0x80u; *nanc = 0x7Fu; return 0;
+    case BSGO_E2M1: *emax = 2;  *maxc = 0x7u;  *sign = 0x8u;  *nanc = 0x0u;  return 0;
+    default: return -1;
+    }
+}
+
+/* Code of the out_dtype value nearest to y (finite), ties to the even code,
+ * saturating; the non-negative codes 0..maxc decode in increasing order. */
+static unsigned nearest_code(double y, const double *tab, unsigned maxc, unsigned sign)
+{
+    double a = fabs(y);
+    unsigned lo = 0u, hi = maxc, c;
+    if (a >= tab[maxc]) {
+        c = maxc;
+    } else {
+        /* largest c with tab[c] <= a (tab[0] = 0 <= a) */
+        while (lo < hi) {
+            unsigned mid = (lo + hi + 1u) / 2u;
+            if (tab[mid] <= a) lo = mid; else hi = mid - 1u;
+        }
+        c = lo;
+        if (tab[c] != a) {
+            double d_lo = a - tab[c], d_hi = tab[c + 1u] - a;
+            if (d_hi < d_lo || (d_hi == d_lo && ((c + 1u) & 1u) == 0u)) c = c + 1u;
+        }
+    }
+    return signbit(y) ? (c | sign) : c;
+}
+
+/* One element: the code of y under out_dtype (after scaling), or -1. */
+int bsgo_quantize_value(double y, int out_dtype)
+{
+    int emax;
+    unsigned maxc, sign, nanc;
+    double tab[256];
+    if (quant_format(out_dtype, &emax, &maxc, &sign, &nanc) != 0) return -1;
+    bsgo_decode_table(out_dtype, tab);
+    if (isnan(y) || isinf(y)) return (int)nanc;
+    return (int)nearest_code(y, tab, maxc, sign);
+}
+
+/* X: rows*cols*L doubles, element (l, r, k) at (l*rows + r)*cols + k.
+ * codes: (l*rows + r)*cols + k bytes for FP8; for E2M1 two per byte, element
+ * k in the low nibble of byte k/2 when k is even.  sf: the whole padded atom
+ * tensor, L * ceil(rows/128) * ceil(cols/sfv/4) * 512 bytes.  Returns 0, or -1
+ * for an unsupported request (unknown dtype, sfv not 16/32, cols not a
+ * multiple of sfv). */
+int bsgo_quantize(const double *X, int64_t rows, int64_t cols, int64_t L, int out_dtype,
+                  int sfv, uint8_t *codes, uint8_t *sf)
+{
+    int emax;
+    unsigned maxc, sign, nanc;
+    double tab[256];
+    int64_t nblk, t_r, t_k, l, r, b, k;
+    if (quant_format(out_dtype, &emax, &maxc, &sign, &nanc) != 0) return -1;
+    if ((sfv != 16 && sfv != 32) || rows < 1 || cols < 1 || L < 1 || cols % sfv != 0) return -1;
+    bsgo_decode_table(out_dtype, tab);
+    nblk = cols / sfv;
+    t_r = ceil_div(rows, 128);
+    t_k = ceil_div(nblk, 4);
+    memset(sf, 127, (size_t)(L * t_r * t_k * 512));
+    for (l = 0; l < L; l++)
+        for (r = 0; r < rows; r++)
+            for (b = 0; b < nblk; b++) {
+                const double *x = X + (l * rows + r) * cols + b * sfv;
+                double amax = 0.0, scale = 1.0;
+                int nonfinite = 0, e = 0, E;
+                unsigned byte = 127u;
+                for (k = 0; k < sfv; k++) {
+                    if (isnan(x[k]) || isinf(x[k])) nonfinite = 1;
+                    else if (fabs(x[k]) > amax) amax = fabs(x[k]);
+                }
+                if (nonfinite) {
+                    byte = 0xFFu;
+                } else if (amax > 0.0) {
+                    frexp(amax, &E);            /* amax = f * 2^E, f in [0.5, 1) */
+                    e = (E - 1) - emax;         /* floor(log2 amax) - emax */
+                    if (e < -127) e = -127;
+                    if (e > 127) e = 127;
+                    byte = (unsigned)(e + 127);
+                    scale = ldexp(1.0, e);
+                }
+                sf[bsgo_sf_offset(r, b, l, t_r, t_k)] = (uint8_t)byte;
+                for (k = 0; k < sfv; k++) {
+                    const int64_t idx = (l * rows + r) * cols + b * sfv + k;
+                    unsigned c = nonfinite ? nanc : nearest_code(x[k] / scale, tab, maxc, sign);
+                    if (out_dtype == BSGO_E2M1) {
+                        uint8_t *p = codes + idx / 2;
+                        if ((idx & 1) == 0) *p = (uint8_t)((*p & 0xF0u) | c);
+                        else *p = (uint8_t)((*p & 0x0Fu) | (c << 4));
+                    } else {
+                        codes[idx] = (uint8_t)c;
+                    }
+                }
+            }
+    return 0;
+}

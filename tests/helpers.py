@@ -72,8 +72,9 @@ def load_golden(name):
         return json.load(f)
 
 
-def golden_names():
-    return sorted(n for n in os.listdir(GOLDEN) if n.endswith(".json"))
+def golden_names(prefix="ex"):
+    """Fixture files of one kind: ``ex*`` GEMM examples, ``q*`` quantizer blocks."""
+    return sorted(n for n in os.listdir(GOLDEN) if n.startswith(prefix) and n.endswith(".json"))
 
 
 def build_golden_inputs(g):

@@ -1,0 +1,237 @@
+"""Pins of the oracle's MX quantizer (the row upstream of the GEMM) to things
+other than itself.
+
+* **Hand-worked blocks** (``tests/golden/q*.json``): each with its citation
+  and derivation.
+* **Element rounding:** against torch's float8 conversions of float32 values,
+  which round to nearest even; E2M1 against an exhaustive grid worked with
+  exact fractions.
+* **Defining properties:**
+  - the block maximum lands in the element format's top binade;
+  - the rounding error stays within half a step of the element format;
+  - negating the input flips only the sign bits;
+  - scaling by 2^j moves only the scale bytes;
+  - an already-quantized tensor with a top-binade element in every block
+    round-trips exactly through the pinned dequantizer;
+  - special blocks and atom padding behave as stated.
+* **A third implementation:** the input generator's numpy/torch quantizer,
+  on ordinary data.
+
+No GPU needed.
+"""
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import E2M1_VALUES, golden_names
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+EMAX = {"e4m3": 8, "e5m2": 15, "e2m1": 2}
+MAXV = {"e4m3": 448.0, "e5m2": 57344.0, "e2m1": 6.0}
+SIGN = {"e4m3": 0x80, "e5m2": 0x80, "e2m1": 0x8}
+
+
+def code_at(codes, dtype, l, r, k):
+    if dtype == "e2m1":
+        b = int(codes[l, r, k // 2])
+        return b & 0xF if k % 2 == 0 else b >> 4
+    return int(codes[l, r, k])
+
+
+def unpack(codes, dtype):
+    """Codes as one integer per element, shape (L, rows, cols)."""
+    if dtype != "e2m1":
+        return codes.astype(np.int64)
+    lo = (codes & 0xF).astype(np.int64)
+    hi = (codes >> 4).astype(np.int64)
+    out = np.empty(codes.shape[:2] + (codes.shape[2] * 2,), dtype=np.int64)
+    out[..., 0::2] = lo
+    out[..., 1::2] = hi
+    return out
+
+
+def scale_bytes(sf, rows, nblk):
+    """Scale bytes as (L, rows, nblk), through the pinned atom offsets."""
+    L, t_r, t_k = sf.shape[:3]
+    flat = sf.reshape(-1)
+    out = np.empty((L, rows, nblk), dtype=np.int64)
+    for l in range(L):
+        for r in range(rows):
+            for b in range(nblk):
+                out[l, r, b] = flat[oracle.sf_offset(r, b, l, t_r, t_k)]
+    return out
+
+
+@pytest.mark.parametrize("name", golden_names("q"))
+def test_golden_blocks(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        g = json.load(f)
+    X = np.zeros((1, g["rows"], g["cols"]))
+    for k, v in g.get("x_set", []):
+        X[0, 0, k] = v
+    for r, k, v in g.get("x_set_rc", []):
+        X[0, r, k] = v
+    codes, sf = oracle.quantize(X, g["out_dtype"], g["sfv"])
+    for k, v in g.get("expect_codes", []):
+        assert code_at(codes, g["out_dtype"], 0, 0, k) == v, (name, k)
+    for r, k, v in g.get("expect_codes_rc", []):
+        assert code_at(codes, g["out_dtype"], 0, r, k) == v, (name, r, k)
+    t_r, t_k = sf.shape[1], sf.shape[2]
+    for r, b, v in g["expect_scale_bytes"]:
+        assert int(sf.reshape(-1)[oracle.sf_offset(r, b, 0, t_r, t_k)]) == v, (name, r, b)
+
+
+@pytest.mark.parametrize("dtype,tdt", [("e4m3", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)])
+def test_element_rounding_matches_torch(dtype, tdt):
+    rng = np.random.default_rng(7)
+    m = MAXV[dtype]
+    # float32 inputs (torch then rounds once), spread over every binade in range
+    mag = np.exp2(rng.uniform(-20, np.log2(m), 20000)).astype(np.float32)
+    y = (mag * rng.choice([-1, 1], mag.size)).astype(np.float32)
+    y = y[np.abs(y) <= m]
+    # exact ties: midpoints between neighbouring codes
+    tab = oracle.decode_table(dtype)
+    finite = [c for c in range(0x80) if np.isfinite(tab[c])]
+    mids = np.array([(tab[c] + tab[c + 1]) / 2 for c in finite[:-1]], dtype=np.float64)
+    mids = mids[mids.astype(np.float32) == mids].astype(np.float32)
+    y = np.concatenate([y, mids, -mids, np.float32([0.0, -0.0, m, -m])])
+    want = torch.from_numpy(y).to(tdt).view(torch.uint8).numpy()
+    got = np.array([oracle.quantize_value(float(v), dtype) for v in y], dtype=np.uint8)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("dtype", ["e4m3", "e5m2", "e2m1"])
+def test_saturation(dtype):
+    m = MAXV[dtype]
+    maxc = oracle.quantize_value(m, dtype)
+    for y in (m * 1.01, m * 1.5, m * 8, 1e30):
+        assert oracle.quantize_value(y, dtype) == maxc
+        assert oracle.quantize_value(-y, dtype) == maxc | SIGN[dtype]
+
+
+def test_e2m1_exhaustive_grid():
+    vals = [Fraction(v).limit_denominator(4) for v in E2M1_VALUES[:8]]  # 0 .. 6, codes 0 .. 7
+    for i in range(-8 * 64, 8 * 64 + 1):
+        y = Fraction(i, 64)
+        a = abs(y)
+        if a >= vals[-1]:
+            c = 7
+        else:
+            best = min(range(8), key=lambda c: (abs(vals[c] - a), c & 1))
+            c = best
+        if y < 0 or (y == 0 and i < 0):
+            c |= 0x8
+        assert oracle.quantize_value(float(y), "e2m1") == c, float(y)
+
+
+def random_blocks(rng, L, rows, cols, sfv):
+    # magnitudes spread over many binades, per block
+    x = rng.standard_normal((L, rows, cols))
+    x *= np.repeat(np.exp2(rng.integers(-30, 30, (L, rows, cols // sfv))), sfv, axis=2)
+    return x.astype(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("dtype,sfv", [("e4m3", 32), ("e5m2", 32), ("e2m1", 16), ("e2m1", 32)])
+def test_block_properties(dtype, sfv):
+    rng = np.random.default_rng(11)
+    L, rows, cols = 2, 37, 4 * sfv
+    X = random_blocks(rng, L, rows, cols, sfv)
+    codes, sf = oracle.quantize(X, dtype, sfv)
+    c = unpack(codes, dtype)
+    sb = scale_bytes(sf, rows, cols // sfv)
+    tab = oracle.decode_table(dtype)
+    dec = tab[c]
+    scale = np.exp2(sb.astype(np.float64) - 127).repeat(sfv, axis=2)
+    y = X / scale
+    # the block maximum lands in the top binade [2^emax, 2^(emax+1))
+    ymax = np.abs(y).reshape(L, rows, -1, sfv).max(axis=3)
+    assert np.all(ymax >= 2.0 ** EMAX[dtype]) and np.all(ymax < 2.0 ** (EMAX[dtype] + 1))
+    # rounding error: within half the spacing of the format at |y|, or saturated
+    m = MAXV[dtype]
+    mant = {"e4m3": 3, "e5m2": 2, "e2m1": 1}[dtype]
+    emin = {"e4m3": -6, "e5m2": -14, "e2m1": 0}[dtype]
+    ay = np.abs(y)
+    ex = np.maximum(np.floor(np.log2(np.where(ay > 0, ay, 1.0))), emin)
+    half = np.exp2(ex - mant) / 2
+    sat = ay > m
+    assert np.all(np.abs(dec[~sat] - y[~sat]) <= half[~sat])
+    assert np.all(np.abs(dec[sat]) == m) and np.all(np.sign(dec[sat]) == np.sign(y[sat]))
+
+
+@pytest.mark.parametrize("dtype,sfv", [("e4m3", 32), ("e5m2", 32), ("e2m1", 16)])
+def test_sign_and_power_of_two_invariance(dtype, sfv):
+    rng = np.random.default_rng(5)
+    X = random_blocks(rng, 1, 9, 2 * sfv, sfv)
+    codes, sf = oracle.quantize(X, dtype, sfv)
+    ncodes, nsf = oracle.quantize(-X, dtype, sfv)
+    assert np.array_equal(unpack(ncodes, dtype), unpack(codes, dtype) ^ SIGN[dtype])
+    assert np.array_equal(nsf, sf)
+    for j in (-3, 1, 7):
+        scodes, ssf = oracle.quantize(X * 2.0 ** j, dtype, sfv)
+        assert np.array_equal(scodes, codes)
+        a = scale_bytes(sf, 9, 2).astype(np.int64)
+        b = scale_bytes(ssf, 9, 2).astype(np.int64)
+        assert np.array_equal(b - a, np.full_like(a, j))
+
+
+@pytest.mark.parametrize("dtype,sfv", [("e4m3", 32), ("e5m2", 32), ("e2m1", 16), ("e2m1", 32)])
+def test_exact_round_trip_of_mx_data(dtype, sfv):
+    """Codes with one top-binade element per block and finite scales,
+    dequantized by the pinned GEMM-side dequantizer, quantize back to
+    themselves."""
+    rng = np.random.default_rng(3)
+    L, rows, cols = 1, 130, 8 * sfv
+    tab = oracle.decode_table(dtype)
+    finite = np.array([c for c in range(len(tab)) if np.isfinite(tab[c])])
+    top = np.array([c for c in finite if 2.0 ** EMAX[dtype] <= abs(tab[c]) <= MAXV[dtype]])
+    c = rng.choice(finite, (L, rows, cols))
+    c[..., ::sfv] = rng.choice(top, (L, rows, cols // sfv))
+    if dtype == "e2m1":
+        packed = (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+    else:
+        packed = c.astype(np.uint8)
+    sfl = rng.integers(100, 150, (L, rows, cols // sfv)).astype(np.uint8)
+    sf = synth.pack_scale_atoms(sfl, rows, cols, sfv)
+    X = oracle.dequantize(packed, dtype, sf, sfv, rows, cols, L)
+    codes, sf2 = oracle.quantize(X, dtype, sfv)
+    got = unpack(codes, dtype)
+    want = c.copy()
+    # a zero keeps its sign bit through dequantize/quantize
+    assert np.array_equal(got, want)
+    assert np.array_equal(sf2, sf)
+
+
+def test_special_blocks_and_padding():
+    X = np.zeros((1, 3, 64))
+    X[0, 1, 5] = np.nan
+    X[0, 2, 40] = np.inf
+    X[0, 2, 2] = 1.0
+    codes, sf = oracle.quantize(X, "e4m3", 32)
+    sb = scale_bytes(sf, 3, 2)
+    assert sb[0, 0, 0] == 127 and sb[0, 0, 1] == 127          # all-zero blocks
+    assert sb[0, 1, 0] == 0xFF and np.all(codes[0, 1, :32] == 0x7F)
+    assert sb[0, 1, 1] == 127 and np.all(codes[0, 1, 32:] == 0)
+    assert sb[0, 2, 1] == 0xFF and np.all(codes[0, 2, 32:] == 0x7F)
+    assert sb[0, 2, 0] == 127 - 8 and codes[0, 2, 2] == 0x78   # 1.0 -> 256 = 2^8
+    # every other byte of the padded atom (rows 3..127, blocks 2..3) is 127
+    flat = sf.reshape(-1)
+    used = {oracle.sf_offset(r, b, 0, 1, 1) for r in range(3) for b in range(2)}
+    assert all(flat[i] == 127 for i in range(flat.size) if i not in used)
+
+
+@pytest.mark.parametrize("dtype,sfv", [("e4m3", 32), ("e5m2", 32), ("e2m1", 16)])
+def test_matches_the_input_generator(dtype, sfv):
+    """The seeded generators carry their own quantizer (numpy frexp, float32
+    scaling, torch casts); on ordinary data both follow the same rule."""
+    rng = np.random.default_rng(17)
+    x = rng.standard_normal((64, 8 * sfv)).astype(np.float32)
+    codes_g, sf_g = synth.quantize_blocks(x, dtype, sfv)
+    codes_o, sf_o = oracle.quantize(x.astype(np.float64)[None], dtype, sfv)
+    assert np.array_equal(codes_o[0], codes_g)
+    assert np.array_equal(scale_bytes(sf_o, 64, 8)[0], sf_g.astype(np.int64))
