@@ -10,6 +10,11 @@ B (N,K,L) holding FP8 or packed FP4 codes with E8M0 scales per sf_vec_size
 K-block in the 128-row atom layout, C[m,n,l] = sum_k Ahat[m,k,l] Bhat[n,k,l]
 and Amax = max |C|.
 
+The MX quantizer that produces such operands ("GEMM + RoPE + MXFP8
+Projection (SM100)", section "Equations"; ``include/bsquant.h``) is bound here
+too: ``bsg_quant_check``, ``bsg_quant_sizes``, ``bsg_quantize`` and the torch
+convenience ``quantize``.
+
 The functions keep the C names and return the C status code (0 = BSG_OK);
 functions with C out-parameters return ``(status, value)``.  ``GemmAmax`` is
 a convenience holder of a plan and its workspace for torch tensors.
@@ -62,6 +67,12 @@ class bsg_plan_info(ctypes.Structure):
                 ("kernel_name", ctypes.c_char * 64)]
 
 
+class bsg_quant_problem(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("L", ctypes.c_int64),
+                ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
+                ("sf_vec_size", ctypes.c_int)]
+
+
 class bsg_device_buffers(ctypes.Structure):
     _fields_ = [("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("SFA", ctypes.c_void_p),
                 ("SFB", ctypes.c_void_p), ("C", ctypes.c_void_p), ("amax", ctypes.c_void_p),
@@ -96,10 +107,14 @@ def library() -> ctypes.CDLL:
     lib.bsg_plan_describe.argtypes = [vp, ctypes.POINTER(bsg_plan_info)]
     lib.bsg_plan_destroy.argtypes = [vp]
     lib.bsg_plan_destroy.restype = None
+    qp = ctypes.POINTER(bsg_quant_problem)
+    lib.bsg_quant_check.argtypes = [qp]
+    lib.bsg_quant_sizes.argtypes = [qp, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    lib.bsg_quantize.argtypes = [qp, vp, vp, vp, vp]
     for name in ("bsg_problem_check", "bsg_plan_create", "bsg_plan_workspace_size",
                  "bsg_workspace_init", "bsg_run", "bsg_run_host", "bsg_check_device_status",
                  "bsg_run_noalloc",
-                 "bsg_plan_describe"):
+                 "bsg_plan_describe", "bsg_quant_check", "bsg_quant_sizes", "bsg_quantize"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -242,3 +257,52 @@ class GemmAmax:
             self.close()
         except Exception:
             pass
+
+
+# ------------------------------------------------------------- quantizer
+
+def make_quant_problem(rows, cols, L=1, in_dtype="f32", out_dtype="e4m3",
+                       sf_vec_size=32) -> bsg_quant_problem:
+    d = lambda x: DTYPE[x] if isinstance(x, str) else int(x)
+    return bsg_quant_problem(int(rows), int(cols), int(L), d(in_dtype), d(out_dtype),
+                             int(sf_vec_size))
+
+
+def bsg_quant_check(q: bsg_quant_problem) -> int:
+    return library().bsg_quant_check(ctypes.byref(q))
+
+
+def bsg_quant_sizes(q: bsg_quant_problem):
+    cb, sb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    st = library().bsg_quant_sizes(ctypes.byref(q), ctypes.byref(cb), ctypes.byref(sb))
+    return st, (cb.value, sb.value)
+
+
+def bsg_quantize(q: bsg_quant_problem, X: int, codes: int, sf: int, stream: int = 0) -> int:
+    return library().bsg_quantize(ctypes.byref(q), X, codes, sf, stream)
+
+
+def quantize(X, out_dtype="e4m3", sf_vec_size=32, codes=None, sf=None, stream=None):
+    """Quantize a contiguous CUDA tensor X (L, rows, cols) or (rows, cols) of
+    float32 or bfloat16 into (codes, sf) uint8 tensors (allocated when not
+    given); one launch on torch's current stream."""
+    import torch
+    if not X.is_cuda or not X.is_contiguous():
+        raise ValueError("X must be a contiguous CUDA tensor")
+    shape = tuple(X.shape) if X.dim() == 3 else (1,) + tuple(X.shape)
+    in_dtype = {torch.float32: "f32", torch.bfloat16: "bf16"}.get(X.dtype)
+    if in_dtype is None:
+        raise ValueError("X must be float32 or bfloat16")
+    q = make_quant_problem(shape[1], shape[2], shape[0], in_dtype, out_dtype, sf_vec_size)
+    st, (cb, sb) = bsg_quant_sizes(q)
+    check(st, "bsg_quant_sizes")
+    if codes is None:
+        codes = torch.empty(cb, dtype=torch.uint8, device=X.device)
+    if sf is None:
+        sf = torch.empty(sb, dtype=torch.uint8, device=X.device)
+    if codes.numel() < cb or sf.numel() < sb:
+        raise ValueError("codes / sf buffers too small")
+    s = stream if stream is not None else torch.cuda.current_stream(X.device).cuda_stream
+    check(bsg_quantize(q, X.data_ptr(), codes.data_ptr(), sf.data_ptr(), s), "bsg_quantize")
+    return codes, sf
+

@@ -10,7 +10,7 @@ import subprocess
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
-SOURCES = [os.path.join(HERE, "csrc", "bsgemm.cu")]
+SOURCES = [os.path.join(HERE, "csrc", "bsgemm.cu"), os.path.join(HERE, "csrc", "quant.cu")]
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libbsgemm.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -27,7 +27,7 @@ def needs_build() -> bool:
     if not os.path.exists(LIB):
         return True
     t = os.path.getmtime(LIB)
-    deps = SOURCES + [os.path.join(INCLUDE, "bsgemm.h")]
+    deps = SOURCES + [os.path.join(INCLUDE, h) for h in ("bsgemm.h", "bsquant.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
 

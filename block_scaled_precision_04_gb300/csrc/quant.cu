@@ -1,0 +1,323 @@
+// quant.cu -- MX quantizer for sm_103a: real values -> FP8 / packed FP4 codes
+// plus one E8M0 scale per block of K elements, the scales written straight
+// into the atom layout the GEMM reads.
+//
+// Operation ("GEMM + RoPE + MXFP8 Projection (SM100)", section "Equations":
+// MXFP8 quantize, an E8M0 per-block scale with E4M3 data; "GEMM + Amax
+// (SM100)" for the scale atom layout and the E5M2 / packed E2M1 formats).  The
+// pages do not spell out how a block's scale is chosen; the reading used takes
+// the block's largest magnitude to the top binade of the element format:
+//   amax = max |x| over the block, e = floor(log2 amax) - emax (E4M3 8,
+//   E5M2 15, E2M1 2), e clamped to [-127, 127], scale byte e + 127,
+//   code = round-to-nearest-even of x * 2^-e, saturated to the largest finite
+//   value.  All-zero block: byte 127.  NaN or infinity in the block: byte 0xFF
+//   and every code the format's NaN (E4M3 / E5M2 0x7F; E2M1 has none: 0).
+//   Padding scale positions of the last atoms: byte 127.
+//
+// HBM-bound: one pass over X, coalesced 16-byte loads (4 fp32 or 8 bf16 per
+// thread and chunk, four chunks in flight per thread), the block maximum by
+// shuffles among the 2..8 lanes sharing a block, packed round-to-nearest
+// saturating conversions, coalesced code stores, one scale byte per block.
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "bsgemm.h"
+#include "bsquant.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;        // chunks per thread per unit
+constexpr int kChunkBytes = 16;   // input bytes per thread per chunk
+
+enum OutKind : int { kOutE4M3 = 0, kOutE5M2 = 1, kOutE2M1 = 2 };
+
+struct QParams {
+  const uint8_t* x;
+  uint8_t* codes;
+  uint8_t* sf;
+  int64_t rows, cols, L;
+  int64_t chunks_per_row;  // cols / elements per chunk
+  int64_t units_per_row;   // ceil(chunks_per_row / (kThreads * kUnroll))
+  int64_t num_units;       // L * rows * units_per_row
+  int64_t nblk, t_r, t_k;  // blocks per row, atoms along rows and K
+};
+
+template <int OUT>
+struct OutFmt;
+template <>
+struct OutFmt<kOutE4M3> { static constexpr int kEmax = 8; static constexpr uint32_t kNan = 0x7Fu; };
+template <>
+struct OutFmt<kOutE5M2> { static constexpr int kEmax = 15; static constexpr uint32_t kNan = 0x7Fu; };
+template <>
+struct OutFmt<kOutE2M1> { static constexpr int kEmax = 2; static constexpr uint32_t kNan = 0x0u; };
+
+// Two values -> two codes, round to nearest even, saturating: `lo` in the
+// low byte (FP8) or low nibble (FP4).
+template <int OUT>
+__device__ __forceinline__ uint32_t cvt2(float lo, float hi) {
+  if (OUT == kOutE4M3) {
+    uint16_t h;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(hi), "f"(lo));
+    return h;
+  } else if (OUT == kOutE5M2) {
+    uint16_t h;
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(h) : "f"(hi), "f"(lo));
+    return h;
+  } else {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    return r;
+  }
+}
+
+// floor(log2 |v|) of a positive finite float given its magnitude bits.
+__device__ __forceinline__ int floor_log2_bits(uint32_t a) {
+  const int ef = static_cast<int>(a >> 23);
+  if (ef > 0) return ef - 127;                  // normal: the unbiased exponent
+  return (31 - __clz(static_cast<int>(a))) - 149;  // subnormal: a * 2^-149
+}
+
+// Byte offset of the scale of row `r`, block `kb`, batch `l` in the
+// (L, t_r, t_k, 32, 4, 4) atom tensor (row r = 128 rt + 32 m1 + m0).
+__device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t kb, int64_t l, int64_t t_r,
+                                             int64_t t_k) {
+  const int64_t rt = r >> 7, rr = r & 127, kt = kb >> 2;
+  return (((l * t_r + rt) * t_k + kt) * 512) + (rr & 31) * 16 + (rr >> 5) * 4 + (kb & 3);
+}
+
+template <int IN_BF16, int OUT, int SFV>
+__global__ void __launch_bounds__(kThreads) bsq_quantize_kernel(const QParams p) {
+  constexpr int E = IN_BF16 ? 8 : 4;   // elements per chunk
+  constexpr int G = SFV / E;           // lanes per scale block (2..8)
+  constexpr int kCodeBytes = OUT == kOutE2M1 ? E / 2 : E;
+  using F = OutFmt<OUT>;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+
+  for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    const int64_t flat_row = u / p.units_per_row;
+    const int64_t seg = u - flat_row * p.units_per_row;
+    const int64_t l = flat_row / p.rows;
+    const int64_t r = flat_row - l * p.rows;
+    const uint8_t* xrow = p.x + flat_row * p.cols * (IN_BF16 ? 2 : 4);
+    uint8_t* crow = p.codes + flat_row * (OUT == kOutE2M1 ? p.cols / 2 : p.cols);
+    // all loads of the unit first, then the arithmetic
+    uint4 raw[kUnroll];
+    int64_t ch[kUnroll];
+#pragma unroll
+    for (int i = 0; i < kUnroll; ++i) {
+      ch[i] = (seg * kUnroll + i) * kThreads + tid;
+      raw[i] = ch[i] < p.chunks_per_row
+                   ? __ldcs(reinterpret_cast<const uint4*>(xrow + ch[i] * kChunkBytes))
+                   : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < kUnroll; ++i) {
+      // a G-lane group holds one block, and is wholly in or out of the row
+      const bool valid = ch[i] < p.chunks_per_row;
+      float v[E];
+      const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+      if (IN_BF16) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[2 * j] = __uint_as_float(w[j] << 16);
+          v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = __uint_as_float(w[j]);
+      }
+      // block maximum of the magnitude bits (NaN and infinity order above
+      // every finite value)
+      uint32_t amax = 0u;
+#pragma unroll
+      for (int j = 0; j < E; ++j) amax = max(amax, __float_as_uint(v[j]) & 0x7FFFFFFFu);
+#pragma unroll
+      for (int off = 1; off < G; off <<= 1) amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+      if (!valid) continue;
+      uint32_t byte = 127u;
+      float inv = 1.0f;  // 2^-e
+      const bool nonfinite = amax >= 0x7F800000u;
+      if (nonfinite) {
+        byte = 0xFFu;
+      } else if (amax != 0u) {
+        int e = floor_log2_bits(amax) - F::kEmax;
+        e = min(max(e, -127), 127);
+        byte = static_cast<uint32_t>(e + 127);
+        // 2^-e as a float: normal for -e >= -126, the subnormal 2^-127 otherwise
+        inv = -e >= -126 ? __uint_as_float(static_cast<uint32_t>(127 - e) << 23)
+                         : __uint_as_float(0x00400000u);
+      }
+      uint32_t out[2] = {0u, 0u};
+      if (nonfinite) {
+        const uint32_t nan = F::kNan;
+        if (OUT == kOutE2M1) {
+          out[0] = 0u;
+          out[1] = 0u;
+        } else {
+          out[0] = nan * 0x01010101u;
+          out[1] = nan * 0x01010101u;
+        }
+      } else if (OUT == kOutE2M1) {
+        // E/2 bytes, element 2j in the low nibble of byte j
+#pragma unroll
+        for (int j = 0; j < E / 2; ++j)
+          out[j / 4] |= cvt2<OUT>(v[2 * j] * inv, v[2 * j + 1] * inv) << (8 * (j % 4));
+      } else {
+#pragma unroll
+        for (int j = 0; j < E / 2; ++j)
+          out[j / 2] |= cvt2<OUT>(v[2 * j] * inv, v[2 * j + 1] * inv) << (16 * (j % 2));
+      }
+      uint8_t* cdst = crow + ch[i] * kCodeBytes;
+      if (kCodeBytes == 8) *reinterpret_cast<uint2*>(cdst) = make_uint2(out[0], out[1]);
+      else if (kCodeBytes == 4) *reinterpret_cast<uint32_t*>(cdst) = out[0];
+      else *reinterpret_cast<uint16_t*>(cdst) = static_cast<uint16_t>(out[0]);
+      if ((lane % G) == 0) {
+        const int64_t kb = ch[i] / G;
+        p.sf[sf_offset(r, kb, l, p.t_r, p.t_k)] = static_cast<uint8_t>(byte);
+      }
+    }
+  }
+
+  // padding scale positions: rows past `rows` in the last row atoms, blocks
+  // past `nblk` in the last K atoms (the loop above writes every other byte)
+  const bool pad_rows = (p.rows & 127) != 0, pad_k = (p.nblk & 3) != 0;
+  if (!pad_rows && !pad_k) return;
+  const int64_t atoms = p.L * (p.t_k + p.t_r);
+  for (int64_t a = blockIdx.x; a < atoms; a += gridDim.x) {
+    int64_t l = a / (p.t_k + p.t_r), rt, kt;
+    const int64_t j = a - l * (p.t_k + p.t_r);
+    if (j < p.t_k) {
+      if (!pad_rows) continue;
+      rt = p.t_r - 1;
+      kt = j;
+    } else {
+      if (!pad_k) continue;
+      rt = j - p.t_k;
+      kt = p.t_k - 1;
+    }
+    for (int b = tid; b < 512; b += kThreads) {
+      const int m0 = b >> 4, m1 = (b >> 2) & 3, kin = b & 3;
+      const int64_t row = rt * 128 + m1 * 32 + m0, kb = kt * 4 + kin;
+      if (row >= p.rows || kb >= p.nblk)
+        p.sf[((l * p.t_r + rt) * p.t_k + kt) * 512 + b] = 127u;
+    }
+  }
+}
+
+template <int IN_BF16, int OUT, int SFV>
+const void* kernel_of() {
+  return reinterpret_cast<const void*>(&bsq_quantize_kernel<IN_BF16, OUT, SFV>);
+}
+
+const void* pick_kernel(int in_bf16, int out, int sfv) {
+  if (out == kOutE4M3) return in_bf16 ? kernel_of<1, kOutE4M3, 32>() : kernel_of<0, kOutE4M3, 32>();
+  if (out == kOutE5M2) return in_bf16 ? kernel_of<1, kOutE5M2, 32>() : kernel_of<0, kOutE5M2, 32>();
+  if (sfv == 16) return in_bf16 ? kernel_of<1, kOutE2M1, 16>() : kernel_of<0, kOutE2M1, 16>();
+  return in_bf16 ? kernel_of<1, kOutE2M1, 32>() : kernel_of<0, kOutE2M1, 32>();
+}
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+int g_dev_sms[kMaxDevices] = {};   // 0: not queried yet; -1: not an sm_103 device
+
+}  // namespace
+
+extern "C" {
+
+bsg_status bsg_quant_check(const bsg_quant_problem* q) {
+  if (!q) return BSG_ERR_INVALID_ARG;
+  const int64_t lim = (int64_t(1) << 31) - 1;
+  if (q->rows < 1 || q->cols < 1 || q->L < 1) return BSG_ERR_INVALID_ARG;
+  if (q->rows > lim || q->cols > lim || q->L > lim || q->rows * q->L > lim)
+    return BSG_ERR_INVALID_ARG;
+  if (q->in_dtype != BSG_F32 && q->in_dtype != BSG_BF16) return BSG_ERR_INVALID_ARG;
+  if (q->out_dtype != BSG_E4M3 && q->out_dtype != BSG_E5M2 && q->out_dtype != BSG_E2M1)
+    return BSG_ERR_INVALID_ARG;
+  if (q->sf_vec_size != 16 && q->sf_vec_size != 32) return BSG_ERR_INVALID_ARG;
+  if (q->out_dtype != BSG_E2M1 && q->sf_vec_size != 32) return BSG_ERR_UNSUPPORTED;
+  if (q->cols % q->sf_vec_size != 0) return BSG_ERR_UNSUPPORTED;  // whole blocks only
+  return BSG_OK;
+}
+
+bsg_status bsg_quant_sizes(const bsg_quant_problem* q, size_t* code_bytes, size_t* sf_bytes) {
+  const bsg_status st = bsg_quant_check(q);
+  if (st != BSG_OK) return st;
+  if (!code_bytes || !sf_bytes) return BSG_ERR_INVALID_ARG;
+  const int64_t per_row = q->out_dtype == BSG_E2M1 ? q->cols / 2 : q->cols;
+  *code_bytes = static_cast<size_t>(q->L * q->rows * per_row);
+  *sf_bytes = static_cast<size_t>(q->L * cdiv(q->rows, 128) * cdiv(q->cols / q->sf_vec_size, 4) * 512);
+  return BSG_OK;
+}
+
+bsg_status bsg_quantize(const bsg_quant_problem* q, const void* X, void* codes, void* sf,
+                        void* stream) {
+  const bsg_status st = bsg_quant_check(q);
+  if (st != BSG_OK) return st;
+  if (!X || !codes || !sf) return BSG_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(codes) || !aligned16(sf)) return BSG_ERR_ALIGNMENT;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return BSG_ERR_CUDA;
+  }
+  int sms;
+  {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (g_dev_sms[dev] == 0) {
+      int major = 0, minor = 0, n = 0;
+      if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return BSG_ERR_CUDA;
+      }
+      g_dev_sms[dev] = (major == 10 && minor == 3) ? n : -1;
+    }
+    sms = g_dev_sms[dev];
+  }
+  if (sms < 0) return BSG_ERR_ARCH;
+  QParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int in_bf16 = q->in_dtype == BSG_BF16 ? 1 : 0;
+  const int elems = in_bf16 ? 8 : 4;
+  p.x = static_cast<const uint8_t*>(X);
+  p.codes = static_cast<uint8_t*>(codes);
+  p.sf = static_cast<uint8_t*>(sf);
+  p.rows = q->rows;
+  p.cols = q->cols;
+  p.L = q->L;
+  p.chunks_per_row = q->cols / elems;
+  p.units_per_row = cdiv(p.chunks_per_row, int64_t(kThreads) * kUnroll);
+  p.num_units = q->L * q->rows * p.units_per_row;
+  p.nblk = q->cols / q->sf_vec_size;
+  p.t_r = cdiv(q->rows, 128);
+  p.t_k = cdiv(p.nblk, 4);
+  const int out = q->out_dtype == BSG_E4M3 ? kOutE4M3 : (q->out_dtype == BSG_E5M2 ? kOutE5M2 : kOutE2M1);
+  const void* fn = pick_kernel(in_bf16, out, q->sf_vec_size);
+  // enough resident CTAs per SM to keep 16-byte loads in flight for HBM
+  const int64_t want = static_cast<int64_t>(sms) * 8;
+  const int64_t extra = q->L * (p.t_k + p.t_r);
+  int64_t grid = p.num_units > extra ? p.num_units : extra;
+  if (grid > want) grid = want;
+  if (grid < 1) grid = 1;
+  void* args[1] = {&p};
+  if (cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(kThreads), args, 0,
+                       static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return BSG_ERR_CUDA;
+  }
+  return BSG_OK;
+}
+
+}  // extern "C"

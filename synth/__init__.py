@@ -286,3 +286,46 @@ def sample_points(p: Problem, count: int, seed: int, extra=()) -> np.ndarray:
     if len(extra):
         allp.append(np.asarray(extra, dtype=np.int64).reshape(-1, 3))
     return np.concatenate(allp, axis=0).astype(np.int64)
+
+
+# ------------------------------------------------------ quantizer inputs
+
+def real_blocks(L: int, rows: int, cols: int, seed: int, block: int = 32, spread: int = 30,
+                specials: bool = False) -> np.ndarray:
+    """Seeded real-valued input of the MX quantizer, float32 (L, rows, cols):
+    N(0, 1) values with every `block`-element run scaled by its own 2^j,
+    j uniform in [-spread, spread].  With `specials`, some runs are replaced
+    by edge cases: all zeros, a NaN, an infinity, fp32 subnormals, values near
+    the fp32 maximum, exact powers of two, and one value between binades."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((L, rows, cols))
+    x *= np.repeat(np.exp2(rng.integers(-spread, spread + 1, (L, rows, cols // block))),
+                   block, axis=2)
+    x = x.astype(np.float32)
+    if specials:
+        nb = cols // block
+        picks = rng.choice(L * rows * nb, size=min(L * rows * nb, 8), replace=False)
+        for i, f in enumerate(picks):
+            l, rem = divmod(int(f), rows * nb)
+            r, b = divmod(rem, nb)
+            blk = x[l, r, b * block:(b + 1) * block]
+            kind = i % 8
+            if kind == 0:
+                blk[:] = 0.0
+            elif kind == 1:
+                blk[rng.integers(block)] = np.nan
+            elif kind == 2:
+                blk[rng.integers(block)] = -np.inf
+            elif kind == 3:
+                blk[:] = (rng.standard_normal(block) * 1e-41).astype(np.float32)
+            elif kind == 4:
+                blk[:] = (rng.uniform(-3.3e38, 3.3e38, block)).astype(np.float32)
+            elif kind == 5:
+                blk[:] = np.exp2(rng.integers(-20, 20, block)).astype(np.float32)
+            elif kind == 6:
+                blk[:] = 0.0
+                blk[0] = -0.0
+                blk[1] = 1.0e-45
+            else:
+                blk[:] = np.float32(1.5) * np.exp2(np.float32(rng.integers(-5, 5)))
+    return x

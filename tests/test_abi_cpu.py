@@ -1,6 +1,6 @@
 """Host-side checks of the C ABI (no GPU needed, no kernel launched).
 
-* the library builds, loads and exports every function include/bsgemm.h declares;
+* the library builds, loads and exports every function include/*.h declares;
 * the ctypes structures have the C layout (compiled probe with gcc);
 * bsg_problem_check enforces the page's support surface ("Support surface
   and constraints") and returns a status, before anything touches a device.
@@ -15,7 +15,7 @@ import pytest
 import block_scaled_precision_04_gb300 as bsg
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "bsgemm.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("bsgemm.h", "bsquant.h")]
 
 
 @pytest.fixture(scope="module")
@@ -25,14 +25,16 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(bsg_\w+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(bsg_\w+)\s*\(", text))
+    return sorted(names)
 
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert "bsg_run" in names and "bsg_plan_create" in names
+    assert "bsg_run" in names and "bsg_plan_create" in names and "bsg_quantize" in names
     out = subprocess.run(["nm", "-D", "--defined-only", bsg.LIB], capture_output=True, text=True,
                          check=True).stdout
     exported = set(re.findall(r"\bT (bsg_\w+)", out))
@@ -47,10 +49,13 @@ def test_struct_layout_matches_c(tmp_path):
 #include <stdio.h>
 #include <stddef.h>
 #include "bsgemm.h"
+#include "bsquant.h"
 int main(void) {
   printf("%zu %zu %zu %zu %zu\n", sizeof(bsg_problem), offsetof(bsg_problem, a_major),
          offsetof(bsg_problem, sf_vec_size), offsetof(bsg_problem, cluster_n), sizeof(bsg_plan_info));
   printf("%zu %zu\n", sizeof(bsg_device_buffers), offsetof(bsg_device_buffers, ws_bytes));
+  printf("%zu %zu %zu\n", sizeof(bsg_quant_problem), offsetof(bsg_quant_problem, in_dtype),
+         offsetof(bsg_quant_problem, sf_vec_size));
   return 0;
 }
 ''')
@@ -64,6 +69,9 @@ int main(void) {
                  bsg.bsg_problem.sf_vec_size.offset, bsg.bsg_problem.cluster_n.offset,
                  ctypes.sizeof(bsg.bsg_plan_info)]
     assert b == [ctypes.sizeof(bsg.bsg_device_buffers), bsg.bsg_device_buffers.ws_bytes.offset]
+    c = [int(x) for x in lines[2].split()]
+    assert c == [ctypes.sizeof(bsg.bsg_quant_problem), bsg.bsg_quant_problem.in_dtype.offset,
+                 bsg.bsg_quant_problem.sf_vec_size.offset]
 
 
 def test_status_strings(lib):
@@ -154,3 +162,41 @@ def test_invalid_problem_fails_before_device(lib):
     even on a machine with no GPU."""
     st, _ = bsg.bsg_plan_create(bsg.make_problem(4, 4, 32, 1, sf_vec_size=16), 0)
     assert st == bsg.BSG_ERR_UNSUPPORTED
+
+
+QUANT_OK = [
+    dict(rows=1, cols=32),
+    dict(rows=16384, cols=8192, in_dtype="bf16", out_dtype="e2m1", sf_vec_size=16),
+    dict(rows=130, cols=96, L=3, out_dtype="e5m2"),
+    dict(rows=7, cols=64, out_dtype="e2m1", sf_vec_size=32),
+]
+
+
+@pytest.mark.parametrize("kw", QUANT_OK)
+def test_quant_supported(lib, kw):
+    assert bsg.bsg_quant_check(bsg.make_quant_problem(**kw)) == bsg.BSG_OK
+
+
+QUANT_BAD = [
+    (dict(rows=0, cols=32), bsg.BSG_ERR_INVALID_ARG, "empty rows"),
+    (dict(rows=4, cols=0), bsg.BSG_ERR_INVALID_ARG, "empty cols"),
+    (dict(rows=4, cols=32, L=0), bsg.BSG_ERR_INVALID_ARG, "empty L"),
+    (dict(rows=1 << 20, cols=32, L=1 << 12), bsg.BSG_ERR_INVALID_ARG, "rows * L beyond 2^31-1"),
+    (dict(rows=4, cols=32, in_dtype="f16"), bsg.BSG_ERR_INVALID_ARG, "fp16 input"),
+    (dict(rows=4, cols=32, out_dtype="bf16"), bsg.BSG_ERR_INVALID_ARG, "bf16 output"),
+    (dict(rows=4, cols=32, sf_vec_size=64), bsg.BSG_ERR_INVALID_ARG, "sfv 64"),
+    (dict(rows=4, cols=32, out_dtype="e4m3", sf_vec_size=16), bsg.BSG_ERR_UNSUPPORTED, "FP8 sfv 16"),
+    (dict(rows=4, cols=48), bsg.BSG_ERR_UNSUPPORTED, "partial block"),
+]
+
+
+@pytest.mark.parametrize("kw,status,rule", QUANT_BAD, ids=[c[2] for c in QUANT_BAD])
+def test_quant_rejections(lib, kw, status, rule):
+    assert bsg.bsg_quant_check(bsg.make_quant_problem(**kw)) == status, rule
+
+
+def test_quant_sizes(lib):
+    st, (cb, sb) = bsg.bsg_quant_sizes(bsg.make_quant_problem(130, 256, 2, "bf16", "e2m1", 16))
+    assert st == bsg.BSG_OK and cb == 2 * 130 * 128 and sb == 2 * 2 * 4 * 512
+    assert lib.bsg_quantize(None, None, None, None, None) == bsg.BSG_ERR_INVALID_ARG
+
