@@ -8,6 +8,7 @@ between steps.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+  python bench.py --op quantize [--qworkload 1|2]  # the MX quantizer (HBM GB/s)
 
 Under torchrun (N > 1) every rank runs its own replica of the workload on its
 own GPU (no data exchanged); rank 0 prints the max-over-ranks timing.
@@ -46,9 +47,20 @@ TRAFFIC = {
 }
 
 
-def kernel_source_hash() -> str:
+# the same for the quantizer kernel (csrc/quant.cu), keyed by its code hash
+# and quantizer workload
+TRAFFIC_Q = {}
+
+QMETRIC = "MX quantize GB/s on 1 GB300 (X read + codes and scales written); % of HBM copy bandwidth"
+QWORKLOADS = {
+    1: ("quantize-f32-16384x8192-e4m3-sfv32", 16384, 8192, "f32", "e4m3", 32),
+    2: ("quantize-bf16-16384x8192-e2m1-sfv16", 16384, 8192, "bf16", "e2m1", 16),
+}
+
+
+def kernel_source_hash(name: str = "bsgemm.cu") -> str:
     import re
-    path = os.path.join(ROOT, "block_scaled_precision_04_gb300", "csrc", "bsgemm.cu")
+    path = os.path.join(ROOT, "block_scaled_precision_04_gb300", "csrc", name)
     with open(path) as f:
         src = f.read()
     # drop comments (string literals in this file hold no comment markers)
@@ -307,6 +319,164 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     return line
 
 
+def quant_numbers(rows, cols, in_dtype, out_dtype, sfv):
+    x = rows * cols * (4 if in_dtype == "f32" else 2)
+    codes = rows * cols // (2 if out_dtype == "e2m1" else 1)
+    sf = -(-rows // 128) * -(-(cols // sfv) // 4) * 512
+    return {"bytes": x + codes + sf, "h2d": x, "d2h": codes + sf}
+
+
+def quant_oracle_sample(X32, out_dtype, sfv, target_s: float):
+    """The oracle's quantizer (single thread), timed on the first r rows,
+    r sized for about target_s seconds."""
+    import oracle
+    rows = min(X32.shape[1], 64)
+    for attempt in range(3):
+        t0 = time.perf_counter()
+        oracle.quantize(X32[:, :rows].astype(np.float64), out_dtype, sfv)
+        t = time.perf_counter() - t0
+        want = int(min(X32.shape[1], max(1, (target_s / max(t, 1e-3)) * rows)))
+        if t >= 0.5 * target_s or want <= rows or attempt == 2:
+            break
+        rows = want
+    return rows, t
+
+
+def run_quant(args, rank: int, world: int, local_rank: int):
+    import torch
+    import block_scaled_precision_04_gb300 as bsg
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    name, rows, cols, in_dtype, out_dtype, sfv = QWORKLOADS[args.qworkload]
+    X32 = synth.real_blocks(1, rows, cols, seed=1500 + args.qworkload, block=sfv)
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16}[in_dtype]
+    hX = torch.from_numpy(X32).to(tdt)
+    X = hX.to(dev)
+    q = bsg.make_quant_problem(rows, cols, 1, in_dtype, out_dtype, sfv)
+    st, (cb, sb) = bsg.bsg_quant_sizes(q)
+    bsg.check(st, "bsg_quant_sizes")
+    codes = torch.empty(cb, dtype=torch.uint8, device=dev)
+    sf = torch.empty(sb, dtype=torch.uint8, device=dev)
+    nums = quant_numbers(rows, cols, in_dtype, out_dtype, sfv)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    s = stream.cuda_stream
+    launch = lambda: bsg.check(bsg.bsg_quantize(q, X.data_ptr(), codes.data_ptr(), sf.data_ptr(), s),
+                               "bsg_quantize")
+    for _ in range(args.warmup):
+        flush.zero_()
+        launch()
+    torch.cuda.synchronize(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        wall0 = time.perf_counter()
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record(stream)
+            launch()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+    if dist is not None:
+        dist.barrier()
+    times_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    total_ms = max_over_ranks(sum(times_ms), dist, dev)
+    ms = total_ms / args.steps
+    value = world * nums["bytes"] * args.steps / (total_ms / 1e3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        pX = hX.pin_memory()
+        pcodes = torch.empty(cb, dtype=torch.uint8).pin_memory()
+        psf = torch.empty(sb, dtype=torch.uint8).pin_memory()
+
+        def run_host():
+            X.copy_(pX, non_blocking=True)
+            launch()
+            pcodes.copy_(codes, non_blocking=True)
+            psf.copy_(sf, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            run_host()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            run_host()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
+        e2e = {"value": world * nums["bytes"] / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": nums["h2d"],
+               "d2h_bytes_per_step": nums["d2h"]}
+
+    _, hbm, source = peaks()
+    achieved = nums["bytes"] / (ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": round(hbm, 1),
+                "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "traffic": TRAFFIC_Q.get((kernel_source_hash("quant.cu"), args.qworkload)),
+                "peak_source": f"{source} HBM copy bandwidth",
+                "kernel": "bsq_quantize_kernel"}
+    line = {"metric": QMETRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": f"{in_dtype} in, {out_dtype} codes + e8m0 scales out",
+            "data": "synthetic (seeded; see synth.real_blocks)",
+            "config": {"workload": name, "rows": rows, "cols": cols, "L": 1, "in_dtype": in_dtype,
+                       "out_dtype": out_dtype, "sf_vec_size": sfv, "seed": 1500 + args.qworkload,
+                       "l2": "flushed between timed steps (512 MiB write)"},
+            "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps,
+            "clocks": clk.summary(), "wall_s_timed_region": round(wall, 4),
+            "step_ms_min": round(min(times_ms), 5),
+            "step_ms_median": round(statistics.median(times_ms), 5)}
+    if rank == 0 and not args.no_cpu:
+        r, t = quant_oracle_sample(X32 if in_dtype == "f32" else hX.float().numpy(), out_dtype, sfv,
+                                   args.cpu_seconds)
+        b = quant_numbers(r, cols, in_dtype, out_dtype, sfv)["bytes"]
+        line["cpu_baseline"] = {"value": b / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": f"rows 0..{r - 1} (all columns): {b / 1e6:.1f} MB "
+                                          f"in {t:.1f} s, one thread, double precision"}
+    elif rank == 0:
+        line["cpu_baseline"] = None
+    return line
+
+
+def run_quant_reference(args):
+    """The oracle's quantizer, as it stands, on a bounded sample per step."""
+    import oracle
+    name, rows, cols, in_dtype, out_dtype, sfv = QWORKLOADS[args.qworkload]
+    X32 = synth.real_blocks(1, rows, cols, seed=1500 + args.qworkload, block=sfv)
+    if in_dtype == "bf16":
+        import torch
+        X32 = torch.from_numpy(X32).to(torch.bfloat16).float().numpy()
+    per_step = max(0.5, args.ref_seconds / max(1, args.steps + args.warmup))
+    r, _ = quant_oracle_sample(X32, out_dtype, sfv, per_step)
+    Xs = X32[:, :r].astype(np.float64)
+    for _ in range(args.warmup):
+        oracle.quantize(Xs, out_dtype, sfv)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.quantize(Xs, out_dtype, sfv)
+    t = time.perf_counter() - t0
+    b = quant_numbers(r, cols, in_dtype, out_dtype, sfv)["bytes"]
+    value = b * args.steps / t / 1e9
+    return {"metric": QMETRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": name, "rows": rows, "cols": cols}, "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"rows 0..{r - 1} per step ({b / 1e6:.1f} MB, double)"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
 def run_reference(args):
     """The CPU oracle, as it stands, on a bounded sample of the same workload
     per step."""
@@ -345,6 +515,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=2, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--op", choices=["gemm", "quantize"], default="gemm")
+    ap.add_argument("--qworkload", type=int, default=1, choices=sorted(QWORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -359,7 +531,8 @@ def main(argv=None):
 
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args)), flush=True)
+            ref = run_quant_reference(args) if args.op == "quantize" else run_reference(args)
+            print(json.dumps(ref), flush=True)
         return 0
 
     if world > 1:
@@ -367,7 +540,7 @@ def main(argv=None):
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    line = run_ours(args, rank, world, local_rank)
+    line = (run_quant if args.op == "quantize" else run_ours)(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -15,7 +15,7 @@
 //   Padding scale positions of the last atoms: byte 127.
 //
 // HBM-bound: one pass over X, coalesced 16-byte loads (4 fp32 or 8 bf16 per
-// thread and chunk, four chunks in flight per thread), the block maximum by
+// thread and chunk; eight fp32 or four bf16 chunks in flight per thread), the block maximum by
 // shuffles among the 2..8 lanes sharing a block, packed round-to-nearest
 // saturating conversions, coalesced code stores, one scale byte per block.
 
@@ -31,20 +31,46 @@
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;        // chunks per thread per unit
+// chunks per thread per unit: 128 bytes of fp32 or 64 of bf16 in flight
+__host__ __device__ constexpr int unroll_of(int in_bf16) { return in_bf16 ? 4 : 8; }
 constexpr int kChunkBytes = 16;   // input bytes per thread per chunk
 
 enum OutKind : int { kOutE4M3 = 0, kOutE5M2 = 1, kOutE2M1 = 2 };
+
+// Division of a 32-bit n by an invariant d > 0 with one multiply-high and a
+// shift (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994): with s = ceil(log2 d) and m = floor(2^32 (2^s - d)
+// / d) + 1, n / d = (mulhi(n, m) + n) >> s for every n < 2^32.
+struct FastDiv {
+  uint32_t d, m, s;
+};
+
+FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  f.d = d;
+  uint32_t s = 0;
+  while ((uint64_t(1) << s) < d) ++s;
+  f.s = s;
+  f.m = static_cast<uint32_t>(((uint64_t(1) << 32) * ((uint64_t(1) << s) - d)) / d + 1);
+  return f;
+}
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
+  return static_cast<uint32_t>((static_cast<uint64_t>(__umulhi(n, f.m)) + n) >> f.s);
+}
 
 struct QParams {
   const uint8_t* x;
   uint8_t* codes;
   uint8_t* sf;
-  int64_t rows, cols, L;
-  int64_t chunks_per_row;  // cols / elements per chunk
-  int64_t units_per_row;   // ceil(chunks_per_row / (kThreads * kUnroll))
-  int64_t num_units;       // L * rows * units_per_row
-  int64_t nblk, t_r, t_k;  // blocks per row, atoms along rows and K
+  int64_t row_in_bytes;     // cols * input element size
+  int64_t row_code_bytes;   // cols, or cols / 2 for E2M1
+  uint32_t rows, cols, L;
+  uint32_t chunks_per_row;  // cols / elements per chunk
+  uint32_t num_units;       // L * rows * units_per_row (< 2^31)
+  uint32_t nblk, t_r, t_k;  // blocks per row, atoms along rows and K
+  FastDiv upr;              // units per row: ceil(chunks_per_row / (kThreads * unroll))
+  FastDiv rows_div;         // rows
 };
 
 template <int OUT>
@@ -77,6 +103,13 @@ __device__ __forceinline__ uint32_t cvt2(float lo, float hi) {
   }
 }
 
+// Two fp32 products in one instruction (x.lo * y.lo, x.hi * y.hi).
+__device__ __forceinline__ uint64_t mul2(uint64_t x, uint64_t y) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(x), "l"(y));
+  return d;
+}
+
 // floor(log2 |v|) of a positive finite float given its magnitude bits.
 __device__ __forceinline__ int floor_log2_bits(uint32_t a) {
   const int ef = static_cast<int>(a >> 23);
@@ -85,11 +118,12 @@ __device__ __forceinline__ int floor_log2_bits(uint32_t a) {
 }
 
 // Byte offset of the scale of row `r`, block `kb`, batch `l` in the
-// (L, t_r, t_k, 32, 4, 4) atom tensor (row r = 128 rt + 32 m1 + m0).
-__device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t kb, int64_t l, int64_t t_r,
-                                             int64_t t_k) {
-  const int64_t rt = r >> 7, rr = r & 127, kt = kb >> 2;
-  return (((l * t_r + rt) * t_k + kt) * 512) + (rr & 31) * 16 + (rr >> 5) * 4 + (kb & 3);
+// (L, t_r, t_k, 32, 4, 4) atom tensor (row r = 128 rt + 32 m1 + m0); the
+// whole tensor is below 2^31 bytes.
+__device__ __forceinline__ uint32_t sf_offset(uint32_t r, uint32_t kb, uint32_t l, uint32_t t_r,
+                                              uint32_t t_k) {
+  const uint32_t rt = r >> 7, rr = r & 127, kt = kb >> 2;
+  return (((l * t_r + rt) * t_k + kt) << 9) + (rr & 31) * 16 + (rr >> 5) * 4 + (kb & 3);
 }
 
 template <int IN_BF16, int OUT, int SFV>
@@ -97,25 +131,26 @@ __global__ void __launch_bounds__(kThreads) bsq_quantize_kernel(const QParams p)
   constexpr int E = IN_BF16 ? 8 : 4;   // elements per chunk
   constexpr int G = SFV / E;           // lanes per scale block (2..8)
   constexpr int kCodeBytes = OUT == kOutE2M1 ? E / 2 : E;
+  constexpr int kUnroll = unroll_of(IN_BF16);
   using F = OutFmt<OUT>;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
 
-  for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-    const int64_t flat_row = u / p.units_per_row;
-    const int64_t seg = u - flat_row * p.units_per_row;
-    const int64_t l = flat_row / p.rows;
-    const int64_t r = flat_row - l * p.rows;
-    const uint8_t* xrow = p.x + flat_row * p.cols * (IN_BF16 ? 2 : 4);
-    uint8_t* crow = p.codes + flat_row * (OUT == kOutE2M1 ? p.cols / 2 : p.cols);
+  for (uint32_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    const uint32_t flat_row = fdiv(u, p.upr);
+    const uint32_t seg = u - flat_row * p.upr.d;
+    const uint32_t l = fdiv(flat_row, p.rows_div);
+    const uint32_t r = flat_row - l * p.rows;
+    const uint8_t* xrow = p.x + static_cast<int64_t>(flat_row) * p.row_in_bytes;
+    uint8_t* crow = p.codes + static_cast<int64_t>(flat_row) * p.row_code_bytes;
     // all loads of the unit first, then the arithmetic
     uint4 raw[kUnroll];
-    int64_t ch[kUnroll];
+    uint32_t ch[kUnroll];
 #pragma unroll
     for (int i = 0; i < kUnroll; ++i) {
-      ch[i] = (seg * kUnroll + i) * kThreads + tid;
+      ch[i] = (seg * kUnroll + i) * kThreads + tid;  // < 2^31: cols < 2^31
       raw[i] = ch[i] < p.chunks_per_row
-                   ? __ldcs(reinterpret_cast<const uint4*>(xrow + ch[i] * kChunkBytes))
+                   ? __ldcs(reinterpret_cast<const uint4*>(xrow + static_cast<size_t>(ch[i]) * kChunkBytes))
                    : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
@@ -135,10 +170,17 @@ __global__ void __launch_bounds__(kThreads) bsq_quantize_kernel(const QParams p)
         for (int j = 0; j < 4; ++j) v[j] = __uint_as_float(w[j]);
       }
       // block maximum of the magnitude bits (NaN and infinity order above
-      // every finite value)
+      // every finite value); bf16 pairs by a SIMD max of the 16-bit halves
       uint32_t amax = 0u;
+      if (IN_BF16) {
+        uint32_t m2 = 0u;
 #pragma unroll
-      for (int j = 0; j < E; ++j) amax = max(amax, __float_as_uint(v[j]) & 0x7FFFFFFFu);
+        for (int j = 0; j < 4; ++j) m2 = __vmaxu2(m2, w[j] & 0x7FFF7FFFu);
+        amax = max(m2 & 0xFFFFu, m2 >> 16) << 16;
+      } else {
+#pragma unroll
+        for (int j = 0; j < E; ++j) amax = max(amax, __float_as_uint(v[j]) & 0x7FFFFFFFu);
+      }
 #pragma unroll
       for (int off = 1; off < G; off <<= 1) amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
       if (!valid) continue;
@@ -165,24 +207,34 @@ __global__ void __launch_bounds__(kThreads) bsq_quantize_kernel(const QParams p)
           out[0] = nan * 0x01010101u;
           out[1] = nan * 0x01010101u;
         }
-      } else if (OUT == kOutE2M1) {
-        // E/2 bytes, element 2j in the low nibble of byte j
-#pragma unroll
-        for (int j = 0; j < E / 2; ++j)
-          out[j / 4] |= cvt2<OUT>(v[2 * j] * inv, v[2 * j + 1] * inv) << (8 * (j % 4));
       } else {
+        // scaled pairs (exact: a power of two), then two codes per conversion
+        const uint64_t inv2 = (static_cast<uint64_t>(__float_as_uint(inv)) << 32) | __float_as_uint(inv);
+        float y[E];
 #pragma unroll
-        for (int j = 0; j < E / 2; ++j)
-          out[j / 2] |= cvt2<OUT>(v[2 * j] * inv, v[2 * j + 1] * inv) << (16 * (j % 2));
+        for (int j = 0; j < E / 2; ++j) {
+          const uint64_t pr = (static_cast<uint64_t>(__float_as_uint(v[2 * j + 1])) << 32) |
+                              __float_as_uint(v[2 * j]);
+          const uint64_t sc = mul2(pr, inv2);
+          y[2 * j] = __uint_as_float(static_cast<uint32_t>(sc));
+          y[2 * j + 1] = __uint_as_float(static_cast<uint32_t>(sc >> 32));
+        }
+        if (OUT == kOutE2M1) {
+          // E/2 bytes, element 2j in the low nibble of byte j
+#pragma unroll
+          for (int j = 0; j < E / 2; ++j)
+            out[j / 4] |= cvt2<OUT>(y[2 * j], y[2 * j + 1]) << (8 * (j % 4));
+        } else {
+#pragma unroll
+          for (int j = 0; j < E / 2; ++j)
+            out[j / 2] |= cvt2<OUT>(y[2 * j], y[2 * j + 1]) << (16 * (j % 2));
+        }
       }
-      uint8_t* cdst = crow + ch[i] * kCodeBytes;
+      uint8_t* cdst = crow + static_cast<size_t>(ch[i]) * kCodeBytes;
       if (kCodeBytes == 8) *reinterpret_cast<uint2*>(cdst) = make_uint2(out[0], out[1]);
       else if (kCodeBytes == 4) *reinterpret_cast<uint32_t*>(cdst) = out[0];
       else *reinterpret_cast<uint16_t*>(cdst) = static_cast<uint16_t>(out[0]);
-      if ((lane % G) == 0) {
-        const int64_t kb = ch[i] / G;
-        p.sf[sf_offset(r, kb, l, p.t_r, p.t_k)] = static_cast<uint8_t>(byte);
-      }
+      if ((lane % G) == 0) p.sf[sf_offset(r, ch[i] / G, l, p.t_r, p.t_k)] = static_cast<uint8_t>(byte);
     }
   }
 
@@ -190,10 +242,11 @@ __global__ void __launch_bounds__(kThreads) bsq_quantize_kernel(const QParams p)
   // past `nblk` in the last K atoms (the loop above writes every other byte)
   const bool pad_rows = (p.rows & 127) != 0, pad_k = (p.nblk & 3) != 0;
   if (!pad_rows && !pad_k) return;
-  const int64_t atoms = p.L * (p.t_k + p.t_r);
-  for (int64_t a = blockIdx.x; a < atoms; a += gridDim.x) {
-    int64_t l = a / (p.t_k + p.t_r), rt, kt;
-    const int64_t j = a - l * (p.t_k + p.t_r);
+  const uint32_t atoms = p.L * (p.t_k + p.t_r);
+  for (uint32_t a = blockIdx.x; a < atoms; a += gridDim.x) {
+    const uint32_t l = a / (p.t_k + p.t_r);
+    const uint32_t j = a - l * (p.t_k + p.t_r);
+    uint32_t rt, kt;
     if (j < p.t_k) {
       if (!pad_rows) continue;
       rt = p.t_r - 1;
@@ -203,11 +256,11 @@ __global__ void __launch_bounds__(kThreads) bsq_quantize_kernel(const QParams p)
       rt = j - p.t_k;
       kt = p.t_k - 1;
     }
-    for (int b = tid; b < 512; b += kThreads) {
-      const int m0 = b >> 4, m1 = (b >> 2) & 3, kin = b & 3;
-      const int64_t row = rt * 128 + m1 * 32 + m0, kb = kt * 4 + kin;
+    for (uint32_t b = tid; b < 512; b += kThreads) {
+      const uint32_t m0 = b >> 4, m1 = (b >> 2) & 3, kin = b & 3;
+      const uint32_t row = rt * 128 + m1 * 32 + m0, kb = kt * 4 + kin;
       if (row >= p.rows || kb >= p.nblk)
-        p.sf[((l * p.t_r + rt) * p.t_k + kt) * 512 + b] = 127u;
+        p.sf[(((l * p.t_r + rt) * p.t_k + kt) << 9) + b] = 127u;
     }
   }
 }
@@ -241,6 +294,12 @@ bsg_status bsg_quant_check(const bsg_quant_problem* q) {
   if (q->rows < 1 || q->cols < 1 || q->L < 1) return BSG_ERR_INVALID_ARG;
   if (q->rows > lim || q->cols > lim || q->L > lim || q->rows * q->L > lim)
     return BSG_ERR_INVALID_ARG;
+  // the scale atom tensor is indexed with 32-bit offsets
+  if (q->sf_vec_size == 16 || q->sf_vec_size == 32) {
+    const int64_t sf_bytes =
+        q->L * ((q->rows + 127) / 128) * ((q->cols / q->sf_vec_size + 3) / 4) * 512;
+    if (sf_bytes > lim) return BSG_ERR_INVALID_ARG;
+  }
   if (q->in_dtype != BSG_F32 && q->in_dtype != BSG_BF16) return BSG_ERR_INVALID_ARG;
   if (q->out_dtype != BSG_E4M3 && q->out_dtype != BSG_E5M2 && q->out_dtype != BSG_E2M1)
     return BSG_ERR_INVALID_ARG;
@@ -294,20 +353,26 @@ bsg_status bsg_quantize(const bsg_quant_problem* q, const void* X, void* codes, 
   p.x = static_cast<const uint8_t*>(X);
   p.codes = static_cast<uint8_t*>(codes);
   p.sf = static_cast<uint8_t*>(sf);
-  p.rows = q->rows;
-  p.cols = q->cols;
-  p.L = q->L;
-  p.chunks_per_row = q->cols / elems;
-  p.units_per_row = cdiv(p.chunks_per_row, int64_t(kThreads) * kUnroll);
-  p.num_units = q->L * q->rows * p.units_per_row;
-  p.nblk = q->cols / q->sf_vec_size;
-  p.t_r = cdiv(q->rows, 128);
-  p.t_k = cdiv(p.nblk, 4);
+  p.row_in_bytes = q->cols * (in_bf16 ? 2 : 4);
+  p.row_code_bytes = q->out_dtype == BSG_E2M1 ? q->cols / 2 : q->cols;
+  p.rows = static_cast<uint32_t>(q->rows);
+  p.cols = static_cast<uint32_t>(q->cols);
+  p.L = static_cast<uint32_t>(q->L);
+  p.chunks_per_row = static_cast<uint32_t>(q->cols / elems);
+  const int64_t upr = cdiv(p.chunks_per_row, int64_t(kThreads) * unroll_of(in_bf16));
+  const int64_t units = q->L * q->rows * upr;
+  if (units > (int64_t(1) << 31) - 1) return BSG_ERR_INVALID_ARG;
+  p.num_units = static_cast<uint32_t>(units);
+  p.upr = make_fastdiv(static_cast<uint32_t>(upr));
+  p.rows_div = make_fastdiv(p.rows);
+  p.nblk = static_cast<uint32_t>(q->cols / q->sf_vec_size);
+  p.t_r = static_cast<uint32_t>(cdiv(q->rows, 128));
+  p.t_k = static_cast<uint32_t>(cdiv(p.nblk, 4));
   const int out = q->out_dtype == BSG_E4M3 ? kOutE4M3 : (q->out_dtype == BSG_E5M2 ? kOutE5M2 : kOutE2M1);
   const void* fn = pick_kernel(in_bf16, out, q->sf_vec_size);
   // enough resident CTAs per SM to keep 16-byte loads in flight for HBM
   const int64_t want = static_cast<int64_t>(sms) * 8;
-  const int64_t extra = q->L * (p.t_k + p.t_r);
+  const int64_t extra = static_cast<int64_t>(p.L) * (p.t_k + p.t_r);
   int64_t grid = p.num_units > extra ? p.num_units : extra;
   if (grid > want) grid = want;
   if (grid < 1) grid = 1;
