@@ -405,14 +405,40 @@ int bsgo_gemm_sample(const int64_t *dims, int a_dtype, int b_dtype, int sf_dtype
 
 /* significand bits p (with the hidden bit), smallest normal exponent, largest
  * exponent, of the output formats */
+/* precision p (with the hidden bit), smallest normal exponent, largest
+ * exponent of each output format */
 static int out_format(int c_dtype, int *p, int *emin, int *emax)
 {
     switch (c_dtype) {
     case BSGO_F32: *p = 24; *emin = -126; *emax = 127; return 0;
     case BSGO_F16: *p = 11; *emin = -14; *emax = 15; return 0;
     case BSGO_BF16: *p = 8; *emin = -126; *emax = 127; return 0;
+    case BSGO_E4M3: *p = 4; *emin = -6; *emax = 8; return 0;
+    case BSGO_E5M2: *p = 3; *emin = -14; *emax = 15; return 0;
+    case BSGO_E2M1: *p = 2; *emin = 0; *emax = 2; return 0;
     default: return -1;
     }
+}
+
+static int quant_format(int dtype, int *emax, unsigned *maxc, unsigned *sign, unsigned *nanc);
+static unsigned nearest_code(double y, const double *tab, unsigned maxc, unsigned sign);
+
+/* Low-precision C ("GEMM + Amax (SM100)", "Parameters": C may be
+ * float8_e4m3fn, float8_e5m2 or packed float4_e2m1fn_x2, with no scale; the
+ * page does not say how the fp32 result is converted).  The reading used:
+ * round to nearest even, magnitudes past the largest finite value (and
+ * infinities) saturate to it, NaN stays NaN in E4M3 / E5M2 and becomes +0 in
+ * E2M1, which has no NaN. */
+static double round_low_precision(double x, int c_dtype)
+{
+    int emax;
+    unsigned maxc, sign, nanc;
+    double tab[256];
+    if (quant_format(c_dtype, &emax, &maxc, &sign, &nanc) != 0) return NAN;
+    bsgo_decode_table(c_dtype, tab);
+    if (isnan(x)) return c_dtype == BSGO_E2M1 ? 0.0 : NAN;
+    if (isinf(x)) return copysign(tab[maxc], x);
+    return tab[nearest_code(x, tab, maxc, sign)];
 }
 
 /* Round x to the nearest value of the output format, ties to even, overflow
@@ -422,6 +448,8 @@ double bsgo_round(double x, int c_dtype)
     int p, emin, emax, E;
     double q, r;
     if (out_format(c_dtype, &p, &emin, &emax) != 0) return NAN;
+    if (c_dtype == BSGO_E4M3 || c_dtype == BSGO_E5M2 || c_dtype == BSGO_E2M1)
+        return round_low_precision(x, c_dtype);
     if (isnan(x) || isinf(x) || x == 0.0) return x;
     frexp(fabs(x), &E);            /* |x| = f * 2^E, f in [0.5, 1) */
     E -= 1;                        /* |x| in [2^E, 2^(E+1)) */
@@ -432,7 +460,8 @@ double bsgo_round(double x, int c_dtype)
     return r;
 }
 
-/* Spacing of the output format at |x|: 2^(max(floor(log2|x|), emin) - (p-1)). */
+/* Spacing of the output format at |x|: 2^(max(floor(log2|x|), emin) - (p-1));
+ * a saturating format caps floor(log2|x|) at its largest exponent. */
 double bsgo_ulp(double x, int c_dtype)
 {
     int p, emin, emax, E;
@@ -442,6 +471,7 @@ double bsgo_ulp(double x, int c_dtype)
     frexp(fabs(x), &E);
     E -= 1;
     if (E < emin) E = emin;
+    if (E > emax) E = emax;
     return ldexp(1.0, E - (p - 1));
 }
 

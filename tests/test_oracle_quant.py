@@ -235,3 +235,47 @@ def test_matches_the_input_generator(dtype, sfv):
     codes_o, sf_o = oracle.quantize(x.astype(np.float64)[None], dtype, sfv)
     assert np.array_equal(codes_o[0], codes_g)
     assert np.array_equal(scale_bytes(sf_o, 64, 8)[0], sf_g.astype(np.int64))
+
+
+# ------------------------------------------------- low-precision C rounding
+
+@pytest.mark.parametrize("dtype,tdt", [("e4m3", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)])
+def test_c_rounding_matches_torch_saturated(dtype, tdt):
+    """C rounded to FP8: round to nearest even with saturation, i.e. torch's
+    (round-to-nearest-even) cast of the value clamped to the largest finite
+    magnitude, decoded back."""
+    rng = np.random.default_rng(23)
+    m = MAXV[dtype]
+    x = (np.exp2(rng.uniform(-24, np.log2(m) + 3, 20000)) *
+         rng.choice([-1, 1], 20000)).astype(np.float32)
+    want = torch.from_numpy(np.clip(x, -m, m)).to(tdt).to(torch.float64).numpy()
+    got = oracle.round_to(x.astype(np.float64), dtype)
+    assert np.array_equal(got, want)
+
+
+def test_c_rounding_e2m1_grid_and_specials():
+    vals = [Fraction(v).limit_denominator(4) for v in E2M1_VALUES[:8]]
+    ys = [Fraction(i, 64) for i in range(-9 * 64, 9 * 64 + 1)]
+    got = oracle.round_to(np.array([float(y) for y in ys]), "e2m1")
+    for y, g in zip(ys, got):
+        a = abs(y)
+        c = 7 if a >= vals[-1] else min(range(8), key=lambda c: (abs(vals[c] - a), c & 1))
+        want = float(vals[c]) * (-1.0 if y < 0 else 1.0)
+        assert g == want, float(y)
+    spec = oracle.round_to(np.array([np.nan, np.inf, -np.inf]), "e2m1")
+    assert spec[0] == 0.0 and spec[1] == 6.0 and spec[2] == -6.0
+    spec = oracle.round_to(np.array([np.nan, np.inf, -np.inf, 1e30]), "e4m3")
+    assert np.isnan(spec[0]) and list(spec[1:]) == [448.0, -448.0, 448.0]
+
+
+@pytest.mark.parametrize("dtype,spacing_at_1,emax", [("e4m3", 0.125, 8), ("e5m2", 0.25, 15),
+                                                     ("e2m1", 0.5, 2)])
+def test_c_ulp(dtype, spacing_at_1, emax):
+    """The tolerance's ulp: the gap between neighbouring codes at |x|, taken
+    from the decode table (capped at the largest binade)."""
+    assert oracle.ulp(1.0, dtype) == spacing_at_1
+    tab = np.sort(np.unique(np.abs(oracle.decode_table(dtype)[np.isfinite(oracle.decode_table(dtype))])))
+    for lo, hi in zip(tab[1:-1], tab[2:]):
+        if lo >= 2.0 ** (emax - 3):   # normal range: the spacing right above lo
+            assert oracle.ulp(lo, dtype) == hi - lo or lo >= 2.0 ** emax
+    assert oracle.ulp(tab[-1] * 4, dtype) == oracle.ulp(tab[-1], dtype)
