@@ -415,6 +415,50 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Para
 
 __device__ __forceinline__ uint32_t abs_bits_f32(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
 
+// Low-precision C: two fp32 values -> two codes, round to nearest even,
+// saturating (`lo` in the low byte / nibble).  E2M1 has no NaN: a NaN is
+// stored as +0.
+__device__ __forceinline__ uint32_t cvt2_e4m3(float lo, float hi) {
+  uint16_t h;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(hi), "f"(lo));
+  return h;
+}
+__device__ __forceinline__ uint32_t cvt2_e5m2(float lo, float hi) {
+  uint16_t h;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(h) : "f"(hi), "f"(lo));
+  return h;
+}
+__device__ __forceinline__ uint32_t cvt2_e2m1(float lo, float hi) {
+  uint32_t r;
+  lo = lo != lo ? 0.0f : lo;
+  hi = hi != hi ? 0.0f : hi;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// |value| of a low-precision code (sign ignored) as an fp32, from the
+// format's fields: E4M3 (bias 7, S.1111.111 NaN), E5M2 (bias 15, IEEE-like
+// infinity / NaN), E2M1 (bias 1, no specials).
+__device__ __forceinline__ float decode_mag(uint32_t code, int c_dtype) {
+  if (c_dtype == BSG_E4M3) {
+    const uint32_t e = (code >> 3) & 15u, m = code & 7u;
+    if (e == 15u && m == 7u) return __uint_as_float(0x7FC00000u);
+    if (e == 0u) return static_cast<float>(m) * 0.001953125f;  // m * 2^-9
+    return __uint_as_float(((e + 120u) << 23) | (m << 20));
+  }
+  if (c_dtype == BSG_E5M2) {
+    const uint32_t e = (code >> 2) & 31u, m = code & 3u;
+    if (e == 31u) return __uint_as_float(m ? 0x7FC00000u : 0x7F800000u);
+    if (e == 0u) return static_cast<float>(m) * 1.52587890625e-05f;  // m * 2^-16
+    return __uint_as_float(((e + 112u) << 23) | (m << 21));
+  }
+  const uint32_t e = (code >> 1) & 3u, m = code & 1u;
+  if (e == 0u) return 0.5f * static_cast<float>(m);
+  return __uint_as_float(((e + 126u) << 23) | (m << 22));
+}
+
 // A warp's 32 rows of W 32-bit words (row t in lane t's v[0..W)) to global
 // memory, row-major with a pitch of `pitch` bytes from `g` (row 0, word 0),
 // through the warp's 2 KB staging buffer `stg`.  Each store instruction then
@@ -813,11 +857,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int h = (warp - kEpiWarp0) >> 2;
     uint8_t* const stg = smem + p.smem_epi + (warp - kEpiWarp0) * kEpiStageBytes;
-    uint32_t vmax = 0;  // max |stored value| as fp32 bits
-    // 16-bit C: the largest magnitudes kept as two packed 16-bit halves (the
-    // magnitude bits of a 16-bit float order like its value, so an unsigned
-    // SIMD max finds it), widened to fp32 bits once at the end
-    uint32_t vmax16 = 0;
+    // max |stored value|, kept per C dtype and turned into fp32 bits at the
+    // end: fp32 C -> the fp32 bits; 16-bit C -> two packed 16-bit magnitudes
+    // (they order like their values, so an unsigned SIMD max finds the
+    // largest); FP8 / E2M1 C -> the largest stored |C| before rounding
+    uint32_t vmax = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = unit0; u < p.num_units; u += unit_step) {
@@ -843,10 +887,85 @@ __global__ void __launch_bounds__(kThreads, 1)
           else mbar_arrive(release_bar);
         }
       };
-      if (p.c_dtype != BSG_F32) {
+      // packed rounded values of the 16- and 8-bit paths, and the two-deep
+      // tensor-memory load buffer (chunk c converts while chunk c + 1 loads)
+      uint32_t pk[kCols / 2];
+      uint32_t rb[2][16];
+      if (KIND != kKindF8F6F4 &&
+          (p.c_dtype == BSG_E4M3 || p.c_dtype == BSG_E5M2 || p.c_dtype == BSG_E2M1)) {
+        // FP8 or packed E2M1 C (FP4 operands only): each 16-column chunk is
+        // converted as it leaves tensor memory; Amax is the rounded value of
+        // the largest stored magnitude (the rounding is monotone in |x|).
+        // pk: four FP8 codes per register (E2M1: eight, the first kCols/8)
+        const bool fp4 = p.c_dtype == BSG_E2M1, e5 = p.c_dtype == BSG_E5M2;
+        tc_ld_32x32b_x16(taddr, rb[0]);
+        tc_wait_ld();
+#pragma unroll
+        for (int cc = 0; cc < kCols; cc += 16) {
+          uint32_t* r = rb[(cc / 16) & 1];
+          if (cc + 16 < kCols) tc_ld_32x32b_x16(taddr + cc + 16, rb[((cc / 16) + 1) & 1]);
+          const bool whole = row_ok && n0 + cc + 16 <= p.N;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            uint32_t a = r[j] & 0x7FFFFFFFu;
+            if (fp4 && a > 0x7F800000u) a = 0u;  // stored as +0
+            if (!whole && !(row_ok && n0 + cc + j < p.N)) a = 0u;
+            vmax = max(vmax, a);
+          }
+          if (fp4) {
+            uint32_t w0 = 0u, w1 = 0u;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t b = cvt2_e2m1(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+              if (j < 4) w0 |= b << (8 * j);
+              else w1 |= b << (8 * (j - 4));
+            }
+            pk[cc / 8] = w0;
+            pk[cc / 8 + 1] = w1;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) {
+              const float a0 = __uint_as_float(r[2 * j]), a1 = __uint_as_float(r[2 * j + 1]);
+              const float b0 = __uint_as_float(r[2 * j + 2]), b1 = __uint_as_float(r[2 * j + 3]);
+              const uint32_t lo = e5 ? cvt2_e5m2(a0, a1) : cvt2_e4m3(a0, a1);
+              const uint32_t hi = e5 ? cvt2_e5m2(b0, b1) : cvt2_e4m3(b0, b1);
+              pk[cc / 4 + j / 2] = lo | (hi << 16);
+            }
+          }
+          tc_wait_ld();
+        }
+        release();
+        uint8_t* const cbase = static_cast<uint8_t*>(p.c) + (fp4 ? batch_off / 2 : batch_off);
+        if (p.c_major == 0) {
+          const int row0 = tc.mt * kTileM + q * 32;
+          if (fp4) {
+            // kCols / 2 bytes per row: one staged chunk
+            char* const g0 = reinterpret_cast<char*>(cbase + static_cast<size_t>(row0) * (p.N / 2) + n0 / 2);
+            // (an FP8-operand kernel never takes this branch; its width only
+            // has to name a valid chunk)
+            constexpr int kW4 = (kCols / 8 == 8 || kCols / 8 == 16) ? kCols / 8 : 8;
+            store_rows_coalesced<kW4>(stg, pk, lane, g0, static_cast<size_t>(p.N / 2), p.M - row0,
+                                      (p.N - n0) / 2);
+          } else {
+            char* const g0 = reinterpret_cast<char*>(cbase + static_cast<size_t>(row0) * p.N + n0);
+#pragma unroll
+            for (int cc = 0; cc + 64 <= kCols; cc += 64)
+              store_rows_coalesced<16>(stg, pk + cc / 4, lane, g0 + cc, static_cast<size_t>(p.N),
+                                       p.M - row0, p.N - n0 - cc);
+          }
+        } else {
+          // m-major FP8: column by column, the 32 lanes write 32 consecutive rows
+          uint8_t* dst = cbase + static_cast<size_t>(n0) * p.M + row;
+          const int ncols = row_ok ? min(kCols, p.N - n0) : 0;
+#pragma unroll
+          for (int j = 0; j < kCols; ++j) {
+            if (j < ncols) *dst = static_cast<uint8_t>(pk[j / 4] >> (8 * (j % 4)));
+            dst += p.M;
+          }
+        }
+      } else if (p.c_dtype != BSG_F32) {
+        // pk: two rounded 16-bit values per register
         const bool bf = p.c_dtype == BSG_BF16;
-        uint32_t pk[kCols / 2];  // two rounded 16-bit values per register
-        uint32_t rb[2][16];      // chunk c converts while chunk c + 1 loads
         tc_ld_32x32b_x16(taddr, rb[0]);
         tc_wait_ld();
 #pragma unroll
@@ -876,7 +995,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!(row_ok && n < p.N)) m &= 0xFFFF0000u;
               if (!(row_ok && n + 1 < p.N)) m &= 0x0000FFFFu;
             }
-            vmax16 = __vmaxu2(vmax16, m);
+            vmax = __vmaxu2(vmax, m);
           }
           tc_wait_ld();
         }
@@ -958,11 +1077,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    {
-      const uint32_t hmax = max(vmax16 & 0xFFFFu, vmax16 >> 16);
-      vmax = max(vmax, p.c_dtype == BSG_BF16
-                           ? hmax << 16
-                           : abs_bits_f32(__half2float(__ushort_as_half(static_cast<unsigned short>(hmax)))));
+    if (KIND != kKindF8F6F4 &&
+        (p.c_dtype == BSG_E4M3 || p.c_dtype == BSG_E5M2 || p.c_dtype == BSG_E2M1)) {
+      // the stored magnitude of the largest |C|: round it like the stores did
+      const float mx = __uint_as_float(vmax);
+      const uint32_t code = p.c_dtype == BSG_E2M1 ? cvt2_e2m1(mx, 0.0f) & 0xFu
+                            : p.c_dtype == BSG_E5M2 ? cvt2_e5m2(mx, 0.0f) & 0xFFu
+                                                    : cvt2_e4m3(mx, 0.0f) & 0xFFu;
+      vmax = abs_bits_f32(decode_mag(code, p.c_dtype));
+    } else if (p.c_dtype != BSG_F32) {
+      const uint32_t hmax = max(vmax & 0xFFFFu, vmax >> 16);
+      vmax = p.c_dtype == BSG_BF16
+                 ? hmax << 16
+                 : abs_bits_f32(__half2float(__ushort_as_half(static_cast<unsigned short>(hmax))));
     }
     vmax = __reduce_max_sync(0xFFFFFFFFu, vmax);
     if (lane == 0) atomicMax(cta_amax, vmax);
@@ -1066,7 +1193,16 @@ constexpr size_t kWorkspaceBytes = 256;
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
-inline int c_size(int d) { return d == BSG_F32 ? 4 : 2; }
+// bytes of C's contiguous extent of `n` elements
+inline int64_t c_extent_bytes(int64_t n, int d) {
+  switch (d) {
+    case BSG_F32: return n * 4;
+    case BSG_F16:
+    case BSG_BF16: return n * 2;
+    case BSG_E2M1: return n / 2;
+    default: return n;  // FP8
+  }
+}
 
 }  // namespace
 
@@ -1121,13 +1257,15 @@ bsg_status bsg_problem_check(const bsg_problem* p) {
     if (d != BSG_E4M3 && d != BSG_E5M2 && d != BSG_E2M1) return BSG_ERR_INVALID_ARG;
   if (p->sf_dtype == BSG_E4M3) return BSG_ERR_UNSUPPORTED;  // NVFP4-style scales
   if (p->sf_dtype != BSG_UE8M0) return BSG_ERR_INVALID_ARG;
-  if (p->c_dtype == BSG_E4M3 || p->c_dtype == BSG_E5M2 || p->c_dtype == BSG_E2M1)
-    return BSG_ERR_UNSUPPORTED;  // low-precision C
-  if (p->c_dtype != BSG_F32 && p->c_dtype != BSG_F16 && p->c_dtype != BSG_BF16)
+  const bool c_low = p->c_dtype == BSG_E4M3 || p->c_dtype == BSG_E5M2 || p->c_dtype == BSG_E2M1;
+  if (!c_low && p->c_dtype != BSG_F32 && p->c_dtype != BSG_F16 && p->c_dtype != BSG_BF16)
     return BSG_ERR_INVALID_ARG;
   if (p->sf_vec_size != 16 && p->sf_vec_size != 32) return BSG_ERR_INVALID_ARG;
   const bool a4 = p->a_dtype == BSG_E2M1, b4 = p->b_dtype == BSG_E2M1;
   if (a4 != b4) return BSG_ERR_UNSUPPORTED;                  // FP4 x FP8
+  // low-precision C ("Support surface", "Dtypes"): FP8 C with FP8 operands
+  // is disabled, E2M1 C needs FP4 operands and an n-major C
+  if (c_low && !a4) return BSG_ERR_UNSUPPORTED;
   if (!a4 && p->sf_vec_size == 16) return BSG_ERR_UNSUPPORTED;  // FP8 needs sfv 32
   const char majors[2] = {p->a_major, p->b_major};
   for (char mj : majors) {
@@ -1135,6 +1273,7 @@ bsg_status bsg_problem_check(const bsg_problem* p) {
     if (mj != 'k') return BSG_ERR_INVALID_ARG;
   }
   if (p->c_major != 'n' && p->c_major != 'm') return BSG_ERR_INVALID_ARG;
+  if (p->c_dtype == BSG_E2M1 && p->c_major != 'n') return BSG_ERR_UNSUPPORTED;
   if (p->tile_m != 0 && p->tile_m != 128) return BSG_ERR_INVALID_ARG;
   if (p->tile_n != 0 && p->tile_n != 128 && p->tile_n != 224 && p->tile_n != 256)
     return BSG_ERR_INVALID_ARG;
@@ -1144,8 +1283,9 @@ bsg_status bsg_problem_check(const bsg_problem* p) {
   const int64_t row_bytes = a4 ? p->K / 2 : p->K;
   if (a4 && (p->K % 2)) return BSG_ERR_ALIGNMENT;
   if (row_bytes % 16) return BSG_ERR_ALIGNMENT;
-  const int64_t c_row = (p->c_major == 'n' ? p->N : p->M) * c_size(p->c_dtype);
-  if (c_row % 16) return BSG_ERR_ALIGNMENT;
+  const int64_t c_n = p->c_major == 'n' ? p->N : p->M;
+  if (p->c_dtype == BSG_E2M1 && (c_n % 2)) return BSG_ERR_ALIGNMENT;
+  if (c_extent_bytes(c_n, p->c_dtype) % 16) return BSG_ERR_ALIGNMENT;
   return BSG_OK;
 }
 
@@ -1540,7 +1680,7 @@ bsg_status bsg_run_host(const bsg_plan* plan, const void* hA, const void* hB, co
   const size_t b_bytes = static_cast<size_t>(p.L * p.N) * (fp4 ? p.K / 2 : p.K);
   const size_t sfa_bytes = static_cast<size_t>(p.L * plan->base.t_m * plan->base.t_k) * kAtomBytes;
   const size_t sfb_bytes = static_cast<size_t>(p.L * plan->base.t_n * plan->base.t_k) * kAtomBytes;
-  const size_t c_bytes = static_cast<size_t>(p.L * p.M * p.N) * c_size(p.c_dtype);
+  const size_t c_bytes = static_cast<size_t>(p.L * p.M * c_extent_bytes(p.N, p.c_dtype));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (!dev->A || !dev->B || !dev->SFA || !dev->SFB || !dev->C || !dev->amax)
     return BSG_ERR_INVALID_ARG;

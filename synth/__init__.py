@@ -82,8 +82,8 @@ class Problem:
         return self.K // 2 if dtype == "e2m1" else self.K
 
     @property
-    def c_itemsize(self) -> int:
-        return {"f32": 4, "f16": 2, "bf16": 2}[self.c_dtype]
+    def c_itemsize(self) -> float:
+        return {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1, "e5m2": 1, "e2m1": 0.5}[self.c_dtype]
 
     def describe(self) -> str:
         ab = self.a_dtype if self.a_dtype == self.b_dtype else f"{self.a_dtype}x{self.b_dtype}"
@@ -267,7 +267,10 @@ def workload(number: int, **shape) -> Inputs:
 
 
 def c_shape(p: Problem):
-    """Memory shape of C: (L, M, N) for n-major, (L, N, M) for m-major."""
+    """Memory shape of C: (L, M, N) for n-major, (L, N, M) for m-major; packed
+    E2M1 C (n-major only) is (L, M, N/2) bytes."""
+    if p.c_dtype == "e2m1":
+        return (p.L, p.M, p.N // 2)
     return (p.L, p.M, p.N) if p.c_major == "n" else (p.L, p.N, p.M)
 
 

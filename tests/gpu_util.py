@@ -7,7 +7,10 @@ import block_scaled_precision_04_gb300 as bsg
 import oracle
 import synth
 
-TORCH_C = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+TORCH_C = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16,
+           "e4m3": torch.uint8, "e5m2": torch.uint8, "e2m1": torch.uint8}
+LOW_C = ("e4m3", "e5m2", "e2m1")
+POISON_BYTE = 0xA5
 
 
 def problem_of(p: synth.Problem, **hints) -> bsg.bsg_problem:
@@ -21,8 +24,18 @@ def to_device(inp: synth.Inputs, dev="cuda:0"):
 
 
 def c_to_logical(c: torch.Tensor, p: synth.Problem) -> np.ndarray:
-    """Device C in its memory layout -> float64 numpy (L, M, N)."""
-    x = c.float().cpu().numpy().astype(np.float64)
+    """Device C in its memory layout -> float64 numpy (L, M, N); FP8 / E2M1
+    codes are decoded with the oracle's tables."""
+    if p.c_dtype in LOW_C:
+        codes = c.cpu().numpy()
+        if p.c_dtype == "e2m1":
+            full = np.empty(codes.shape[:2] + (codes.shape[2] * 2,), dtype=np.uint8)
+            full[..., 0::2] = codes & 0xF
+            full[..., 1::2] = codes >> 4
+            codes = full
+        x = oracle.decode_table(p.c_dtype)[codes]
+    else:
+        x = c.float().cpu().numpy().astype(np.float64)
     return x if p.c_major == "n" else x.transpose(0, 2, 1)
 
 
@@ -32,10 +45,11 @@ def run_gpu(inp: synth.Inputs, op=None, runs=1, guard=0, **hints):
     if op is None:
         op = bsg.GemmAmax(problem_of(p, **hints))
     A, B, SFA, SFB = to_device(inp)
-    numel = p.L * p.M * p.N
-    poison = float("nan")
+    shape = synth.c_shape(p)
+    numel = int(np.prod(shape))
+    poison = POISON_BYTE if p.c_dtype in LOW_C else float("nan")
     buf = torch.full((numel + 2 * guard,), poison, dtype=TORCH_C[p.c_dtype], device="cuda:0")
-    C = buf[guard:guard + numel].view(synth.c_shape(p))
+    C = buf[guard:guard + numel].view(shape)
     amax = torch.full((1,), -1.0, dtype=torch.float32, device="cuda:0")
     for _ in range(runs):
         op.run(A, B, SFA, SFB, C, amax)
@@ -45,7 +59,8 @@ def run_gpu(inp: synth.Inputs, op=None, runs=1, guard=0, **hints):
     guard_ok = True
     if guard:
         g = torch.cat([buf[:guard], buf[guard + numel:]])
-        guard_ok = bool(torch.isnan(g.float()).all())
+        guard_ok = bool((g == POISON_BYTE).all()) if p.c_dtype in LOW_C else \
+            bool(torch.isnan(g.float()).all())
     return c_to_logical(C, p), float(amax.item()), C, op, guard_ok
 
 

@@ -91,6 +91,12 @@ OK_CASES = [
     dict(M=4, N=1, K=32, L=3, c_major="m"),
     dict(M=3, N=8, K=32, L=1, a_dtype="e2m1", b_dtype="e2m1", sf_vec_size=32, c_dtype="f16"),
     dict(M=128, N=128, K=128, L=1, tile_m=128, tile_n=256, cluster_m=2, cluster_n=1),
+    dict(M=256, N=256, K=256, L=1, a_dtype="e2m1", b_dtype="e2m1", sf_vec_size=16,
+         c_dtype="e4m3"),
+    dict(M=256, N=256, K=256, L=2, a_dtype="e2m1", b_dtype="e2m1", sf_vec_size=32,
+         c_dtype="e5m2", c_major="m"),
+    dict(M=130, N=96, K=128, L=1, a_dtype="e2m1", b_dtype="e2m1", sf_vec_size=16,
+         c_dtype="e2m1"),
 ]
 
 
@@ -114,6 +120,12 @@ BAD_CASES = [
     (dict(M=4, N=4, K=32, L=1, sf_dtype="f32"), bsg.BSG_ERR_INVALID_ARG, "scale dtype"),
     (dict(M=4, N=4, K=32, L=1, c_dtype="e4m3"), bsg.BSG_ERR_UNSUPPORTED, "FP8 in, FP8 out"),
     (dict(M=4, N=4, K=32, L=1, c_dtype="e2m1"), bsg.BSG_ERR_UNSUPPORTED, "FP4 C with FP8 in"),
+    (dict(M=4, N=64, K=64, L=1, a_dtype="e2m1", b_dtype="e2m1", sf_vec_size=16, c_dtype="e2m1",
+          c_major="m"), bsg.BSG_ERR_UNSUPPORTED, "FP4 C m-major"),
+    (dict(M=4, N=48, K=64, L=1, a_dtype="e2m1", b_dtype="e2m1", sf_vec_size=16, c_dtype="e2m1"),
+     bsg.BSG_ERR_ALIGNMENT, "FP4 C row of 24 bytes"),
+    (dict(M=4, N=24, K=64, L=1, a_dtype="e2m1", b_dtype="e2m1", sf_vec_size=16, c_dtype="e4m3"),
+     bsg.BSG_ERR_ALIGNMENT, "FP8 C row of 24 bytes"),
     (dict(M=4, N=4, K=32, L=1, c_dtype="ue8m0"), bsg.BSG_ERR_INVALID_ARG, "C dtype"),
     (dict(M=4, N=4, K=32, L=1, a_dtype="f32"), bsg.BSG_ERR_INVALID_ARG, "A dtype"),
     (dict(M=4, N=4, K=64, L=1, a_dtype="e2m1", b_dtype="e2m1", sf_vec_size=16, a_major="m"),
