@@ -34,6 +34,16 @@ import synth  # noqa: E402
 
 METRIC = "block-scaled GEMM+amax TFLOP/s on 1 GB300; % of FP8/FP4 dense tensor peak"
 L2_FLUSH_BYTES = 512 << 20  # > 4x the 129 MB L2
+L2_NOTE = ("flushed between timed steps: a 512 MiB buffer written, then read, so the "
+           "timed step starts with no input in L2 and no dirty lines to write back")
+
+
+def flush_l2(buf) -> None:
+    """Evict L2 outside the timed region: write a buffer larger than L2, then
+    read it so that the written lines are retired to HBM before the next
+    timed step rather than during it."""
+    buf.zero_()
+    buf.amax()
 NOMINAL_RATIO = {"fp8": 4.5 / 2.25, "fp4": 13.5 / 2.25}  # dense tensor peak vs bf16
 FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM bytes per launch of the GEMM kernel from an ncu capture, keyed by the
@@ -110,7 +120,7 @@ def config_of(number: int, p: synth.Problem, name: str) -> dict:
     return {"workload": name, "M": p.M, "N": p.N, "K": p.K, "L": p.L, "a_dtype": p.a_dtype,
             "b_dtype": p.b_dtype, "sf_vec_size": p.sfv, "sf_dtype": p.sf_dtype,
             "c_dtype": p.c_dtype, "c_major": p.c_major, "seed": 1000 + number,
-            "l2": "flushed between timed steps (512 MiB write)"}
+            "l2": L2_NOTE}
 
 
 # ------------------------------------------------------------ CPU oracle leg
@@ -120,7 +130,8 @@ def oracle_sample(inp, target_s: float, max_rows: int | None = None):
     sized so the run takes about target_s seconds."""
     import oracle
     p = inp.problem
-    args = (p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv, inp.A, inp.B, inp.SFA, inp.SFB)
+    args = (p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv, inp.A, inp.B, inp.SFA, inp.SFB,
+            p.sf_dtype)
     # calibrate on enough rows to keep every oracle thread busy (the oracle
     # splits rows over threads), then size the sample; one more resize if the
     # sample ran well short of the target
@@ -216,7 +227,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     inp = synth.workload(args.workload)
     nums = workload_numbers(p)
     op = bsg.GemmAmax(bsg.make_problem(p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv,
-                                       p.c_dtype, p.c_major), device=local_rank)
+                                       p.c_dtype, p.c_major, sf_dtype=p.sf_dtype),
+                      device=local_rank)
     info = op.describe()
     hA, hB, hSFA, hSFB = [torch.from_numpy(np.ascontiguousarray(x)) for x in
                           (inp.A, inp.B, inp.SFA, inp.SFB)]
@@ -234,7 +246,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                               op.workspace.data_ptr(), op.ws_bytes, s), "bsg_run")
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2(flush)
         launch()
     torch.cuda.synchronize(dev)
     bsg.check(op.device_status(), "device status (warm-up)")
@@ -249,7 +261,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     with ClockSampler(local_rank) as clk:
         wall0 = time.perf_counter()
         for e0, e1 in evs:
-            flush.zero_()
+            flush_l2(flush)
             e0.record(stream)
             launch()
             e1.record(stream)
@@ -365,7 +377,7 @@ def run_quant(args, rank: int, world: int, local_rank: int):
     launch = lambda: bsg.check(bsg.bsg_quantize(q, X.data_ptr(), codes.data_ptr(), sf.data_ptr(), s),
                                "bsg_quantize")
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2(flush)
         launch()
     torch.cuda.synchronize(dev)
     dist = None
@@ -378,7 +390,7 @@ def run_quant(args, rank: int, world: int, local_rank: int):
     with ClockSampler(local_rank) as clk:
         wall0 = time.perf_counter()
         for e0, e1 in evs:
-            flush.zero_()
+            flush_l2(flush)
             e0.record(stream)
             launch()
             e1.record(stream)
@@ -431,7 +443,7 @@ def run_quant(args, rank: int, world: int, local_rank: int):
             "data": "synthetic (seeded; see synth.real_blocks)",
             "config": {"workload": name, "rows": rows, "cols": cols, "L": 1, "in_dtype": in_dtype,
                        "out_dtype": out_dtype, "sf_vec_size": sfv, "seed": 1500 + args.qworkload,
-                       "l2": "flushed between timed steps (512 MiB write)"},
+                       "l2": L2_NOTE},
             "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps,
             "clocks": clk.summary(), "wall_s_timed_region": round(wall, 4),
             "step_ms_min": round(min(times_ms), 5),
@@ -486,7 +498,8 @@ def run_reference(args):
     per_step = max(0.5, args.ref_seconds / max(1, args.steps + args.warmup))
     _, rows, _ = oracle_sample(inp, per_step)
     import oracle
-    pargs = (p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv, inp.A, inp.B, inp.SFA, inp.SFB)
+    pargs = (p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv, inp.A, inp.B, inp.SFA, inp.SFB,
+             p.sf_dtype)
     for _ in range(args.warmup):
         oracle.gemm(*pargs, rows=(0, rows), want_s=False)
     t0 = time.perf_counter()

@@ -1255,8 +1255,7 @@ bsg_status bsg_problem_check(const bsg_problem* p) {
   const int ops[2] = {p->a_dtype, p->b_dtype};
   for (int d : ops)
     if (d != BSG_E4M3 && d != BSG_E5M2 && d != BSG_E2M1) return BSG_ERR_INVALID_ARG;
-  if (p->sf_dtype == BSG_E4M3) return BSG_ERR_UNSUPPORTED;  // NVFP4-style scales
-  if (p->sf_dtype != BSG_UE8M0) return BSG_ERR_INVALID_ARG;
+  if (p->sf_dtype != BSG_UE8M0 && p->sf_dtype != BSG_E4M3) return BSG_ERR_INVALID_ARG;
   const bool c_low = p->c_dtype == BSG_E4M3 || p->c_dtype == BSG_E5M2 || p->c_dtype == BSG_E2M1;
   if (!c_low && p->c_dtype != BSG_F32 && p->c_dtype != BSG_F16 && p->c_dtype != BSG_BF16)
     return BSG_ERR_INVALID_ARG;
@@ -1267,6 +1266,8 @@ bsg_status bsg_problem_check(const bsg_problem* p) {
   // is disabled, E2M1 C needs FP4 operands and an n-major C
   if (c_low && !a4) return BSG_ERR_UNSUPPORTED;
   if (!a4 && p->sf_vec_size == 16) return BSG_ERR_UNSUPPORTED;  // FP8 needs sfv 32
+  // E4M3 scales ("Dtypes"): only the NVFP4 form, FP4 operands with sfv 16
+  if (p->sf_dtype == BSG_E4M3 && (!a4 || p->sf_vec_size != 16)) return BSG_ERR_UNSUPPORTED;
   const char majors[2] = {p->a_major, p->b_major};
   for (char mj : majors) {
     if (mj == 'm' || mj == 'n') return BSG_ERR_UNSUPPORTED;  // MN-major operands
@@ -1394,7 +1395,8 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   }
   const int mma_m = plan->pair ? 2 * kTileM : kTileM;
   k.idesc = (a_fmt << 7) | (b_fmt << 10) | (static_cast<uint32_t>(k.tile_n >> 3) << 17) |
-            (1u << 23) /* E8M0 scales */ | (static_cast<uint32_t>(mma_m >> 4) << 24);
+            (prob->sf_dtype == BSG_UE8M0 ? 1u << 23 : 0u) /* scale type: 1 UE8M0, 0 UE4M3 */ |
+            (static_cast<uint32_t>(mma_m >> 4) << 24);
   k.c_dtype = prob->c_dtype;
   k.c_major = prob->c_major == 'm' ? 1 : 0;
 

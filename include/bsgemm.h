@@ -3,10 +3,21 @@
  *
  * Operation ("GEMM + Amax (SM100)", section "Equations"):
  *
- *     Ahat[m,k,l] = dec(A[m,k,l]) * 2^(SFA[m, k/sf_vec_size, l] - 127)
- *     Bhat[n,k,l] = dec(B[n,k,l]) * 2^(SFB[n, k/sf_vec_size, l] - 127)
+ *     Ahat[m,k,l] = dec(A[m,k,l]) * sf(SFA[m, k/sf_vec_size, l])
+ *     Bhat[n,k,l] = dec(B[n,k,l]) * sf(SFB[n, k/sf_vec_size, l])
  *     C[m,n,l]    = sum_k Ahat[m,k,l] * Bhat[n,k,l]      (fp32 accumulation)
  *     Amax        = max_{m,n,l} |C[m,n,l]|               (of the stored C)
+ *
+ * sf(byte) is 2^(byte - 127) for E8M0 scale bytes and the float8_e4m3fn
+ * value of the byte for E4M3 scales (the NVFP4 form, "Dtypes").  E4M3 scale
+ * bytes must have the sign bit clear (the tensor cores read them as
+ * unsigned E4M3); a byte with it set gives unspecified results.
+ *
+ * C is stored rounded to its type, to nearest with ties to even.  For the
+ * low-precision C types (E4M3, E5M2, packed E2M1; "Support surface and
+ * constraints", "Dtypes") the rounding saturates to the largest finite
+ * value, a NaN stays NaN in FP8 and becomes +0 in E2M1 (which has no NaN),
+ * and Amax is the largest stored magnitude decoded back to fp32.
  *
  * Tensors ("Parameters", "Input/Output tensors"; all device memory of one
  * GPU, "Environment": all tensors on the same device):
@@ -15,24 +26,28 @@
  *        per byte; packed FP4 (E2M1) two per byte, element 2i in the low
  *        nibble, so a row holds K/2 bytes ("Layouts and strides").
  *   B    (N, K, L), k-major, same element type rules as A.
- *   SFA  E8M0 bytes, physical C-contiguous (L, ceil(M/128), ceil(K/(4*sfv)),
+ *   SFA  E8M0 (or E4M3) bytes, physical C-contiguous (L, ceil(M/128), ceil(K/(4*sfv)),
  *        32, 4, 4), which is the page's logical (32, 4, ceil(M/128), 4,
  *        ceil(K/(4*sfv)), L) view permuted ("Using JAX arrays").  Row
  *        m = 128*mt + 32*m1 + m0 and K-block kb = 4*kt + kin sit at byte
  *        ((l*T_m + mt)*T_k + kt)*512 + m0*16 + m1*4 + kin.
  *   SFB  the same for the N rows of B.
- *   C    (M, N, L), fp32 / fp16 / bf16, n-major strides (N, 1, M*N) or
- *        m-major strides (1, M, M*N).
+ *   C    (M, N, L), fp32 / fp16 / bf16 / E4M3 / E5M2, n-major strides
+ *        (N, 1, M*N) or m-major strides (1, M, M*N); packed E2M1 only
+ *        n-major, two per byte (element 2i of a row in the low nibble).
  *   Amax one fp32 (shape (1,1,1)); overwritten by every run, not accumulated.
  *
  * Padding entries of SFA/SFB (rows past M or N, K-blocks past
  * ceil(K/sfv)) multiply zero codes or rows that are never stored; they must
- * hold a finite scale (any byte but 0xFF) so that 0 * scale stays 0.
+ * hold a finite scale (any byte but 0xFF for E8M0; any byte but 0x7F and
+ * 0xFF for E4M3) so that 0 * scale stays 0.
  *
  * Support ("Support surface and constraints"): A/B k-major; A/B both FP8
- * (E4M3/E5M2, each on its own) with sf_vec_size 32, or both E2M1 with
- * sf_vec_size 16 or 32; E8M0 scales; C fp32/fp16/bf16.  Rows of A, B and C
- * must be 16-byte aligned along their contiguous dimension, every pointer
+ * (E4M3/E5M2, each on its own) with sf_vec_size 32 and E8M0 scales, or both
+ * E2M1 with sf_vec_size 32 and E8M0 scales or sf_vec_size 16 and E8M0 or
+ * E4M3 scales; C fp32/fp16/bf16 always, E4M3/E5M2/E2M1 with E2M1 operands
+ * only.  Rows of A, B and C must be 16-byte aligned along their contiguous
+ * dimension (an E2M1 C row of N/2 bytes included, N even), every pointer
  * 16-byte aligned.  Everything else returns BSG_ERR_UNSUPPORTED or
  * BSG_ERR_INVALID_ARG before any launch (errors are reported before launch,
  * as "Grouped GEMM (SM100 BF16)", "Scheduling, caching, and errors", does).
@@ -64,9 +79,9 @@ typedef enum {
 } bsg_status;
 
 typedef enum {
-    BSG_E4M3 = 0,   /* float8_e4m3fn codes (A/B) */
-    BSG_E5M2 = 1,   /* float8_e5m2 codes (A/B) */
-    BSG_E2M1 = 2,   /* float4_e2m1fn, packed two per byte (A/B) */
+    BSG_E4M3 = 0,   /* float8_e4m3fn codes (A/B/C) or scale bytes (SFA/SFB) */
+    BSG_E5M2 = 1,   /* float8_e5m2 codes (A/B/C) */
+    BSG_E2M1 = 2,   /* float4_e2m1fn, packed two per byte (A/B/C) */
     BSG_UE8M0 = 3,  /* float8_e8m0fnu scale bytes (SFA/SFB) */
     BSG_F32 = 4,    /* C */
     BSG_F16 = 5,    /* C */
@@ -82,8 +97,8 @@ typedef enum {
 typedef struct {
     int64_t M, N, K, L;
     int32_t a_dtype, b_dtype;   /* bsg_dtype */
-    int32_t sf_dtype;           /* BSG_UE8M0 */
-    int32_t c_dtype;            /* BSG_F32, BSG_F16 or BSG_BF16 */
+    int32_t sf_dtype;           /* BSG_UE8M0, or BSG_E4M3 (E2M1 A/B, sfv 16) */
+    int32_t c_dtype;            /* BSG_F32, BSG_F16, BSG_BF16, BSG_E4M3, BSG_E5M2, BSG_E2M1 */
     char a_major, b_major;      /* 'k' */
     char c_major;               /* 'n' or 'm' */
     char reserved0;

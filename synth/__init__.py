@@ -1,9 +1,10 @@
 """Seeded synthetic inputs for the block-scaled GEMM + Amax.
 
 This module only draws random numbers and encodes them into the input
-formats the operation consumes (FP8/FP4 codes plus E8M0 block scales laid out
-in the 128-row scale atoms).  It holds none of the operation's own arithmetic:
-no decoding, no dot products, no reductions.  Both the CUDA path's tests and
+formats the operation consumes (FP8/FP4 codes plus E8M0 or E4M3 block scales
+laid out in the 128-row scale atoms).  It holds none of the operation's own
+arithmetic: no decoding tables, no dot products, no reductions (torch's
+float8 casts encode, and for the E4M3 scale recipe decode, single values).  Both the CUDA path's tests and
 the CPU oracle are fed from here; neither of them is imported.
 
 Layouts produced (page "GEMM + Amax (SM100)", section "Parameters"):
@@ -30,6 +31,10 @@ Workloads (seed = 1000 + workload number):
    C bf16 n-major.
 5. Ragged MXFP8 L=2, 8000x1000x7168: A ~ U[-1,1], B ~ N(0, 0.02), E4M3;
    C fp32 m-major.
+6. NVFP4 8192^3, L=1: A, B ~ N(0,1), per-16 K-block E2M1 with an E4M3 scale
+   byte = the block amax / 6 rounded to E4M3 (nearest, ties to even; at least
+   the smallest subnormal, 1.0 for an all-zero block), each element divided
+   by the decoded scale, saturated to +-6 and rounded to E2M1; C bf16 n-major.
 
 The exponent offset of a block scale is the element format's largest
 exponent (E4M3 8, E5M2 15, E2M1 2); the scaled block is saturated to the
@@ -112,7 +117,11 @@ WORKLOADS = {
         Problem(8192, 8192, 8192, 1, "e2m1", "e2m1", 16, "bf16", "n")),
     5: ("mxfp8-ragged-L2-8000x1000x7168-mmajor",
         Problem(8000, 1000, 7168, 2, "e4m3", "e4m3", 32, "f32", "m")),
+    6: ("nvfp4-8192^3-sfv16-e4m3-scales-bf16",
+        Problem(8192, 8192, 8192, 1, "e2m1", "e2m1", 16, "bf16", "n", sf_dtype="e4m3")),
 }
+
+E4M3_ONE = 0x38  # the E4M3 byte of 1.0, the padding scale of E4M3 atoms
 
 
 # ---------------------------------------------------------------- encoding
@@ -166,6 +175,20 @@ def quantize_blocks(x: np.ndarray, dtype: str, sfv: int):
     return codes, sf
 
 
+def quantize_blocks_e4m3_scale(x: np.ndarray, sfv: int = 16):
+    """NVFP4-style: x (R, K) float32, K % sfv == 0 -> (packed E2M1 codes
+    (R, K/2), E4M3 scale bytes (R, K/sfv)) by the workload-6 recipe."""
+    R, K = x.shape
+    xb = x.reshape(R, K // sfv, sfv)
+    amax = np.max(np.abs(xb), axis=2)
+    sb = _encode_fp8(np.minimum(amax / np.float32(6.0), np.float32(448.0)), "e4m3")
+    sb = np.where(sb == 0, np.uint8(1), sb)
+    sb = np.where(amax > 0, sb, np.uint8(E4M3_ONE)).astype(np.uint8)
+    dec = torch.from_numpy(sb).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    y = np.clip(xb / dec[:, :, None], -6.0, 6.0).reshape(R, K)
+    return _pack_e2m1(_encode_e2m1(y)), sb
+
+
 def pack_scale_atoms(sf: np.ndarray, rows: int, K: int, sfv: int, pad: int = 127) -> np.ndarray:
     """Logical scales (L, rows, ceil(K/sfv)) -> physical (L, T, T_k, 32, 4, 4) bytes.
 
@@ -216,6 +239,12 @@ def quantized(p: Problem, seed: int, a_dist: str = "normal", b_dist: str = "norm
     """Real-valued draws quantised per sf_vec_size K-block (see module doc)."""
     if p.K % p.sfv:
         raise ValueError("quantised workloads need K % sf_vec_size == 0")
+    if p.sf_dtype == "e4m3":
+        if p.a_dtype != "e2m1" or p.b_dtype != "e2m1":
+            raise ValueError("E4M3 scales are for E2M1 operands")
+        enc = lambda x, dtype: quantize_blocks_e4m3_scale(x, p.sfv)
+    else:
+        enc = lambda x, dtype: quantize_blocks(x, dtype, p.sfv)
     rng = np.random.default_rng(seed)
     a_bytes = p.row_bytes(p.a_dtype)
     b_bytes = p.row_bytes(p.b_dtype)
@@ -232,19 +261,20 @@ def quantized(p: Problem, seed: int, a_dist: str = "normal", b_dist: str = "norm
             n_out = int(math.ceil(outlier_frac * p.M))
             rows = rng.choice(p.M, size=n_out, replace=False)
             x[rows] *= np.float32(outlier_scale)
-        A[l], sfa[l] = quantize_blocks(x, p.a_dtype, p.sfv)
+        A[l], sfa[l] = enc(x, p.a_dtype)
     for l in range(p.L):
         x = rng.standard_normal((p.N, p.K), dtype=np.float32)
         if b_sigma != 1.0:
             x *= np.float32(b_sigma)
-        B[l], sfb[l] = quantize_blocks(x, p.b_dtype, p.sfv)
-    SFA = pack_scale_atoms(sfa, p.M, p.K, p.sfv)
-    SFB = pack_scale_atoms(sfb, p.N, p.K, p.sfv)
+        B[l], sfb[l] = enc(x, p.b_dtype)
+    pad = E4M3_ONE if p.sf_dtype == "e4m3" else 127
+    SFA = pack_scale_atoms(sfa, p.M, p.K, p.sfv, pad)
+    SFB = pack_scale_atoms(sfb, p.N, p.K, p.sfv, pad)
     return Inputs(p, A, B, SFA, SFB)
 
 
 def workload(number: int, **shape) -> Inputs:
-    """Inputs of workload `number` (1..5).  Keyword overrides (M, N, K, L)
+    """Inputs of workload `number` (1..6).  Keyword overrides (M, N, K, L)
     keep the recipe and change the shape (parity cases at reduced size)."""
     name, p = WORKLOADS[number]
     if shape:
@@ -260,6 +290,8 @@ def workload(number: int, **shape) -> Inputs:
         inp = quantized(p, seed)
     elif number == 5:
         inp = quantized(p, seed, a_dist="uniform", b_sigma=0.02)
+    elif number == 6:
+        inp = quantized(p, seed)
     else:
         raise KeyError(number)
     inp.name = name if not shape else name + "@" + ",".join(f"{k}={v}" for k, v in shape.items())

@@ -15,7 +15,7 @@ POISON_BYTE = 0xA5
 
 def problem_of(p: synth.Problem, **hints) -> bsg.bsg_problem:
     return bsg.make_problem(p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv, p.c_dtype,
-                            p.c_major, **hints)
+                            p.c_major, sf_dtype=p.sf_dtype, **hints)
 
 
 def to_device(inp: synth.Inputs, dev="cuda:0"):
@@ -76,7 +76,7 @@ def assert_parity(inp: synth.Inputs, c_gpu: np.ndarray, amax_gpu: float, ref=Non
     p = inp.problem
     if ref is None:
         ref = oracle.reference(p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv, inp.A, inp.B,
-                               inp.SFA, inp.SFB, p.c_dtype)
+                               inp.SFA, inp.SFB, p.c_dtype, sf_dtype=p.sf_dtype)
     finite = np.isfinite(ref["c"])
     with np.errstate(invalid="ignore"):
         err = np.abs(c_gpu - ref["c"])

@@ -62,8 +62,8 @@ def dense_operand(codes, dtype, phys_sf, rows, K, sfv, sf_dtype="ue8m0"):
 
 def independent_gemm(inp):
     p = inp.problem
-    a = dense_operand(inp.A, p.a_dtype, inp.SFA, p.M, p.K, p.sfv)
-    b = dense_operand(inp.B, p.b_dtype, inp.SFB, p.N, p.K, p.sfv)
+    a = dense_operand(inp.A, p.a_dtype, inp.SFA, p.M, p.K, p.sfv, p.sf_dtype)
+    b = dense_operand(inp.B, p.b_dtype, inp.SFB, p.N, p.K, p.sfv, p.sf_dtype)
     return np.einsum("lmk,lnk->lmn", a, b), np.einsum("lmk,lnk->lmn", np.abs(a), np.abs(b))
 
 

@@ -97,6 +97,10 @@ OK_CASES = [
          c_dtype="e5m2", c_major="m"),
     dict(M=130, N=96, K=128, L=1, a_dtype="e2m1", b_dtype="e2m1", sf_vec_size=16,
          c_dtype="e2m1"),
+    dict(M=8192, N=8192, K=8192, L=1, a_dtype="e2m1", b_dtype="e2m1", sf_vec_size=16,
+         sf_dtype="e4m3", c_dtype="bf16"),
+    dict(M=130, N=96, K=160, L=2, a_dtype="e2m1", b_dtype="e2m1", sf_vec_size=16,
+         sf_dtype="e4m3", c_dtype="e2m1"),
 ]
 
 
@@ -116,7 +120,11 @@ BAD_CASES = [
     (dict(M=4, N=4, K=32, L=1, a_dtype="e2m1", b_dtype="e4m3"), bsg.BSG_ERR_UNSUPPORTED,
      "FP4 x FP8"),
     (dict(M=4, N=4, K=32, L=1, sf_dtype="e4m3"), bsg.BSG_ERR_UNSUPPORTED,
-     "E4M3 scales (NVFP4 style)"),
+     "E4M3 scales with FP8 operands"),
+    (dict(M=4, N=4, K=64, L=1, a_dtype="e2m1", b_dtype="e2m1", sf_vec_size=32,
+          sf_dtype="e4m3"), bsg.BSG_ERR_UNSUPPORTED, "E4M3 scales with sfv 32"),
+    (dict(M=4, N=4, K=32, L=1, a_dtype="e2m1", b_dtype="e2m1", sf_vec_size=16,
+          sf_dtype="e5m2"), bsg.BSG_ERR_INVALID_ARG, "E5M2 scales"),
     (dict(M=4, N=4, K=32, L=1, sf_dtype="f32"), bsg.BSG_ERR_INVALID_ARG, "scale dtype"),
     (dict(M=4, N=4, K=32, L=1, c_dtype="e4m3"), bsg.BSG_ERR_UNSUPPORTED, "FP8 in, FP8 out"),
     (dict(M=4, N=4, K=32, L=1, c_dtype="e2m1"), bsg.BSG_ERR_UNSUPPORTED, "FP4 C with FP8 in"),

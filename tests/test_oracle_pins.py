@@ -22,6 +22,7 @@ from helpers import (E2M1_VALUES, build_golden_inputs, dense_operand, golden_nam
 
 def run_oracle(inp, **kw):
     p = inp.problem
+    kw.setdefault("sf_dtype", p.sf_dtype)
     return oracle.gemm(p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv, inp.A, inp.B,
                        inp.SFA, inp.SFB, **kw)
 
@@ -233,6 +234,66 @@ def test_e2m1_exhaustive_pairs():
         vals = np.array(E2M1_VALUES + [-v for v in E2M1_VALUES])
         expect = np.outer(vals, vals) * 2.0 ** (sa - 127) * 2.0 ** (sb - 127)
         np.testing.assert_array_equal(C[0], expect)
+
+
+# ------------------------------------------------------ E4M3 (NVFP4) scales
+
+# A few E4M3 bytes with their values worked out by hand from the format
+# (bias 7, three mantissa bits, exponent field 0 subnormal with 2^-6 * m/8).
+E4M3_SCALE_BYTES = {0x38: 1.0, 0x3C: 1.5, 0x30: 0.5, 0x40: 2.0, 0x45: 3.25,
+                    0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x7E: 448.0}
+
+
+def test_e4m3_scale_exhaustive_pairs():
+    """Every E2M1 code against every E2M1 code under hand-decoded E4M3 scales
+    (sfv 16): C is the product of the two listed values and the two scales."""
+    codes = np.arange(16, dtype=np.uint8)
+    M = N = 16
+    K = 32
+    p = synth.Problem(M, N, K, 1, "e2m1", "e2m1", 16, "f32", "n", sf_dtype="e4m3")
+    A = np.zeros((1, M, K), dtype=np.uint8)
+    B = np.zeros((1, N, K), dtype=np.uint8)
+    A[0, :, 17] = codes  # element 17: the second K-block of each row
+    B[0, :, 17] = codes
+    pack = lambda x: (x[..., 0::2] | (x[..., 1::2] << 4)).astype(np.uint8)
+    vals = np.array(E2M1_VALUES + [-v for v in E2M1_VALUES])
+    for sa, sb in [(0x38, 0x38), (0x3C, 0x45), (0x01, 0x7E), (0x07, 0x08), (0x30, 0x40)]:
+        sfa = np.full((1, M, 2), 0x38, dtype=np.uint8)
+        sfb = np.full((1, N, 2), 0x38, dtype=np.uint8)
+        sfa[..., 1] = sa  # only the second block's scale matters
+        sfb[..., 1] = sb
+        inp = synth.Inputs(p, pack(A), pack(B),
+                           synth.pack_scale_atoms(sfa, M, K, 16, synth.E4M3_ONE),
+                           synth.pack_scale_atoms(sfb, N, K, 16, synth.E4M3_ONE))
+        C, S, _ = run_oracle(inp)
+        expect = np.outer(vals, vals) * E4M3_SCALE_BYTES[sa] * E4M3_SCALE_BYTES[sb]
+        np.testing.assert_array_equal(C[0], expect)
+        np.testing.assert_array_equal(S[0], np.abs(expect))
+
+
+@pytest.mark.parametrize("K", [16, 48, 160])
+@pytest.mark.parametrize("lo,hi", [(0x28, 0x50), (0x01, 0x0F), (0x60, 0x7E)])
+def test_e4m3_scale_brute_force_tiny(K, lo, hi):
+    """Random E4M3 scale bytes (normal, subnormal, near the top) with sfv 16
+    against the independent numpy path, whose scales are decoded by torch."""
+    rng = np.random.default_rng(K + lo)
+    for M, N, L in [(1, 1, 1), (3, 2, 2), (5, 7, 1)]:
+        p = synth.Problem(M, N, K, L, "e2m1", "e2m1", 16, "f32", "n", sf_dtype="e4m3")
+        inp = synth.uniform_codes(p, int(rng.integers(1 << 30)), lo, hi)
+        C, S, _ = run_oracle(inp)
+        Ci, Si = independent_gemm(inp)
+        assert np.all(np.abs(C - Ci) <= 1e-15 * np.maximum(Si, 1e-300)), (M, N, L)
+        np.testing.assert_allclose(S, Si, rtol=1e-15, atol=0)
+
+
+def test_e4m3_scale_differs_from_e8m0_reading():
+    """The same scale bytes read as E4M3 and as E8M0 give different C (a
+    scale-table mix-up would pass the E8M0 pins but fail here)."""
+    p8 = synth.Problem(4, 4, 32, 1, "e2m1", "e2m1", 16, "f32", "n")
+    inp = synth.uniform_codes(p8, 5, 0x38, 0x38)
+    C8, _, _ = run_oracle(inp)
+    C4, _, _ = run_oracle(inp, sf_dtype="e4m3")
+    np.testing.assert_array_equal(C4, C8 * 2.0 ** (2 * (127 - 0x38)))
 
 
 # -------------------------------------------------------------- closed form
