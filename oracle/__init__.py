@@ -111,8 +111,18 @@ def _ptr(a: np.ndarray):
     return ctypes.c_void_p(a.ctypes.data)
 
 
-def _dims(M, N, K, L):
-    return (ctypes.c_int64 * 4)(int(M), int(N), int(K), int(L))
+def _mn(major: str, mn_name: str) -> int:
+    """1 for an operand stored with its M (N) rows contiguous, 0 for k-major."""
+    if major == "k":
+        return 0
+    if major == mn_name:
+        return 1
+    raise ValueError("operand major must be 'k' or %r, got %r" % (mn_name, major))
+
+
+def _dims(M, N, K, L, a_major="k", b_major="k"):
+    return (ctypes.c_int64 * 6)(int(M), int(N), int(K), int(L), _mn(a_major, "m"),
+                                _mn(b_major, "n"))
 
 
 def num_threads(requested: int = 0) -> int:
@@ -147,16 +157,19 @@ def dequantize(codes: np.ndarray, dtype: str, sf: np.ndarray, sfv: int, rows: in
 
 
 def gemm(M, N, K, L, a_dtype, b_dtype, sfv, A, B, SFA, SFB, sf_dtype="ue8m0",
-         rows=None, nthreads=0, want_s=True):
+         rows=None, nthreads=0, want_s=True, a_major="k", b_major="k"):
     """C[l, m, n] = sum_k Ahat[m,k,l] Bhat[n,k,l] in double, and S = sum_k |Ahat Bhat|.
 
+    A is k-major bytes (L, M, K) (K/2 for E2M1) or, with ``a_major="m"``
+    (FP8 only), m-major bytes (L, K, M); B likewise with ``b_major="n"``.
     ``rows=(m0, m1)`` restricts to rows m0 <= m < m1 (every batch).
     Returns (C, S, threads_used); S is None when ``want_s`` is false."""
     A, B, SFA, SFB = _u8(A), _u8(B), _u8(SFA), _u8(SFB)
     m0, m1 = (0, M) if rows is None else rows
     C = np.empty((L, m1 - m0, N), dtype=np.float64)
     S = np.empty_like(C) if want_s else None
-    nt = _load().bsgo_gemm_rows(_dims(M, N, K, L), DTYPES[a_dtype], DTYPES[b_dtype],
+    nt = _load().bsgo_gemm_rows(_dims(M, N, K, L, a_major, b_major), DTYPES[a_dtype],
+                                DTYPES[b_dtype],
                                 DTYPES[sf_dtype], int(sfv), _ptr(A), _ptr(B), _ptr(SFA),
                                 _ptr(SFB), int(m0), int(m1), _ptr(C),
                                 _ptr(S) if S is not None else None, int(nthreads))
@@ -166,13 +179,14 @@ def gemm(M, N, K, L, a_dtype, b_dtype, sfv, A, B, SFA, SFB, sf_dtype="ue8m0",
 
 
 def gemm_sample(M, N, K, L, a_dtype, b_dtype, sfv, A, B, SFA, SFB, mnl, sf_dtype="ue8m0",
-                nthreads=0):
+                nthreads=0, a_major="k", b_major="k"):
     """The sums at points mnl (an (n, 3) int array of (m, n, l)).  Returns (C, S)."""
     A, B, SFA, SFB = _u8(A), _u8(B), _u8(SFA), _u8(SFB)
     mnl = np.ascontiguousarray(mnl, dtype=np.int64).reshape(-1, 3)
     C = np.empty(len(mnl), dtype=np.float64)
     S = np.empty(len(mnl), dtype=np.float64)
-    nt = _load().bsgo_gemm_sample(_dims(M, N, K, L), DTYPES[a_dtype], DTYPES[b_dtype],
+    nt = _load().bsgo_gemm_sample(_dims(M, N, K, L, a_major, b_major), DTYPES[a_dtype],
+                                  DTYPES[b_dtype],
                                   DTYPES[sf_dtype], int(sfv), _ptr(A), _ptr(B), _ptr(SFA),
                                   _ptr(SFB), mnl.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
                                   len(mnl), _ptr(C), _ptr(S), int(nthreads))
@@ -210,12 +224,12 @@ def tolerance(cref: np.ndarray, S: np.ndarray, c_dtype: str, rel: float = REL_TO
 
 
 def reference(M, N, K, L, a_dtype, b_dtype, sfv, A, B, SFA, SFB, c_dtype, sf_dtype="ue8m0",
-              nthreads=0):
+              nthreads=0, a_major="k", b_major="k"):
     """Everything a parity check needs for a whole problem, arrays shaped (L, M, N):
     ``c`` (C_ref rounded to c_dtype), ``exact`` (the double sum), ``s``, ``tau`` and
     ``amax`` (max |C_ref|)."""
     C, S, _ = gemm(M, N, K, L, a_dtype, b_dtype, sfv, A, B, SFA, SFB, sf_dtype=sf_dtype,
-                   nthreads=nthreads)
+                   nthreads=nthreads, a_major=a_major, b_major=b_major)
     cref = round_to(C, c_dtype)
     tau = tolerance(cref, S, c_dtype)
     return {"c": cref, "exact": C, "s": S, "tau": tau, "amax": float(np.max(np.abs(cref)))}

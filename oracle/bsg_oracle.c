@@ -21,8 +21,10 @@
  * tolerance are separate, explicit steps.
  *
  * Layouts (same page, "Parameters" / "Input/Output tensors"):
- *   A  (M, K, L), k-major: byte (l*M + m)*Kb + kb, Kb = K bytes (K/2 for FP4)
- *   B  (N, K, L), k-major, likewise.
+ *   A  (M, K, L), k-major, strides (K, 1, M*K): byte (l*M + m)*Kb + kb,
+ *      Kb = K bytes (K/2 for FP4); or m-major (FP8 only), strides
+ *      (1, M, M*K): byte (l*K + k)*M + m
+ *   B  (N, K, L), k-major or n-major, likewise.
  *   FP4 (E2M1) is packed two per byte ("Support surface", "Layouts and
  *   strides"); element 2i sits in the low nibble, 2i+1 in the high nibble
  *   (the float4_e2m1fn_x2 convention; the pages do not spell it out).
@@ -143,6 +145,7 @@ int64_t bsgo_sf_offset(int64_t mn, int64_t kb, int64_t l, int64_t t_mn, int64_t 
 
 typedef struct {
     int64_t M, N, K, L;
+    int a_mn, b_mn;               /* 1: the operand is m- (n-) major */
     int a_dtype, b_dtype, sf_dtype, sfv;
     const uint8_t *A, *B, *SFA, *SFB;
     double tab_a[256], tab_b[256], tab_sf[256];
@@ -150,10 +153,12 @@ typedef struct {
 
 static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-/* raw code of element (r, k) of batch l of an operand with `rows` rows */
-static unsigned code_at(const uint8_t *X, int dtype, int64_t rows, int64_t K,
+/* raw code of element (r, k) of batch l of an operand with `rows` rows,
+ * stored k-major (mn == 0) or with the rows contiguous (mn == 1, FP8 only) */
+static unsigned code_at(const uint8_t *X, int dtype, int mn, int64_t rows, int64_t K,
                         int64_t r, int64_t k, int64_t l)
 {
+    if (mn) return X[(l * K + k) * rows + r];
     if (dtype == BSGO_E2M1) {
         uint8_t byte = X[(l * rows + r) * (K / 2) + k / 2];
         return (k & 1) ? (unsigned)(byte >> 4) : (unsigned)(byte & 0xFu);
@@ -163,14 +168,14 @@ static unsigned code_at(const uint8_t *X, int dtype, int64_t rows, int64_t K,
 
 /* Dequantized row r of batch l: out[k] = dec(X[r,k,l]) * sf(SF, r, k/sfv, l) */
 static void dequant_row(const problem_t *p, const uint8_t *X, const uint8_t *SF,
-                        const double *tab, int dtype, int64_t rows, int64_t r,
+                        const double *tab, int dtype, int mn, int64_t rows, int64_t r,
                         int64_t l, double *out)
 {
     int64_t t_mn = ceil_div(rows, 128), t_k = ceil_div(p->K, 4 * (int64_t)p->sfv);
     int64_t k;
     for (k = 0; k < p->K; k++) {
         double scale = p->tab_sf[SF[bsgo_sf_offset(r, k / p->sfv, l, t_mn, t_k)]];
-        out[k] = tab[code_at(X, dtype, rows, p->K, r, k, l)] * scale;
+        out[k] = tab[code_at(X, dtype, mn, rows, p->K, r, k, l)] * scale;
     }
 }
 
@@ -180,10 +185,13 @@ static int setup(problem_t *p, const int64_t *dims, int a_dtype, int b_dtype,
 {
     memset(p, 0, sizeof(*p));
     p->M = dims[0]; p->N = dims[1]; p->K = dims[2]; p->L = dims[3];
+    p->a_mn = dims[4] != 0; p->b_mn = dims[5] != 0;
     p->a_dtype = a_dtype; p->b_dtype = b_dtype; p->sf_dtype = sf_dtype; p->sfv = sfv;
     p->A = A; p->B = B; p->SFA = SFA; p->SFB = SFB;
     if (p->M < 1 || p->N < 1 || p->K < 1 || p->L < 1 || sfv < 1) return -1;
     if ((a_dtype == BSGO_E2M1 || b_dtype == BSGO_E2M1) && (p->K % 2)) return -1;
+    /* packed FP4 is k-major only ("Support surface and constraints") */
+    if ((a_dtype == BSGO_E2M1 && p->a_mn) || (b_dtype == BSGO_E2M1 && p->b_mn)) return -1;
     if (bsgo_decode_table(a_dtype, p->tab_a) < 0) return -1;
     if (bsgo_decode_table(b_dtype, p->tab_b) < 0) return -1;
     /* the scales are UE8M0, or E4M3 read as a non-negative multiplier */
@@ -197,12 +205,12 @@ int bsgo_dequantize(const uint8_t *X, int dtype, const uint8_t *SF, int sf_dtype
                     int sfv, int64_t rows, int64_t K, int64_t L, double *out)
 {
     problem_t p;
-    int64_t dims[4] = {rows, rows, K, L};
+    int64_t dims[6] = {rows, rows, K, L, 0, 0};
     int64_t l, r;
     if (setup(&p, dims, dtype, dtype, sf_dtype, sfv, X, X, SF, SF) != 0) return -1;
     for (l = 0; l < L; l++)
         for (r = 0; r < rows; r++)
-            dequant_row(&p, X, SF, p.tab_a, dtype, rows, r, l, out + (l * rows + r) * K);
+            dequant_row(&p, X, SF, p.tab_a, dtype, 0, rows, r, l, out + (l * rows + r) * K);
     return 0;
 }
 
@@ -244,7 +252,7 @@ static void *rows_worker(void *arg)
     if (!ahat) return (void *)1;
     for (it = j->item_begin; it < j->item_end; it++) {
         int64_t l = it / rows, m = j->m_begin + it % rows, n, k;
-        dequant_row(p, p->A, p->SFA, p->tab_a, p->a_dtype, p->M, m, l, ahat);
+        dequant_row(p, p->A, p->SFA, p->tab_a, p->a_dtype, p->a_mn, p->M, m, l, ahat);
         for (n = 0; n < p->N; n++) {
             const double *bh = j->bhat + (l * p->N + n) * p->K;
             double acc = 0.0, sabs = 0.0;
@@ -264,7 +272,8 @@ static void *rows_worker(void *arg)
 /*
  * C[l][m - m_begin][n] = sum_k Ahat[m,k,l] * Bhat[n,k,l]   for m_begin <= m < m_end
  * S[l][m - m_begin][n] = sum_k |Ahat[m,k,l] * Bhat[n,k,l]| (S may be NULL)
- * dims = {M, N, K, L}.  Returns the number of threads used, or -1.
+ * dims = {M, N, K, L, a_mn, b_mn} (a_mn / b_mn: 1 for an m- / n-major
+ * operand, 0 for k-major).  Returns the number of threads used, or -1.
  */
 int bsgo_gemm_rows(const int64_t *dims, int a_dtype, int b_dtype, int sf_dtype, int sfv,
                    const uint8_t *A, const uint8_t *B, const uint8_t *SFA,
@@ -283,7 +292,7 @@ int bsgo_gemm_rows(const int64_t *dims, int a_dtype, int b_dtype, int sf_dtype, 
     if (!bhat) return -1;
     for (l = 0; l < p.L; l++)
         for (n = 0; n < p.N; n++)
-            dequant_row(&p, p.B, p.SFB, p.tab_b, p.b_dtype, p.N, n, l,
+            dequant_row(&p, p.B, p.SFB, p.tab_b, p.b_dtype, p.b_mn, p.N, n, l,
                         bhat + (l * p.N + n) * p.K);
     items = p.L * (m_end - m_begin);
     nt = bsgo_num_threads(nthreads);
@@ -343,8 +352,8 @@ static void *sample_worker(void *arg)
     for (i = j->begin; i < j->end; i++) {
         int64_t m = j->mnl[3 * i], n = j->mnl[3 * i + 1], l = j->mnl[3 * i + 2];
         double acc = 0.0, sabs = 0.0;
-        dequant_row(p, p->A, p->SFA, p->tab_a, p->a_dtype, p->M, m, l, ah);
-        dequant_row(p, p->B, p->SFB, p->tab_b, p->b_dtype, p->N, n, l, bh);
+        dequant_row(p, p->A, p->SFA, p->tab_a, p->a_dtype, p->a_mn, p->M, m, l, ah);
+        dequant_row(p, p->B, p->SFB, p->tab_b, p->b_dtype, p->b_mn, p->N, n, l, bh);
         for (k = 0; k < p->K; k++) {
             double prod = ah[k] * bh[k];
             acc += prod;

@@ -35,6 +35,8 @@ Workloads (seed = 1000 + workload number):
    byte = the block amax / 6 rounded to E4M3 (nearest, ties to even; at least
    the smallest subnormal, 1.0 for an all-zero block), each element divided
    by the decoded scale, saturated to +-6 and rounded to E2M1; C bf16 n-major.
+7. MXFP8 4096^3 with MN-major operands: workload 2's recipe, A stored m-major
+   (strides (1, M, M*K)) and B n-major.
 
 The exponent offset of a block scale is the element format's largest
 exponent (E4M3 8, E5M2 15, E2M1 2); the scaled block is saturated to the
@@ -70,6 +72,8 @@ class Problem:
     c_dtype: str = "f32"
     c_major: str = "n"
     sf_dtype: str = "ue8m0"
+    a_major: str = "k"   # "k": A bytes (L, M, K); "m" (FP8 only): (L, K, M)
+    b_major: str = "k"   # "k": B bytes (L, N, K); "n" (FP8 only): (L, K, N)
 
     @property
     def t_m(self) -> int:
@@ -93,7 +97,8 @@ class Problem:
     def describe(self) -> str:
         ab = self.a_dtype if self.a_dtype == self.b_dtype else f"{self.a_dtype}x{self.b_dtype}"
         return (f"{ab} M={self.M} N={self.N} K={self.K} L={self.L} sfv={self.sfv} "
-                f"C={self.c_dtype} {self.c_major}-major")
+                f"A {self.a_major}-major B {self.b_major}-major C={self.c_dtype} "
+                f"{self.c_major}-major")
 
 
 @dataclasses.dataclass
@@ -119,6 +124,8 @@ WORKLOADS = {
         Problem(8000, 1000, 7168, 2, "e4m3", "e4m3", 32, "f32", "m")),
     6: ("nvfp4-8192^3-sfv16-e4m3-scales-bf16",
         Problem(8192, 8192, 8192, 1, "e2m1", "e2m1", 16, "bf16", "n", sf_dtype="e4m3")),
+    7: ("mxfp8-4096^3-a-mmajor-b-nmajor-bf16",
+        Problem(4096, 4096, 4096, 1, "e4m3", "e4m3", 32, "bf16", "n", a_major="m", b_major="n")),
 }
 
 E4M3_ONE = 0x38  # the E4M3 byte of 1.0, the padding scale of E4M3 atoms
@@ -212,6 +219,15 @@ def scale_shape(rows: int, K: int, sfv: int, L: int):
 _FINITE_E4M3 = np.array([b for b in range(256) if b not in (0x7F, 0xFF)], dtype=np.uint8)
 
 
+def to_major(codes: np.ndarray, major: str) -> np.ndarray:
+    """k-major operand bytes (L, rows, K) in the stored layout: unchanged for
+    "k", (L, K, rows) with the rows contiguous for "m" / "n" ("Parameters":
+    strides (1, M, M*K))."""
+    if major == "k":
+        return codes
+    return np.ascontiguousarray(codes.transpose(0, 2, 1))
+
+
 def uniform_codes(p: Problem, seed: int, sf_lo: int = 124, sf_hi: int = 130) -> Inputs:
     """Codes uniform over the finite codes of each format; every scale byte
     (padding included) uniform in [sf_lo, sf_hi]."""
@@ -230,7 +246,7 @@ def uniform_codes(p: Problem, seed: int, sf_lo: int = 124, sf_hi: int = 130) -> 
     B = codes(p.N, p.b_dtype)
     SFA = rng.integers(sf_lo, sf_hi + 1, size=scale_shape(p.M, p.K, p.sfv, p.L)).astype(np.uint8)
     SFB = rng.integers(sf_lo, sf_hi + 1, size=scale_shape(p.N, p.K, p.sfv, p.L)).astype(np.uint8)
-    return Inputs(p, A, B, SFA, SFB)
+    return Inputs(p, to_major(A, p.a_major), to_major(B, p.b_major), SFA, SFB)
 
 
 def quantized(p: Problem, seed: int, a_dist: str = "normal", b_dist: str = "normal",
@@ -270,11 +286,11 @@ def quantized(p: Problem, seed: int, a_dist: str = "normal", b_dist: str = "norm
     pad = E4M3_ONE if p.sf_dtype == "e4m3" else 127
     SFA = pack_scale_atoms(sfa, p.M, p.K, p.sfv, pad)
     SFB = pack_scale_atoms(sfb, p.N, p.K, p.sfv, pad)
-    return Inputs(p, A, B, SFA, SFB)
+    return Inputs(p, to_major(A, p.a_major), to_major(B, p.b_major), SFA, SFB)
 
 
 def workload(number: int, **shape) -> Inputs:
-    """Inputs of workload `number` (1..6).  Keyword overrides (M, N, K, L)
+    """Inputs of workload `number` (1..7).  Keyword overrides (M, N, K, L)
     keep the recipe and change the shape (parity cases at reduced size)."""
     name, p = WORKLOADS[number]
     if shape:
@@ -290,7 +306,7 @@ def workload(number: int, **shape) -> Inputs:
         inp = quantized(p, seed)
     elif number == 5:
         inp = quantized(p, seed, a_dist="uniform", b_sigma=0.02)
-    elif number == 6:
+    elif number in (6, 7):
         inp = quantized(p, seed)
     else:
         raise KeyError(number)

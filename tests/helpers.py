@@ -50,8 +50,11 @@ def logical_scales(phys: np.ndarray, rows: int, kblocks: int) -> np.ndarray:
     return np.ascontiguousarray(out.transpose(2, 0, 1))
 
 
-def dense_operand(codes, dtype, phys_sf, rows, K, sfv, sf_dtype="ue8m0"):
-    """Dequantized operand (L, rows, K) in float64, computed independently of the oracle."""
+def dense_operand(codes, dtype, phys_sf, rows, K, sfv, sf_dtype="ue8m0", major="k"):
+    """Dequantized operand (L, rows, K) in float64, computed independently of the oracle.
+    `codes` is k-major (L, rows, K) or, for major "m" / "n", (L, K, rows)."""
+    if major != "k":
+        codes = codes.reshape(-1, K, rows).transpose(0, 2, 1)
     if dtype == "e2m1":
         codes = unpack_e2m1(codes)
     vals = lib_decode(codes, dtype)
@@ -62,8 +65,8 @@ def dense_operand(codes, dtype, phys_sf, rows, K, sfv, sf_dtype="ue8m0"):
 
 def independent_gemm(inp):
     p = inp.problem
-    a = dense_operand(inp.A, p.a_dtype, inp.SFA, p.M, p.K, p.sfv, p.sf_dtype)
-    b = dense_operand(inp.B, p.b_dtype, inp.SFB, p.N, p.K, p.sfv, p.sf_dtype)
+    a = dense_operand(inp.A, p.a_dtype, inp.SFA, p.M, p.K, p.sfv, p.sf_dtype, p.a_major)
+    b = dense_operand(inp.B, p.b_dtype, inp.SFB, p.N, p.K, p.sfv, p.sf_dtype, p.b_major)
     return np.einsum("lmk,lnk->lmn", a, b), np.einsum("lmk,lnk->lmn", np.abs(a), np.abs(b))
 
 
@@ -83,7 +86,8 @@ def build_golden_inputs(g):
     import synth
     pr = g["problem"]
     p = synth.Problem(pr["M"], pr["N"], pr["K"], pr["L"], pr["a_dtype"], pr["b_dtype"],
-                      pr["sfv"], pr.get("c_dtype", "f32"), pr.get("c_major", "n"))
+                      pr["sfv"], pr.get("c_dtype", "f32"), pr.get("c_major", "n"),
+                      a_major=pr.get("a_major", "k"), b_major=pr.get("b_major", "k"))
 
     def operand(rows, dtype, fills):
         codes = np.zeros((p.L, rows, p.K), dtype=np.uint8)
@@ -100,6 +104,7 @@ def build_golden_inputs(g):
             sf[l, mn, kb] = byte
         return synth.pack_scale_atoms(sf, rows, p.K, p.sfv)
 
-    return synth.Inputs(p, operand(p.M, p.a_dtype, g["A_fill"]),
-                        operand(p.N, p.b_dtype, g["B_fill"]),
-                        scales(p.M, g["SFA_set"]), scales(p.N, g["SFB_set"]))
+    # a fixture may give an operand as its stored bytes, in memory order
+    A = np.array(g["A_flat"], dtype=np.uint8) if "A_flat" in g else operand(p.M, p.a_dtype, g["A_fill"])
+    B = np.array(g["B_flat"], dtype=np.uint8) if "B_flat" in g else operand(p.N, p.b_dtype, g["B_fill"])
+    return synth.Inputs(p, A, B, scales(p.M, g["SFA_set"]), scales(p.N, g["SFB_set"]))

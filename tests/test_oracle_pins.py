@@ -23,6 +23,8 @@ from helpers import (E2M1_VALUES, build_golden_inputs, dense_operand, golden_nam
 def run_oracle(inp, **kw):
     p = inp.problem
     kw.setdefault("sf_dtype", p.sf_dtype)
+    kw.setdefault("a_major", p.a_major)
+    kw.setdefault("b_major", p.b_major)
     return oracle.gemm(p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv, inp.A, inp.B,
                        inp.SFA, inp.SFB, **kw)
 
@@ -107,7 +109,7 @@ def test_golden_example(name):
     inp = build_golden_inputs(g)
     p = inp.problem
     ref = oracle.reference(p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv, inp.A, inp.B,
-                           inp.SFA, inp.SFB, p.c_dtype)
+                           inp.SFA, inp.SFB, p.c_dtype, a_major=p.a_major, b_major=p.b_major)
     for m, n, l, v in g["expect_C"]:
         assert ref["exact"][l, m, n] == v, (m, n, l)
         assert ref["c"][l, m, n] == v
@@ -294,6 +296,48 @@ def test_e4m3_scale_differs_from_e8m0_reading():
     C8, _, _ = run_oracle(inp)
     C4, _, _ = run_oracle(inp, sf_dtype="e4m3")
     np.testing.assert_array_equal(C4, C8 * 2.0 ** (2 * (127 - 0x38)))
+
+
+# ------------------------------------------------------- MN-major operands
+
+@pytest.mark.parametrize("am,bm", [("m", "k"), ("k", "n"), ("m", "n")])
+@pytest.mark.parametrize("a,b", [("e4m3", "e4m3"), ("e5m2", "e4m3")])
+def test_mn_major_brute_force(am, bm, a, b):
+    """m-major A / n-major B ("Parameters": strides (1, M, M*K)) against the
+    independent numpy path, which transposes the stored bytes itself."""
+    rng = np.random.default_rng(len(am + bm + a + b))
+    for M, N, K, L in [(1, 1, 32, 1), (3, 2, 64, 2), (5, 7, 96, 1), (16, 32, 40, 2)]:
+        p = synth.Problem(M, N, K, L, a, b, 32, "f32", "n", a_major=am, b_major=bm)
+        inp = synth.uniform_codes(p, int(rng.integers(1 << 30)), 120, 134)
+        assert inp.A.shape == ((L, K, M) if am == "m" else (L, M, K))
+        C, S, _ = run_oracle(inp)
+        Ci, Si = independent_gemm(inp)
+        assert np.all(np.abs(C - Ci) <= 1e-15 * np.maximum(Si, 1e-300)), (M, N, K, L)
+        np.testing.assert_allclose(S, Si, rtol=1e-15, atol=0)
+
+
+def test_mn_major_is_a_relayout_only():
+    """The same logical operands stored k-major and MN-major give the same C
+    bit for bit (the oracle sums in the same order either way)."""
+    p = synth.Problem(24, 40, 160, 2, "e4m3", "e5m2", 32, "f32", "n")
+    inp = synth.uniform_codes(p, 77, 118, 136)
+    C0, S0, _ = run_oracle(inp)
+    q = synth.Problem(24, 40, 160, 2, "e4m3", "e5m2", 32, "f32", "n", a_major="m", b_major="n")
+    inq = synth.Inputs(q, np.ascontiguousarray(inp.A.transpose(0, 2, 1)),
+                       np.ascontiguousarray(inp.B.transpose(0, 2, 1)), inp.SFA, inp.SFB)
+    C1, S1, _ = run_oracle(inq)
+    np.testing.assert_array_equal(C0, C1)
+    np.testing.assert_array_equal(S0, S1)
+    # and reading MN-major bytes as k-major gives something else
+    C2, _, _ = run_oracle(inq, a_major="k", b_major="k")
+    assert not np.array_equal(C0, C2)
+
+
+def test_mn_major_fp4_rejected():
+    p = synth.Problem(4, 4, 32, 1, "e2m1", "e2m1", 16, "f32", "n")
+    inp = synth.uniform_codes(p, 1)
+    with pytest.raises(ValueError):
+        run_oracle(inp, a_major="m")
 
 
 # -------------------------------------------------------------- closed form
