@@ -119,6 +119,7 @@ def peaks():
 def config_of(number: int, p: synth.Problem, name: str) -> dict:
     return {"workload": name, "M": p.M, "N": p.N, "K": p.K, "L": p.L, "a_dtype": p.a_dtype,
             "b_dtype": p.b_dtype, "sf_vec_size": p.sfv, "sf_dtype": p.sf_dtype,
+            "a_major": p.a_major, "b_major": p.b_major,
             "c_dtype": p.c_dtype, "c_major": p.c_major, "seed": 1000 + number,
             "l2": L2_NOTE}
 
@@ -135,13 +136,14 @@ def oracle_sample(inp, target_s: float, max_rows: int | None = None):
     # calibrate on enough rows to keep every oracle thread busy (the oracle
     # splits rows over threads), then size the sample; one more resize if the
     # sample ran well short of the target
-    _, _, threads = oracle.gemm(*args, rows=(0, min(p.M, 2)), want_s=False)
+    kw = {"a_major": p.a_major, "b_major": p.b_major}
+    _, _, threads = oracle.gemm(*args, rows=(0, min(p.M, 2)), want_s=False, **kw)
     rows = min(p.M, 4 * max(1, threads))
     if max_rows:
         rows = min(rows, max_rows)
     for attempt in range(3):
         t0 = time.perf_counter()
-        _, _, threads = oracle.gemm(*args, rows=(0, rows), want_s=False)
+        _, _, threads = oracle.gemm(*args, rows=(0, rows), want_s=False, **kw)
         t = time.perf_counter() - t0
         want = int(max(2, min(p.M, (target_s / max(t, 1e-3)) * rows)))
         if max_rows:
@@ -227,7 +229,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     inp = synth.workload(args.workload)
     nums = workload_numbers(p)
     op = bsg.GemmAmax(bsg.make_problem(p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv,
-                                       p.c_dtype, p.c_major, sf_dtype=p.sf_dtype),
+                                       p.c_dtype, p.c_major, sf_dtype=p.sf_dtype,
+                                       a_major=p.a_major, b_major=p.b_major),
                       device=local_rank)
     info = op.describe()
     hA, hB, hSFA, hSFB = [torch.from_numpy(np.ascontiguousarray(x)) for x in
@@ -500,12 +503,13 @@ def run_reference(args):
     import oracle
     pargs = (p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv, inp.A, inp.B, inp.SFA, inp.SFB,
              p.sf_dtype)
+    kw = {"a_major": p.a_major, "b_major": p.b_major}
     for _ in range(args.warmup):
-        oracle.gemm(*pargs, rows=(0, rows), want_s=False)
+        oracle.gemm(*pargs, rows=(0, rows), want_s=False, **kw)
     t0 = time.perf_counter()
     threads = 0
     for _ in range(args.steps):
-        _, _, threads = oracle.gemm(*pargs, rows=(0, rows), want_s=False)
+        _, _, threads = oracle.gemm(*pargs, rows=(0, rows), want_s=False, **kw)
     t = time.perf_counter() - t0
     flops = 2.0 * rows * p.N * p.K * p.L
     value = flops * args.steps / t / 1e12

@@ -78,6 +78,7 @@ struct Params {
   int stages;
   int c_dtype;            // bsg_dtype
   int c_major;            // 0 = n-major, 1 = m-major
+  int a_mn, b_mn;         // 1: A m-major / B n-major (FP8), tiles stored MN-contiguous
   uint32_t idesc;         // instruction descriptor, scale ids zero
   uint32_t smem_a, smem_b, smem_sfa, smem_sfb, smem_epi, smem_bar;  // offsets in dynamic smem
   const uint8_t* sfa;
@@ -310,10 +311,16 @@ __device__ __forceinline__ void tc_wait_st() {
 
 // Shared-memory matrix descriptor, K-major operand tile with 128-byte
 // swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+// K-major tiles: rows of 128 K bytes, 8-row groups 1024 bytes apart (the
+// stride byte offset); the leading byte offset is unused.  MN-major tiles:
+// rows of 128 MN bytes, one row per K, 8-row (8-K) groups 1024 bytes apart;
+// each operand's MN extent per CTA is one 128-byte swizzle span, so the
+// leading offset (the step to the next MN span) is never taken -- it is set
+// to the same 1024 bytes.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo_bytes = 16) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
-  d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (unused here)
+  d |= static_cast<uint64_t>(lbo_bytes >> 4) << 16;     // leading byte offset
   d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset
   d |= static_cast<uint64_t>(1) << 46;                  // descriptor version
   d |= static_cast<uint64_t>(2) << 61;                  // 128-byte swizzle
@@ -641,6 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t a_dst0 = base + p.smem_a, b_dst0 = base + p.smem_b;
       const uint32_t sfa_dst0 = base + p.smem_sfa, sfb_dst0 = base + p.smem_sfb;
       const uint32_t bar_base = scales ? sff0 : full0;
+      const bool a_mn = KIND == kKindF8F6F4 && p.a_mn, b_mn = KIND == kKindF8F6F4 && p.b_mn;
       for (int u = unit0; u < p.num_units && ok; u += unit_step) {
         const Tile tc = tile_coords(p, u, CM, crank);
         const int m0 = tc.mt * kTileM, n0 = tc.nt * TILE_N;
@@ -664,10 +672,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int sl = 0; sl < KSL; ++sl) {
               const int kx = ks * kSB + sl * kStageKBytes;
-              tma_load_3d_to_leader(a_dst0 + stage * kAStage + sl * kASlice, &tmap_a, kx, m0, tc.l,
-                                    lbar);
-              tma_load_3d_to_leader(b_dst0 + stage * kBStage + sl * kBSlice, &tmap_b, kx,
-                                    n0 + kBRows, tc.l, lbar);
+              const int nb = n0 + kBRows;
+              // a k-major box is (K bytes, rows); an MN-major one (MN, K rows)
+              tma_load_3d_to_leader(a_dst0 + stage * kAStage + sl * kASlice, &tmap_a,
+                                    a_mn ? m0 : kx, a_mn ? kx : m0, tc.l, lbar);
+              tma_load_3d_to_leader(b_dst0 + stage * kBStage + sl * kBSlice, &tmap_b,
+                                    b_mn ? nb : kx, b_mn ? kx : nb, tc.l, lbar);
             }
           } else {
             // a pair's leader expects the bytes of both CTAs
@@ -675,11 +685,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int sl = 0; sl < KSL; ++sl) {
               const int kx = ks * kSB + sl * kStageKBytes;
-              tma_load_3d(a_dst0 + stage * kAStage + sl * kASlice, &tmap_a, kx, m0, tc.l, bar);
+              tma_load_3d(a_dst0 + stage * kAStage + sl * kASlice, &tmap_a, a_mn ? m0 : kx,
+                          a_mn ? kx : m0, tc.l, bar);
               const uint32_t bdst = b_dst0 + stage * kBStage + sl * kBSlice;
               if (CM == 1 || PAIR)
-                tma_load_3d(bdst, &tmap_b, kx, n0, tc.l, bar);
-              else
+                tma_load_3d(bdst, &tmap_b, b_mn ? n0 : kx, b_mn ? kx : n0, tc.l, bar);
+              else  // k-major B only (the host rejects MN-major B here)
                 tma_load_3d_mc(bdst + crank * kBPart, &tmap_b, kx, n0 + crank * kBPartRows, tc.l,
                                bar, kMask);
             }
@@ -712,8 +723,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       // descriptors of stage 0; a stage or MMA step adds a constant to the
       // 16-byte-granular start address in the low bits
-      const uint64_t adesc0 = desc_sw128(base + p.smem_a);
-      const uint64_t bdesc0 = desc_sw128(base + p.smem_b);
+      const bool a_mn = KIND == kKindF8F6F4 && p.a_mn, b_mn = KIND == kKindF8F6F4 && p.b_mn;
+      const uint64_t adesc0 = desc_sw128(base + p.smem_a, a_mn ? 1024u : 16u);
+      const uint64_t bdesc0 = desc_sw128(base + p.smem_b, b_mn ? 1024u : 16u);
+      // start-address step (16-byte units) of one MMA's K: 32 bytes along a
+      // k-major row, or 32 rows of 128 bytes in an MN-major tile
+      const uint32_t a_kstep = a_mn ? (kMmaKBytes * 128) >> 4 : kMmaKBytes >> 4;
+      const uint32_t b_kstep = b_mn ? (kMmaKBytes * 128) >> 4 : kMmaKBytes >> 4;
       const uint32_t sf_t0 = tmem + kSfCol0;
       const uint32_t idesc = p.idesc;
       auto mma_issue = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t sa,
@@ -743,8 +759,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int c = j / KT::kMmasPerChunk;
               const uint32_t sf_id = static_cast<uint32_t>((j % KT::kMmasPerChunk) * KT::kSfIdStep);
               const int sl = j / kMmasPerSlice, jj = j % kMmasPerSlice;
-              mma_issue(d_tmem, ad + ((sl * kASlice + jj * kMmaKBytes) >> 4),
-                        bd + ((sl * kBSlice + jj * kMmaKBytes) >> 4),
+              mma_issue(d_tmem, ad + ((sl * kASlice) >> 4) + jj * a_kstep,
+                        bd + ((sl * kBSlice) >> 4) + jj * b_kstep,
                         idesc | (sf_id << 29) | (sf_id << 4), sfa_t + 4 * c, sfb_t + 4 * G * c,
                         (j != 0 || ks != 0) ? 1u : 0u);
             }
@@ -1268,11 +1284,12 @@ bsg_status bsg_problem_check(const bsg_problem* p) {
   if (!a4 && p->sf_vec_size == 16) return BSG_ERR_UNSUPPORTED;  // FP8 needs sfv 32
   // E4M3 scales ("Dtypes"): only the NVFP4 form, FP4 operands with sfv 16
   if (p->sf_dtype == BSG_E4M3 && (!a4 || p->sf_vec_size != 16)) return BSG_ERR_UNSUPPORTED;
-  const char majors[2] = {p->a_major, p->b_major};
-  for (char mj : majors) {
-    if (mj == 'm' || mj == 'n') return BSG_ERR_UNSUPPORTED;  // MN-major operands
-    if (mj != 'k') return BSG_ERR_INVALID_ARG;
-  }
+  // operand majors ("Parameters": A k- or m-major, B k- or n-major; packed
+  // FP4 k-major only)
+  if (p->a_major != 'k' && p->a_major != 'm') return BSG_ERR_INVALID_ARG;
+  if (p->b_major != 'k' && p->b_major != 'n') return BSG_ERR_INVALID_ARG;
+  const bool a_mn = p->a_major == 'm', b_mn = p->b_major == 'n';
+  if ((a_mn || b_mn) && a4) return BSG_ERR_UNSUPPORTED;
   if (p->c_major != 'n' && p->c_major != 'm') return BSG_ERR_INVALID_ARG;
   if (p->c_dtype == BSG_E2M1 && p->c_major != 'n') return BSG_ERR_UNSUPPORTED;
   if (p->tile_m != 0 && p->tile_m != 128) return BSG_ERR_INVALID_ARG;
@@ -1281,9 +1298,16 @@ bsg_status bsg_problem_check(const bsg_problem* p) {
   const int cl[2] = {p->cluster_m, p->cluster_n};
   for (int c : cl)
     if (c != 0 && c != 1 && c != 2 && c != 4) return BSG_ERR_INVALID_ARG;
+  // an n-major B tile is loaded whole by one CTA (single 128-wide tiles) or
+  // in halves by a CTA pair; B split over a cluster of four, or 256 columns
+  // in one CTA, are k-major only
+  if (b_mn && (p->cluster_m == 4 || (p->cluster_m == 1 && p->tile_n > 128)))
+    return BSG_ERR_UNSUPPORTED;
   const int64_t row_bytes = a4 ? p->K / 2 : p->K;
   if (a4 && (p->K % 2)) return BSG_ERR_ALIGNMENT;
-  if (row_bytes % 16) return BSG_ERR_ALIGNMENT;
+  // the contiguous extent of each operand: K bytes, or M (N) bytes per K
+  if ((!a_mn || !b_mn) && (row_bytes % 16)) return BSG_ERR_ALIGNMENT;
+  if ((a_mn && p->M % 16) || (b_mn && p->N % 16)) return BSG_ERR_ALIGNMENT;
   const int64_t c_n = p->c_major == 'n' ? p->N : p->M;
   if (p->c_dtype == BSG_E2M1 && (c_n % 2)) return BSG_ERR_ALIGNMENT;
   if (c_extent_bytes(c_n, p->c_dtype) % 16) return BSG_ERR_ALIGNMENT;
@@ -1358,7 +1382,7 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
       if (estimate(224, true) < estimate(256, false)) k.tile_n = 224;
     }
   }
-  const int num_acc = k.tile_n == 256 ? 1 : 2;
+  int num_acc = k.tile_n == 256 ? 1 : 2;
   // 224- and 256-wide tiles run as cta_group::2 pairs by default (hint 1:
   // single CTAs, 4: clusters of four multicasting the B tile; 224 is pairs
   // only); the 128-wide variant runs alone
@@ -1366,6 +1390,14 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   if (k.tile_n == 256) cm = prob->cluster_m == 0 ? 2 : prob->cluster_m;
   if (k.tile_n == 224) cm = 2;
   if (cm > k.tiles_m) cm = k.tiles_m >= 2 ? 2 : 1;
+  const bool b_mn = prob->b_major == 'n';
+  if (b_mn && cm == 1 && k.tile_n > 128) {
+    // a single CTA holds at most one 128-column MN-major B tile
+    if (prob->tile_n != 0) { delete plan; return BSG_ERR_UNSUPPORTED; }
+    k.tile_n = 128;
+    num_acc = 2;
+  }
+  if (b_mn && cm > 2) { delete plan; return BSG_ERR_UNSUPPORTED; }
   // FP8 pairs with 256-wide tiles take 256-byte K stages (8 MMAs per
   // barrier check); each CTA's half tiles keep three such stages in smem
   const int ksl = kind == kKindF8F6F4 && k.tile_n == 256 && cm == 2 ? 2 : 1;
@@ -1394,7 +1426,11 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
     b_fmt = prob->b_dtype == BSG_E5M2 ? 1 : 0;
   }
   const int mma_m = plan->pair ? 2 * kTileM : kTileM;
-  k.idesc = (a_fmt << 7) | (b_fmt << 10) | (static_cast<uint32_t>(k.tile_n >> 3) << 17) |
+  k.a_mn = prob->a_major == 'm' ? 1 : 0;
+  k.b_mn = b_mn ? 1 : 0;
+  // bits 15 / 16: A / B transposed, i.e. MN-major in shared memory
+  k.idesc = (a_fmt << 7) | (b_fmt << 10) | (static_cast<uint32_t>(k.a_mn) << 15) |
+            (static_cast<uint32_t>(k.b_mn) << 16) | (static_cast<uint32_t>(k.tile_n >> 3) << 17) |
             (prob->sf_dtype == BSG_UE8M0 ? 1u << 23 : 0u) /* scale type: 1 UE8M0, 0 UE4M3 */ |
             (static_cast<uint32_t>(mma_m >> 4) << 24);
   k.c_dtype = prob->c_dtype;
@@ -1494,13 +1530,19 @@ bsg_status bsg_workspace_init(const bsg_plan* plan, void* ws, size_t ws_bytes, v
   return BSG_OK;
 }
 
-static bool encode_operand(CUtensorMap* map, const void* ptr, int64_t row_bytes, int64_t rows,
-                           int64_t L, int box_rows) {
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows),
+// An operand of `rows` rows and `k_bytes` bytes of K per row, batch
+// outermost.  k-major: dims (K bytes, rows, L), box (one 128-byte K slice,
+// box_rows rows).  MN-major (FP8; mn): dims (rows, K, L), box (box_rows
+// MN bytes, one 128-row K slice) -- either way a 128-byte-swizzled box.
+static bool encode_operand(CUtensorMap* map, const void* ptr, int64_t k_bytes, int64_t rows,
+                           int64_t L, int box_rows, bool mn) {
+  const int64_t inner = mn ? rows : k_bytes, outer = mn ? k_bytes : rows;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer),
                         static_cast<cuuint64_t>(L)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes),
-                           static_cast<cuuint64_t>(row_bytes * rows)};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(kStageKBytes), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner),
+                           static_cast<cuuint64_t>(inner * outer)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(mn ? box_rows : kStageKBytes),
+                       static_cast<cuuint32_t>(mn ? kStageKBytes : box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = get_encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr),
                                      dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1552,7 +1594,7 @@ bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const vo
   {
     std::lock_guard<std::mutex> lock(plan->mu);
     if (plan->map_a_ptr != A) {
-      if (!encode_operand(&plan->map_a, A, row_bytes, pr.M, pr.L, kTileM)) {
+      if (!encode_operand(&plan->map_a, A, row_bytes, pr.M, pr.L, kTileM, k.a_mn != 0)) {
         plan->map_a_ptr = nullptr;
         return BSG_ERR_CUDA;
       }
@@ -1560,7 +1602,7 @@ bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const vo
     }
     if (plan->map_b_ptr != B) {
       const int b_box = plan->pair ? (k.tile_n / 2 + 127) / 128 * 128 : k.tile_n / plan->cluster_m;
-      if (!encode_operand(&plan->map_b, B, row_bytes, pr.N, pr.L, b_box)) {
+      if (!encode_operand(&plan->map_b, B, row_bytes, pr.N, pr.L, b_box, k.b_mn != 0)) {
         plan->map_b_ptr = nullptr;
         return BSG_ERR_CUDA;
       }

@@ -270,6 +270,11 @@ const void* kernel_of() {
   return reinterpret_cast<const void*>(&bsq_quantize_kernel<IN_BF16, OUT, SFV>);
 }
 
+// variant index for the per-device occupancy cache: [in_bf16][E4M3, E5M2, E2M1/16, E2M1/32]
+int variant_of(int in_bf16, int out, int sfv) {
+  return in_bf16 * 4 + (out == kOutE2M1 ? (sfv == 16 ? 2 : 3) : out);
+}
+
 const void* pick_kernel(int in_bf16, int out, int sfv) {
   if (out == kOutE4M3) return in_bf16 ? kernel_of<1, kOutE4M3, 32>() : kernel_of<0, kOutE4M3, 32>();
   if (out == kOutE5M2) return in_bf16 ? kernel_of<1, kOutE5M2, 32>() : kernel_of<0, kOutE5M2, 32>();
@@ -283,6 +288,7 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
 int g_dev_sms[kMaxDevices] = {};   // 0: not queried yet; -1: not an sm_103 device
+int g_dev_occ[kMaxDevices][8] = {};  // resident CTAs per SM of each variant; 0: not queried
 
 }  // namespace
 
@@ -370,8 +376,23 @@ bsg_status bsg_quantize(const bsg_quant_problem* q, const void* X, void* codes, 
   p.t_k = static_cast<uint32_t>(cdiv(p.nblk, 4));
   const int out = q->out_dtype == BSG_E4M3 ? kOutE4M3 : (q->out_dtype == BSG_E5M2 ? kOutE5M2 : kOutE2M1);
   const void* fn = pick_kernel(in_bf16, out, q->sf_vec_size);
-  // enough resident CTAs per SM to keep 16-byte loads in flight for HBM
-  const int64_t want = static_cast<int64_t>(sms) * 8;
+  // one full wave of resident CTAs (as many per SM as registers allow, at
+  // most 8), each striding over units: no partial second wave
+  int occ;
+  {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    int& slot = g_dev_occ[dev][variant_of(in_bf16, out, q->sf_vec_size)];
+    if (slot == 0) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, 0) != cudaSuccess) {
+        cudaGetLastError();
+        return BSG_ERR_CUDA;
+      }
+      slot = n < 1 ? 1 : (n > 8 ? 8 : n);
+    }
+    occ = slot;
+  }
+  const int64_t want = static_cast<int64_t>(sms) * occ;
   const int64_t extra = static_cast<int64_t>(p.L) * (p.t_k + p.t_r);
   int64_t grid = p.num_units > extra ? p.num_units : extra;
   if (grid > want) grid = want;

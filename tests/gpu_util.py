@@ -15,7 +15,8 @@ POISON_BYTE = 0xA5
 
 def problem_of(p: synth.Problem, **hints) -> bsg.bsg_problem:
     return bsg.make_problem(p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv, p.c_dtype,
-                            p.c_major, sf_dtype=p.sf_dtype, **hints)
+                            p.c_major, sf_dtype=p.sf_dtype, a_major=p.a_major,
+                            b_major=p.b_major, **hints)
 
 
 def to_device(inp: synth.Inputs, dev="cuda:0"):
@@ -76,7 +77,8 @@ def assert_parity(inp: synth.Inputs, c_gpu: np.ndarray, amax_gpu: float, ref=Non
     p = inp.problem
     if ref is None:
         ref = oracle.reference(p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv, inp.A, inp.B,
-                               inp.SFA, inp.SFB, p.c_dtype, sf_dtype=p.sf_dtype)
+                               inp.SFA, inp.SFB, p.c_dtype, sf_dtype=p.sf_dtype,
+                               a_major=p.a_major, b_major=p.b_major)
     finite = np.isfinite(ref["c"])
     with np.errstate(invalid="ignore"):
         err = np.abs(c_gpu - ref["c"])

@@ -101,6 +101,13 @@ OK_CASES = [
          sf_dtype="e4m3", c_dtype="bf16"),
     dict(M=130, N=96, K=160, L=2, a_dtype="e2m1", b_dtype="e2m1", sf_vec_size=16,
          sf_dtype="e4m3", c_dtype="e2m1"),
+    dict(M=4096, N=4096, K=4096, L=1, a_major="m", b_major="n", c_dtype="bf16"),
+    dict(M=144, N=96, K=40, L=2, a_major="m", b_major="n"),     # K free when both are MN-major
+    dict(M=16, N=8, K=64, L=1, a_major="m"),
+    dict(M=8, N=16, K=64, L=1, b_major="n", a_dtype="e5m2"),
+    dict(M=256, N=512, K=256, L=1, b_major="n", tile_n=256, cluster_m=2),
+    dict(M=256, N=512, K=256, L=1, b_major="n", tile_n=128),
+    dict(M=256, N=512, K=256, L=1, a_major="m", tile_n=256, cluster_m=4),
 ]
 
 
@@ -138,7 +145,17 @@ BAD_CASES = [
     (dict(M=4, N=4, K=32, L=1, a_dtype="f32"), bsg.BSG_ERR_INVALID_ARG, "A dtype"),
     (dict(M=4, N=4, K=64, L=1, a_dtype="e2m1", b_dtype="e2m1", sf_vec_size=16, a_major="m"),
      bsg.BSG_ERR_UNSUPPORTED, "FP4 not k-major"),
-    (dict(M=4, N=4, K=32, L=1, b_major="n"), bsg.BSG_ERR_UNSUPPORTED, "MN-major B"),
+    (dict(M=4, N=4, K=32, L=1, b_major="n"), bsg.BSG_ERR_ALIGNMENT, "n-major B, N % 16"),
+    (dict(M=20, N=16, K=32, L=1, a_major="m"), bsg.BSG_ERR_ALIGNMENT, "m-major A, M % 16"),
+    (dict(M=16, N=16, K=40, L=1, a_major="m"), bsg.BSG_ERR_ALIGNMENT, "k-major B, K % 16"),
+    (dict(M=16, N=16, K=32, L=1, a_major="n"), bsg.BSG_ERR_INVALID_ARG, "A n-major"),
+    (dict(M=16, N=16, K=32, L=1, b_major="m"), bsg.BSG_ERR_INVALID_ARG, "B m-major"),
+    (dict(M=16, N=16, K=64, L=1, a_dtype="e2m1", b_dtype="e2m1", sf_vec_size=16, a_major="m"),
+     bsg.BSG_ERR_UNSUPPORTED, "FP4 m-major"),
+    (dict(M=256, N=512, K=256, L=1, b_major="n", tile_n=256, cluster_m=4),
+     bsg.BSG_ERR_UNSUPPORTED, "n-major B over a cluster of four"),
+    (dict(M=256, N=512, K=256, L=1, b_major="n", tile_n=256, cluster_m=1),
+     bsg.BSG_ERR_UNSUPPORTED, "n-major B 256 wide in one CTA"),
     (dict(M=4, N=4, K=32, L=1, a_major="x"), bsg.BSG_ERR_INVALID_ARG, "bad major"),
     (dict(M=4, N=4, K=32, L=1, c_major="k"), bsg.BSG_ERR_INVALID_ARG, "bad C major"),
     (dict(M=4, N=4, K=24, L=1), bsg.BSG_ERR_ALIGNMENT, "FP8 row of 24 bytes"),

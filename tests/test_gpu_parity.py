@@ -64,6 +64,7 @@ REDUCED = [
     (4, dict(M=512, N=384, K=1024)),
     (5, dict(M=328, N=200, K=896, L=2)),
     (6, dict(M=384, N=640, K=1024)),
+    (7, dict(M=640, N=512, K=1024)),
 ]
 
 
@@ -200,7 +201,7 @@ def test_run_host_end_to_end():
 
 # ------------------------------------------------------ full-size workloads
 
-@pytest.mark.parametrize("number", [1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("number", [1, 2, 3, 4, 5, 6, 7])
 def test_workload_full_size_sampled(number):
     """Each workload at its full size, in the benchmark's launch
     configuration: the oracle at 4096 seeded points plus the corners, the
@@ -213,7 +214,8 @@ def test_workload_full_size_sampled(number):
     extra = [(arg[1], arg[2], arg[0]), (p.M - 1, p.N - 1, p.L - 1), (p.M // 2, p.N - 1, 0)]
     pts = synth.sample_points(p, 4096, 77 + number, extra)
     cref, s = oracle.gemm_sample(p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv, inp.A,
-                                 inp.B, inp.SFA, inp.SFB, pts, sf_dtype=p.sf_dtype)
+                                 inp.B, inp.SFA, inp.SFB, pts, sf_dtype=p.sf_dtype,
+                                 a_major=p.a_major, b_major=p.b_major)
     cref = oracle.round_to(cref, p.c_dtype)
     tau = oracle.tolerance(cref, s, p.c_dtype)
     got = c[pts[:, 2], pts[:, 0], pts[:, 1]]
