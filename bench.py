@@ -51,15 +51,22 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # comments and whitespace removed, so only a code change invalidates an
 # entry) and workload.
 TRAFFIC = {
-    ("52da3c12e74b3b92", 2): 37115904,
-    ("52da3c12e74b3b92", 3): 417080320,
-    ("52da3c12e74b3b92", 4): 202603776,
+    ("4efc7f072cbb017e", 2): 36765184,
+    ("4efc7f072cbb017e", 3): 415333120,
+    ("4efc7f072cbb017e", 4): 203169024,
+    ("4efc7f072cbb017e", 6): 203011840,
+    ("4efc7f072cbb017e", 7): 36494336,
 }
 
 
 # the same for the quantizer kernel (csrc/quant.cu), keyed by its code hash
-# and quantizer workload
-TRAFFIC_Q = {}
+# and quantizer workload.  An HBM-bound kernel's writes partly stay in L2 when
+# it ends (up to the 129 MB L2), so its write bytes read below the codes and
+# scales it writes.
+TRAFFIC_Q = {
+    ("b603e92150e0b482", 1): 624015104,
+    ("b603e92150e0b482", 2): 289099776,
+}
 
 QMETRIC = "MX quantize GB/s on 1 GB300 (X read + codes and scales written); % of HBM copy bandwidth"
 QWORKLOADS = {
