@@ -45,6 +45,10 @@ def flush_l2(buf) -> None:
     buf.zero_()
     buf.amax()
 NOMINAL_RATIO = {"fp8": 4.5 / 2.25, "fp4": 13.5 / 2.25}  # dense tensor peak vs bf16
+# Block-scaled MMA throughput per SM and clock, measured on GB300 with
+# back-to-back tcgen05.mma (M=128 or a 256-row CTA pair, N=256): FP8 8192
+# FMA, FP4 (mxf4nvf4 2X/4X, mxf4) 16384 FMA -- twice FP8, not the nominal 3x
+MEASURED_FP4_OVER_FP8 = 2.0
 FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM bytes per launch of the GEMM kernel from an ncu capture, keyed by the
 # kernel source it was taken on (sha256 prefix of csrc/bsgemm.cu with its
@@ -322,6 +326,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                 "kernel": info["kernel_name"],
                 "hbm_gbs_algorithmic": round(nums["bytes"] / (ms / 1e3) / 1e9, 1),
                 "hbm_frac_of_" + source: round(nums["bytes"] / (ms / 1e3) / 1e9 / hbm, 4)}
+    if nums["kind"] == "fp4":
+        # the FP4 rate this part's tensor cores reach: 2x the FP8 peak above
+        fp4_reach = bf16 * NOMINAL_RATIO["fp8"] * MEASURED_FP4_OVER_FP8
+        roofline["frac_of_measured_fp4_mma_rate"] = round(achieved / fp4_reach, 4)
 
     line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),

@@ -153,7 +153,7 @@ bsg_status bsg_run(const bsg_plan *plan, const void *A, const void *B, const voi
 
 /* bsg_run without a caller workspace, for callers that cannot allocate
  * device memory (no allocator to draw from, or code running where
- * cudaMalloc is not permitted).  The paper has no counterpart: it is a
+ * cudaMalloc is not permitted).  The pages have no counterpart: it is a
  * convenience of this library.  The workspace comes from a fixed array
  * inside the library (4096 bytes on every GPU that loads it, kept until the
  * process exits); a plan needing more returns BSG_ERR_WORKSPACE.  The first
