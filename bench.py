@@ -55,11 +55,11 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # comments and whitespace removed, so only a code change invalidates an
 # entry) and workload.
 TRAFFIC = {
-    ("4efc7f072cbb017e", 2): 36765184,
-    ("4efc7f072cbb017e", 3): 415333120,
-    ("4efc7f072cbb017e", 4): 203169024,
-    ("4efc7f072cbb017e", 6): 203011840,
-    ("4efc7f072cbb017e", 7): 36494336,
+    ("416f27cf26ffa77a", 2): 36836352,
+    ("416f27cf26ffa77a", 3): 417184256,
+    ("416f27cf26ffa77a", 4): 203142144,
+    ("416f27cf26ffa77a", 6): 202631680,
+    ("416f27cf26ffa77a", 7): 36548352,
 }
 
 

@@ -870,6 +870,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // MMAs.  fp32 C: two passes of TILE_N/4 columns, released after the
     // second pass's loads.
     constexpr int kCols = TILE_N / 2;
+    constexpr int kCh16 = kCols / 16;  // 16-column chunks of this warp
+    constexpr int kRnd = 4;            // chunks per round of tensor-memory loads
     const int q = warp & 3;
     const int h = (warp - kEpiWarp0) >> 2;
     uint8_t* const stg = smem + p.smem_epi + (warp - kEpiWarp0) * kEpiStageBytes;
@@ -903,10 +905,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           else mbar_arrive(release_bar);
         }
       };
-      // packed rounded values of the 16- and 8-bit paths, and the two-deep
-      // tensor-memory load buffer (chunk c converts while chunk c + 1 loads)
+      // packed rounded values of the 16- and 8-bit paths, and one round of
+      // tensor-memory loads
       uint32_t pk[kCols / 2];
-      uint32_t rb[2][16];
+      uint32_t rb[kRnd][16];
       if (KIND != kKindF8F6F4 &&
           (p.c_dtype == BSG_E4M3 || p.c_dtype == BSG_E5M2 || p.c_dtype == BSG_E2M1)) {
         // FP8 or packed E2M1 C (FP4 operands only): each 16-column chunk is
@@ -914,41 +916,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the largest stored magnitude (the rounding is monotone in |x|).
         // pk: four FP8 codes per register (E2M1: eight, the first kCols/8)
         const bool fp4 = p.c_dtype == BSG_E2M1, e5 = p.c_dtype == BSG_E5M2;
-        tc_ld_32x32b_x16(taddr, rb[0]);
-        tc_wait_ld();
 #pragma unroll
-        for (int cc = 0; cc < kCols; cc += 16) {
-          uint32_t* r = rb[(cc / 16) & 1];
-          if (cc + 16 < kCols) tc_ld_32x32b_x16(taddr + cc + 16, rb[((cc / 16) + 1) & 1]);
-          const bool whole = row_ok && n0 + cc + 16 <= p.N;
+        for (int c0 = 0; c0 < kCh16; c0 += kRnd) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            uint32_t a = r[j] & 0x7FFFFFFFu;
-            if (fp4 && a > 0x7F800000u) a = 0u;  // stored as +0
-            if (!whole && !(row_ok && n0 + cc + j < p.N)) a = 0u;
-            vmax = max(vmax, a);
-          }
-          if (fp4) {
-            uint32_t w0 = 0u, w1 = 0u;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint32_t b = cvt2_e2m1(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-              if (j < 4) w0 |= b << (8 * j);
-              else w1 |= b << (8 * (j - 4));
-            }
-            pk[cc / 8] = w0;
-            pk[cc / 8 + 1] = w1;
-          } else {
-#pragma unroll
-            for (int j = 0; j < 8; j += 2) {
-              const float a0 = __uint_as_float(r[2 * j]), a1 = __uint_as_float(r[2 * j + 1]);
-              const float b0 = __uint_as_float(r[2 * j + 2]), b1 = __uint_as_float(r[2 * j + 3]);
-              const uint32_t lo = e5 ? cvt2_e5m2(a0, a1) : cvt2_e4m3(a0, a1);
-              const uint32_t hi = e5 ? cvt2_e5m2(b0, b1) : cvt2_e4m3(b0, b1);
-              pk[cc / 4 + j / 2] = lo | (hi << 16);
-            }
-          }
+          for (int i = 0; i < kRnd; ++i)
+            if (c0 + i < kCh16) tc_ld_32x32b_x16(taddr + (c0 + i) * 16, rb[i]);
           tc_wait_ld();
+#pragma unroll
+          for (int i = 0; i < kRnd; ++i) {
+            if (c0 + i >= kCh16) continue;
+            const int cc = (c0 + i) * 16;
+            const uint32_t* r = rb[i];
+            const bool whole = row_ok && n0 + cc + 16 <= p.N;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              uint32_t a = r[j] & 0x7FFFFFFFu;
+              if (fp4 && a > 0x7F800000u) a = 0u;  // stored as +0
+              if (!whole && !(row_ok && n0 + cc + j < p.N)) a = 0u;
+              vmax = max(vmax, a);
+            }
+            if (fp4) {
+              uint32_t w0 = 0u, w1 = 0u;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const uint32_t b = cvt2_e2m1(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                if (j < 4) w0 |= b << (8 * j);
+                else w1 |= b << (8 * (j - 4));
+              }
+              pk[cc / 8] = w0;
+              pk[cc / 8 + 1] = w1;
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; j += 2) {
+                const float a0 = __uint_as_float(r[2 * j]), a1 = __uint_as_float(r[2 * j + 1]);
+                const float b0 = __uint_as_float(r[2 * j + 2]), b1 = __uint_as_float(r[2 * j + 3]);
+                const uint32_t lo = e5 ? cvt2_e5m2(a0, a1) : cvt2_e4m3(a0, a1);
+                const uint32_t hi = e5 ? cvt2_e5m2(b0, b1) : cvt2_e4m3(b0, b1);
+                pk[cc / 4 + j / 2] = lo | (hi << 16);
+              }
+            }
+          }
         }
         release();
         uint8_t* const cbase = static_cast<uint8_t*>(p.c) + (fp4 ? batch_off / 2 : batch_off);
@@ -982,38 +989,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (p.c_dtype != BSG_F32) {
         // pk: two rounded 16-bit values per register
         const bool bf = p.c_dtype == BSG_BF16;
-        tc_ld_32x32b_x16(taddr, rb[0]);
-        tc_wait_ld();
+        // rounds of kRnd 16-column loads: all of a round in flight at once,
+        // one wait, then its conversions (fewer waits than one load ahead)
 #pragma unroll
-        for (int cc = 0; cc < kCols; cc += 16) {
-          uint32_t* r = rb[(cc / 16) & 1];
-          if (cc + 16 < kCols) tc_ld_32x32b_x16(taddr + cc + 16, rb[((cc / 16) + 1) & 1]);
-          // the whole chunk is stored (all but a ragged edge)
-          const bool whole = row_ok && n0 + cc + 16 <= p.N;
+        for (int c0 = 0; c0 < kCh16; c0 += kRnd) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float f0 = __uint_as_float(r[2 * j]), f1 = __uint_as_float(r[2 * j + 1]);
-            // two round-to-nearest-even conversions in one: low half column
-            // cc + 2j, high half column cc + 2j + 1
-            uint32_t h;
-            if (bf) {
-              const __nv_bfloat162 v = __floats2bfloat162_rn(f0, f1);
-              h = *reinterpret_cast<const uint32_t*>(&v);
-            } else {
-              const __half2 v = __floats2half2_rn(f0, f1);
-              h = *reinterpret_cast<const uint32_t*>(&v);
-            }
-            pk[cc / 2 + j] = h;
-            // only stored elements count toward Amax
-            uint32_t m = h & 0x7FFF7FFFu;
-            if (!whole) {
-              const int n = n0 + cc + 2 * j;
-              if (!(row_ok && n < p.N)) m &= 0xFFFF0000u;
-              if (!(row_ok && n + 1 < p.N)) m &= 0x0000FFFFu;
-            }
-            vmax = __vmaxu2(vmax, m);
-          }
+          for (int i = 0; i < kRnd; ++i)
+            if (c0 + i < kCh16) tc_ld_32x32b_x16(taddr + (c0 + i) * 16, rb[i]);
           tc_wait_ld();
+#pragma unroll
+          for (int i = 0; i < kRnd; ++i) {
+            if (c0 + i >= kCh16) continue;
+            const int cc = (c0 + i) * 16;
+            const uint32_t* r = rb[i];
+            // the whole chunk is stored (all but a ragged edge)
+            const bool whole = row_ok && n0 + cc + 16 <= p.N;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float f0 = __uint_as_float(r[2 * j]), f1 = __uint_as_float(r[2 * j + 1]);
+              // two round-to-nearest-even conversions in one: low half column
+              // cc + 2j, high half column cc + 2j + 1
+              uint32_t h;
+              if (bf) {
+                const __nv_bfloat162 v = __floats2bfloat162_rn(f0, f1);
+                h = *reinterpret_cast<const uint32_t*>(&v);
+              } else {
+                const __half2 v = __floats2half2_rn(f0, f1);
+                h = *reinterpret_cast<const uint32_t*>(&v);
+              }
+              pk[cc / 2 + j] = h;
+              // only stored elements count toward Amax
+              uint32_t m = h & 0x7FFF7FFFu;
+              if (!whole) {
+                const int n = n0 + cc + 2 * j;
+                if (!(row_ok && n < p.N)) m &= 0xFFFF0000u;
+                if (!(row_ok && n + 1 < p.N)) m &= 0x0000FFFFu;
+              }
+              vmax = __vmaxu2(vmax, m);
+            }
+          }
         }
         release();
         uint16_t* const cbase = static_cast<uint16_t*>(p.c) + batch_off;
