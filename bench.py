@@ -55,11 +55,11 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # comments and whitespace removed, so only a code change invalidates an
 # entry) and workload.
 TRAFFIC = {
-    ("416f27cf26ffa77a", 2): 36836352,
-    ("416f27cf26ffa77a", 3): 417184256,
-    ("416f27cf26ffa77a", 4): 203142144,
-    ("416f27cf26ffa77a", 6): 202631680,
-    ("416f27cf26ffa77a", 7): 36548352,
+    ("55b7b7ae8c77d558", 2): 36427776,
+    ("55b7b7ae8c77d558", 3): 415922944,
+    ("55b7b7ae8c77d558", 4): 203178752,
+    ("55b7b7ae8c77d558", 6): 202455808,
+    ("55b7b7ae8c77d558", 7): 36432128,
 }
 
 

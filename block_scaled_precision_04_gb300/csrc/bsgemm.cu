@@ -895,6 +895,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = row < p.M;
       const size_t batch_off = static_cast<size_t>(tc.l) * p.M * p.N;
       const int n0 = tc.nt * TILE_N + h * kCols;
+      // columns of this warp's half stored in this lane's row
+      const int lim = row_ok ? p.N - n0 : 0;
       const uint32_t release_bar = acce0 + 8u * acc;
       if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1u; }
       auto release = [&]() {
@@ -927,13 +929,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c0 + i >= kCh16) continue;
             const int cc = (c0 + i) * 16;
             const uint32_t* r = rb[i];
-            const bool whole = row_ok && n0 + cc + 16 <= p.N;
+            if (lim >= cc + 16) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              uint32_t a = r[j] & 0x7FFFFFFFu;
-              if (fp4 && a > 0x7F800000u) a = 0u;  // stored as +0
-              if (!whole && !(row_ok && n0 + cc + j < p.N)) a = 0u;
-              vmax = max(vmax, a);
+              for (int j = 0; j < 16; ++j) {
+                uint32_t a = r[j] & 0x7FFFFFFFu;
+                if (fp4 && a > 0x7F800000u) a = 0u;  // stored as +0
+                vmax = max(vmax, a);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                uint32_t a = r[j] & 0x7FFFFFFFu;
+                if (fp4 && a > 0x7F800000u) a = 0u;
+                if (cc + j >= lim) a = 0u;
+                vmax = max(vmax, a);
+              }
             }
             if (fp4) {
               uint32_t w0 = 0u, w1 = 0u;
@@ -1002,8 +1012,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c0 + i >= kCh16) continue;
             const int cc = (c0 + i) * 16;
             const uint32_t* r = rb[i];
-            // the whole chunk is stored (all but a ragged edge)
-            const bool whole = row_ok && n0 + cc + 16 <= p.N;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const float f0 = __uint_as_float(r[2 * j]), f1 = __uint_as_float(r[2 * j + 1]);
@@ -1018,14 +1026,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 h = *reinterpret_cast<const uint32_t*>(&v);
               }
               pk[cc / 2 + j] = h;
-              // only stored elements count toward Amax
-              uint32_t m = h & 0x7FFF7FFFu;
-              if (!whole) {
-                const int n = n0 + cc + 2 * j;
-                if (!(row_ok && n < p.N)) m &= 0xFFFF0000u;
-                if (!(row_ok && n + 1 < p.N)) m &= 0x0000FFFFu;
+            }
+            // only stored elements count toward Amax: a whole chunk without
+            // per-element tests (which made the drain four times slower),
+            // the ragged edge with them
+            if (lim >= cc + 16) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) vmax = __vmaxu2(vmax, pk[cc / 2 + j] & 0x7FFF7FFFu);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                uint32_t m = pk[cc / 2 + j] & 0x7FFF7FFFu;
+                if (cc + 2 * j >= lim) m &= 0xFFFF0000u;
+                if (cc + 2 * j + 1 >= lim) m &= 0x0000FFFFu;
+                vmax = __vmaxu2(vmax, m);
               }
-              vmax = __vmaxu2(vmax, m);
             }
           }
         }
