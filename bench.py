@@ -55,11 +55,11 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # comments and whitespace removed, so only a code change invalidates an
 # entry) and workload.
 TRAFFIC = {
-    ("55b7b7ae8c77d558", 2): 36427776,
-    ("55b7b7ae8c77d558", 3): 415922944,
-    ("55b7b7ae8c77d558", 4): 203178752,
-    ("55b7b7ae8c77d558", 6): 202455808,
-    ("55b7b7ae8c77d558", 7): 36432128,
+    ("56ab9e2f61816786", 2): 36834816,
+    ("56ab9e2f61816786", 3): 415449856,
+    ("56ab9e2f61816786", 4): 202578688,
+    ("56ab9e2f61816786", 6): 202518016,
+    ("56ab9e2f61816786", 7): 36510464,
 }
 
 

@@ -1382,12 +1382,11 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   k.k_bytes = static_cast<int>(fp4 ? prob->K / 2 : prob->K);
   k.k_stages = static_cast<int>(cdiv(k.k_bytes, kStageKBytes));
   // Tile width.  256 (one accumulator) halves the issue work and the L2
-  // traffic per flop against 128; 224 (FP8, CTA pairs only) keeps two
-  // accumulators in tensor memory so the epilogue overlaps the next tile,
-  // and changes how the tiles fill the last wave.  With no hint the cheaper
-  // of 224 and 256 is taken by a model counted in 128-byte K stages of MMA
-  // work: every cluster runs ceil(units / clusters) tiles, and a tile with
-  // one accumulator also waits for its epilogue (about four stages).
+  // traffic per flop against 128, and is the default above N = 128.  224
+  // (FP8, CTA pairs only; a hint) keeps two accumulators in tensor memory so
+  // that the epilogue overlaps the next tile; since the epilogue's drain of a
+  // single accumulator became short, 256 measures faster on every workload
+  // (MXFP8 4096^3: 2165 against 2035 TFLOP/s).
   const bool pair_ok = k.tiles_m >= 2 && (prob->cluster_m == 0 || prob->cluster_m == 2);
   const bool n224_ok = kind == kKindF8F6F4 && pair_ok;
   if (prob->tile_n == 128) {
@@ -1397,19 +1396,8 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   } else if (prob->tile_n == 224) {
     if (!n224_ok) { delete plan; return BSG_ERR_UNSUPPORTED; }
     k.tile_n = 224;
-  } else if (prob->N <= 128) {
-    k.tile_n = 128;
   } else {
-    k.tile_n = 256;
-    if (n224_ok) {
-      const int64_t clusters = sms / 2 > 0 ? sms / 2 : 1;
-      auto estimate = [&](int tn, bool overlapped) {
-        const int64_t units = prob->L * cdiv(k.tiles_m, 2) * cdiv(prob->N, tn);
-        return static_cast<double>(cdiv(units, clusters)) *
-               (k.k_stages * tn / 256.0 + (overlapped ? 0.0 : 4.0));
-      };
-      if (estimate(224, true) < estimate(256, false)) k.tile_n = 224;
-    }
+    k.tile_n = prob->N <= 128 ? 128 : 256;
   }
   int num_acc = k.tile_n == 256 ? 1 : 2;
   // 224- and 256-wide tiles run as cta_group::2 pairs by default (hint 1:
