@@ -97,8 +97,8 @@ class Problem:
     def describe(self) -> str:
         ab = self.a_dtype if self.a_dtype == self.b_dtype else f"{self.a_dtype}x{self.b_dtype}"
         return (f"{ab} M={self.M} N={self.N} K={self.K} L={self.L} sfv={self.sfv} "
-                f"A {self.a_major}-major B {self.b_major}-major C={self.c_dtype} "
-                f"{self.c_major}-major")
+                f"sf={self.sf_dtype} A {self.a_major}-major B {self.b_major}-major "
+                f"C={self.c_dtype} {self.c_major}-major")
 
 
 @dataclasses.dataclass

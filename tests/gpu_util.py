@@ -97,3 +97,29 @@ def assert_parity(inp: synth.Inputs, c_gpu: np.ndarray, amax_gpu: float, ref=Non
     else:
         assert amax_gpu == ref["amax"]
     return ref
+
+
+def run_gpu_host(inp: synth.Inputs, **hints):
+    """bsg_run_host: pinned host A/B/scales in, host C and Amax out (copies
+    and the launch enqueued on one stream).  Returns (C logical float64, amax)."""
+    p = inp.problem
+    op = bsg.GemmAmax(problem_of(p, **hints))
+    dA, dB, dSFA, dSFB = to_device(inp)
+    shape = synth.c_shape(p)
+    dC = torch.empty(shape, dtype=TORCH_C[p.c_dtype], device="cuda:0")
+    damax = torch.empty(1, dtype=torch.float32, device="cuda:0")
+    dev = bsg.bsg_device_buffers(dA.data_ptr(), dB.data_ptr(), dSFA.data_ptr(), dSFB.data_ptr(),
+                                 dC.data_ptr(), damax.data_ptr(), op.workspace.data_ptr(),
+                                 op.ws_bytes)
+    hA, hB, hSFA, hSFB = [torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+                          for x in (inp.A, inp.B, inp.SFA, inp.SFB)]
+    hC = torch.empty(shape, dtype=TORCH_C[p.c_dtype]).pin_memory()
+    hamax = torch.empty(1, dtype=torch.float32).pin_memory()
+    s = torch.cuda.current_stream().cuda_stream
+    st = bsg.bsg_run_host(op.plan, hA.data_ptr(), hB.data_ptr(), hSFA.data_ptr(),
+                          hSFB.data_ptr(), hC.data_ptr(), hamax.data_ptr(), dev, s)
+    assert st == bsg.BSG_OK, bsg.bsg_status_string(st)
+    torch.cuda.synchronize()
+    assert op.device_status() == bsg.BSG_OK
+    return c_to_logical(hC, p), float(hamax[0])
+

@@ -14,7 +14,7 @@ import torch
 import block_scaled_precision_04_gb300 as bsg
 import oracle
 import synth
-from gpu_util import abs_max_bits, assert_parity, problem_of, run_gpu, to_device
+from gpu_util import abs_max_bits, assert_parity, problem_of, run_gpu, run_gpu_host, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -175,28 +175,23 @@ def test_plan_describe():
     assert info["kernel_name"]
 
 
-def test_run_host_end_to_end():
-    """bsg_run_host: host buffers in, host C and Amax out."""
-    inp = synth.workload(2, M=256, N=256, K=256)
-    p = inp.problem
-    op = bsg.GemmAmax(problem_of(p))
-    dA, dB, dSFA, dSFB = to_device(inp)
-    dC = torch.empty(synth.c_shape(p), dtype=torch.bfloat16, device="cuda:0")
-    damax = torch.empty(1, dtype=torch.float32, device="cuda:0")
-    dev = bsg.bsg_device_buffers(dA.data_ptr(), dB.data_ptr(), dSFA.data_ptr(), dSFB.data_ptr(),
-                                 dC.data_ptr(), damax.data_ptr(), op.workspace.data_ptr(),
-                                 op.ws_bytes)
-    hA, hB, hSFA, hSFB = [torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
-                          for x in (inp.A, inp.B, inp.SFA, inp.SFB)]
-    hC = torch.empty(synth.c_shape(p), dtype=torch.bfloat16).pin_memory()
-    hamax = torch.empty(1, dtype=torch.float32).pin_memory()
-    s = torch.cuda.current_stream().cuda_stream
-    st = bsg.bsg_run_host(op.plan, hA.data_ptr(), hB.data_ptr(), hSFA.data_ptr(),
-                          hSFB.data_ptr(), hC.data_ptr(), hamax.data_ptr(), dev, s)
-    assert st == bsg.BSG_OK
-    torch.cuda.synchronize()
-    c = hC.float().numpy().astype(np.float64)
-    assert_parity(inp, c, float(hamax[0]))
+HOST_CASES = [
+    P(256, 256, 256, c="bf16"),
+    P(300, 224, 384, 2, a="e2m1", b="e2m1", sfv=16, c="e2m1"),        # packed FP4 C
+    P(144, 160, 256, a="e2m1", b="e2m1", sfv=16, c="e4m3", major="m"),  # FP8 C, m-major
+    synth.Problem(272, 176, 96, 2, "e4m3", "e5m2", 32, "f32", "n", a_major="m", b_major="n"),
+    synth.Problem(256, 384, 512, 1, "e2m1", "e2m1", 16, "bf16", "n", sf_dtype="e4m3"),
+]
+
+
+@pytest.mark.parametrize("p", HOST_CASES, ids=lambda p: p.describe().replace(" ", "_"))
+def test_run_host_end_to_end(p):
+    """bsg_run_host: host buffers in, host C and Amax out; the copies are
+    sized from the problem (packed E2M1 C, MN-major operands, E4M3 scales)."""
+    lo, hi = (0x30, 0x40) if p.sf_dtype == "e4m3" else (120, 128)
+    inp = synth.uniform_codes(p, p.M + p.N + p.K, lo, hi)
+    c, amax = run_gpu_host(inp)
+    assert_parity(inp, c, amax)
 
 
 # ------------------------------------------------------ full-size workloads
