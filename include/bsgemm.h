@@ -24,10 +24,11 @@
  *
  *   A    (M, K, L), k-major: strides (K, 1, M*K) in elements.  FP8 codes one
  *        per byte; packed FP4 (E2M1) two per byte, element 2i in the low
- *        nibble, so a row holds K/2 bytes ("Layouts and strides").
- *   B    (N, K, L), k-major, same element type rules as A.
- *   SFA  E8M0 (or E4M3) bytes, physical C-contiguous (L, ceil(M/128), ceil(K/(4*sfv)),
- *        32, 4, 4), which is the page's logical (32, 4, ceil(M/128), 4,
+ *        nibble, so a row holds K/2 bytes ("Layouts and strides").  FP8 A
+ *        may instead be m-major: strides (1, M, M*K) ("Parameters").
+ *   B    (N, K, L), k-major (or, FP8, n-major), same element rules as A.
+ *   SFA  E8M0 (or E4M3) bytes, physical C-contiguous (L, ceil(M/128),
+ *        ceil(K/(4*sfv)), 32, 4, 4), which is the page's logical (32, 4, ceil(M/128), 4,
  *        ceil(K/(4*sfv)), L) view permuted ("Using JAX arrays").  Row
  *        m = 128*mt + 32*m1 + m0 and K-block kb = 4*kt + kin sit at byte
  *        ((l*T_m + mt)*T_k + kt)*512 + m0*16 + m1*4 + kin.
@@ -42,15 +43,18 @@
  * hold a finite scale (any byte but 0xFF for E8M0; any byte but 0x7F and
  * 0xFF for E4M3) so that 0 * scale stays 0.
  *
- * Support ("Support surface and constraints"): A/B k-major; A/B both FP8
+ * Support ("Support surface and constraints"): A/B k-major, or m-major A /
+ * n-major B for FP8 (M, N a multiple of 16; an n-major B runs on CTA pairs
+ * or 128-wide tiles, not on clusters of four or one 256-wide CTA); A/B both FP8
  * (E4M3/E5M2, each on its own) with sf_vec_size 32 and E8M0 scales, or both
  * E2M1 with sf_vec_size 32 and E8M0 scales or sf_vec_size 16 and E8M0 or
  * E4M3 scales; C fp32/fp16/bf16 always, E4M3/E5M2/E2M1 with E2M1 operands
  * only.  Rows of A, B and C must be 16-byte aligned along their contiguous
- * dimension (an E2M1 C row of N/2 bytes included, N even), every pointer
- * 16-byte aligned.  Everything else returns BSG_ERR_UNSUPPORTED or
- * BSG_ERR_INVALID_ARG before any launch (errors are reported before launch,
- * as "Grouped GEMM (SM100 BF16)", "Scheduling, caching, and errors", does).
+ * dimension (K bytes of a k-major operand, M or N bytes of an MN-major one,
+ * an E2M1 C row of N/2 bytes with N even), every pointer 16-byte aligned.
+ * Everything else returns BSG_ERR_UNSUPPORTED or BSG_ERR_INVALID_ARG before
+ * any launch (errors are reported before launch, as "Grouped GEMM (SM100
+ * BF16)", "Scheduling, caching, and errors", does).
  *
  * Ownership: the caller owns every device buffer (A, B, SFA, SFB, C, Amax,
  * workspace).  A plan owns host memory only.  No entry point allocates
@@ -99,7 +103,7 @@ typedef struct {
     int32_t a_dtype, b_dtype;   /* bsg_dtype */
     int32_t sf_dtype;           /* BSG_UE8M0, or BSG_E4M3 (E2M1 A/B, sfv 16) */
     int32_t c_dtype;            /* BSG_F32, BSG_F16, BSG_BF16, BSG_E4M3, BSG_E5M2, BSG_E2M1 */
-    char a_major, b_major;      /* 'k' */
+    char a_major, b_major;      /* 'k'; or 'm' (A) / 'n' (B) for FP8 operands */
     char c_major;               /* 'n' or 'm' */
     char reserved0;
     int32_t sf_vec_size;        /* 16 or 32 */
