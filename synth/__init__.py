@@ -380,3 +380,18 @@ def real_blocks(L: int, rows: int, cols: int, seed: int, block: int = 32, spread
             else:
                 blk[:] = np.float32(1.5) * np.exp2(np.float32(rng.integers(-5, 5)))
     return x
+
+
+def device_real_blocks(L: int, rows: int, cols: int, seed: int, device, block: int = 32,
+                       spread: int = 30):
+    """real_blocks' recipe drawn on a CUDA device by torch's seeded generator,
+    for inputs too large to build on the host: N(0, 1) values, each
+    `block`-element run scaled by its own 2^j, j uniform in [-spread, spread].
+    Returns a float32 tensor (L, rows, cols) on `device`."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    x = torch.randn((L, rows, cols), generator=g, device=device, dtype=torch.float32)
+    j = torch.randint(-spread, spread + 1, (L, rows, cols // block), generator=g, device=device)
+    x.view(L, rows, cols // block, block).mul_(torch.exp2(j.float()).unsqueeze(-1))
+    return x
+
