@@ -1,8 +1,12 @@
 // bsgemm.cu -- block-scaled (MX) batched GEMM + global Amax for sm_103a.
 //
 // Operation ("GEMM + Amax (SM100)", section "Equations"):
-//   C[m,n,l] = sum_k dec(A[m,k,l]) 2^(SFA[m,k/sfv,l]-127) * dec(B[n,k,l]) 2^(SFB[n,k/sfv,l]-127)
+//   C[m,n,l] = sum_k dec(A[m,k,l]) sf(SFA[m,k/sfv,l]) * dec(B[n,k,l]) sf(SFB[n,k/sfv,l])
 //   Amax     = max |C|  (over the values as stored in C's dtype)
+// sf(byte) = 2^(byte - 127) for E8M0 scales, the E4M3 value for the NVFP4
+// form (E2M1 operands, sfv 16).  A/B are k-major, or (FP8) m-/n-major tiles
+// read through the instruction descriptor's transpose bits.  C is fp32,
+// fp16 or bf16, or (E2M1 operands) E4M3, E5M2 or packed E2M1.
 //
 // Kernel design (one persistent CTA per SM, 15 warps; by default two CTAs
 // of a cluster form a cta_group::2 pair running 256-row MMAs):
@@ -546,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kSfaStage = kCps * kAtomBytes;
   constexpr uint32_t kSfbStage = kCps * kAtomBytes * kSfbAtoms;
   // scale columns follow the accumulators, one set per smem stage, so that a
-  // stage's tcgen05.cp never rewrites columns an in-flight MMA still reads
+  // stage's tcgen05.st never rewrites columns an in-flight MMA still reads
   constexpr uint32_t kSfCols = 4 * kCps * (1 + G);
   constexpr uint32_t kSfCol0 = NUM_ACC * TILE_N;
   constexpr int kMmasPerStage = kSB / kMmaKBytes;
