@@ -57,3 +57,32 @@ def test_workload_numbers_match_the_page_sizes():
     sf = 32 * 32 * 512
     assert n["bytes"] == 2 * 4096 * 4096 + 2 * sf + 2 * 4096 * 4096
     assert n["kind"] == "fp8"
+
+
+REQUIRED = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+            "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+            "cpu_baseline", "e2e", "impl"}
+
+
+@pytest.mark.parametrize("args", [["--workload", "1"], ["--op", "quantize", "--qworkload", "1"]],
+                         ids=["gemm", "quantize"])
+def test_reference_arm_prints_one_contract_line(args):
+    """`bench.py --impl reference` times the oracle on the host and prints one
+    JSON line with the contract's keys, the metric of the GPU arm and an e2e
+    entry with no host-device copies."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                          "--warmup", "3", "--ref-seconds", "1", *args], cwd=root,
+                         capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert REQUIRED <= set(d), REQUIRED - set(d)
+    assert d["impl"] == "reference" and d["value"] > 0
+    assert d["metric"] == (bench.QMETRIC if "quantize" in args else bench.METRIC)
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
