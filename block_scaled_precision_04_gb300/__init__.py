@@ -130,6 +130,23 @@ def make_problem(M, N, K, L, a_dtype="e4m3", b_dtype="e4m3", sf_vec_size=32, c_d
                        int(sf_vec_size), int(tile_m), int(tile_n), int(cluster_m), int(cluster_n))
 
 
+def problem_bytes(problem: bsg_problem) -> dict:
+    """Bytes each tensor of `problem` spans in the library's layouts: A, B
+    (codes; packed E2M1 two per byte), SFA, SFB (whole 128-row x 4-block
+    scale atoms of 512 bytes) and C."""
+    cdiv = lambda a, b: -(-a // b)
+    fp4 = problem.a_dtype == BSG_E2M1
+    kb = problem.K // 2 if fp4 else problem.K
+    t_k = cdiv(problem.K, 4 * problem.sf_vec_size)
+    item = {BSG_F32: 4, BSG_F16: 2, BSG_BF16: 2}.get(problem.c_dtype, 1)
+    c = problem.L * problem.M * problem.N * item
+    if problem.c_dtype == BSG_E2M1:
+        c //= 2
+    return {"A": problem.L * problem.M * kb, "B": problem.L * problem.N * kb,
+            "SFA": problem.L * cdiv(problem.M, 128) * t_k * 512,
+            "SFB": problem.L * cdiv(problem.N, 128) * t_k * 512, "C": c}
+
+
 def bsg_status_string(status: int) -> str:
     return library().bsg_status_string(int(status)).decode()
 
@@ -234,9 +251,14 @@ class GemmAmax:
 
     def run(self, A, B, SFA, SFB, C, amax, stream=None) -> None:
         import torch
+        need = problem_bytes(self.problem)
+        need["amax"] = 4
         for name, t in (("A", A), ("B", B), ("SFA", SFA), ("SFB", SFB), ("C", C), ("amax", amax)):
             if not t.is_cuda or not t.is_contiguous():
                 raise ValueError(f"{name} must be a contiguous CUDA tensor")
+            if t.numel() * t.element_size() < need[name]:
+                raise ValueError(f"{name} holds {t.numel() * t.element_size()} bytes, "
+                                 f"the problem needs {need[name]}")
         s = stream if stream is not None else torch.cuda.current_stream(self.device).cuda_stream
         check(bsg_run(self.plan, A.data_ptr(), B.data_ptr(), SFA.data_ptr(), SFB.data_ptr(),
                       C.data_ptr(), amax.data_ptr(), self.workspace.data_ptr(), self.ws_bytes, s),

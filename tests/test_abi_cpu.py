@@ -237,3 +237,21 @@ def test_quant_sizes(lib):
     assert st == bsg.BSG_OK and cb == 2 * 130 * 128 and sb == 2 * 2 * 4 * 512
     assert lib.bsg_quantize(None, None, None, None, None) == bsg.BSG_ERR_INVALID_ARG
 
+
+
+def test_problem_bytes_match_the_layouts():
+    """The tensor sizes the Python wrapper checks before a launch: codes
+    (packed E2M1 two per byte), whole scale atoms, and C of its dtype."""
+    pb = bsg.problem_bytes(bsg.make_problem(300, 200, 96, 2, "e4m3", "e5m2", 32, "bf16"))
+    assert pb == {"A": 2 * 300 * 96, "B": 2 * 200 * 96, "SFA": 2 * 3 * 1 * 512,
+                  "SFB": 2 * 2 * 1 * 512, "C": 2 * 300 * 200 * 2}
+    pb = bsg.problem_bytes(bsg.make_problem(130, 96, 128, 1, "e2m1", "e2m1", 16, "e2m1"))
+    assert pb == {"A": 130 * 64, "B": 96 * 64, "SFA": 2 * 2 * 512, "SFB": 1 * 2 * 512,
+                  "C": 130 * 48}
+    # every synthetic generator's tensors have exactly these sizes
+    import synth
+    p = synth.Problem(300, 200, 96, 2, "e4m3", "e5m2", 32, "bf16")
+    inp = synth.uniform_codes(p, 3)
+    pb = bsg.problem_bytes(bsg.make_problem(300, 200, 96, 2, "e4m3", "e5m2", 32, "bf16"))
+    assert (inp.A.nbytes, inp.B.nbytes, inp.SFA.nbytes, inp.SFB.nbytes) == \
+        (pb["A"], pb["B"], pb["SFA"], pb["SFB"])
