@@ -53,6 +53,33 @@ def test_row_split_needs_contiguous_rows():
         sh.local_views(s, inp.A, inp.B, inp.SFA, inp.SFB, C, M=p.M, c_major="m")
 
 
+@pytest.mark.parametrize("M,L,world,a,c", [(300, 4, 3, "e4m3", "f32"), (1000, 1, 4, "e4m3", "bf16"),
+                                           (520, 2, 5, "e2m1", "f16"), (100, 1, 2, "e2m1", "bf16")])
+def test_views_span_the_local_problem(M, L, world, a, c):
+    """Each rank's views hold exactly the bytes its local problem spans (the
+    binding's size check on a run), are C-contiguous (a plain pointer and the
+    library's strides describe them) and start where the rank's rows do."""
+    import block_scaled_precision_04_gb300 as bsg
+    sfv = 16 if a == "e2m1" else 32
+    p = synth.Problem(M, 160, 256, L, a, a, sfv, c, "n")
+    inp = synth.uniform_codes(p, M + world)
+    C = np.zeros(synth.c_shape(p), dtype=np.float32 if c == "f32" else np.uint16)
+    full = bsg.make_problem(p.M, p.N, p.K, p.L, a, a, sfv, c, "n")
+    for r in range(world):
+        s = sh.shard_of(M, L, world, r)
+        if s.empty:
+            continue
+        views = sh.local_views(s, inp.A, inp.B, inp.SFA, inp.SFB, C, M=M)
+        need = bsg.problem_bytes(sh.local_problem(full, s))
+        for key, v in zip(("A", "B", "SFA", "SFB", "C"), views):
+            assert v.flags["C_CONTIGUOUS"], key
+            assert v.nbytes == need[key], (key, r)
+        a_view, c_view = views[0], views[4]
+        row0 = (s.l0 * M + s.m0)
+        assert a_view.ctypes.data - inp.A.ctypes.data == row0 * inp.A.shape[-1]
+        assert c_view.ctypes.data - C.ctypes.data == row0 * C.shape[-1] * C.itemsize
+
+
 # ------------------------------------------------------------- gloo ranks
 
 def _free_port():
