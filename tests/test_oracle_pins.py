@@ -414,13 +414,25 @@ def test_tolerance_formula():
     np.testing.assert_array_equal(tau, [1e-3 + 2.0 ** -7, 1e-4 + 2.0 ** -6, 2.0 ** -133])
 
 
-def test_sample_matches_full():
-    inp = _small(16, a="e5m2", b="e4m3", M=130, N=70, K=96)
-    p = inp.problem
+SAMPLE_CASES = [
+    synth.Problem(130, 70, 96, 2, "e5m2", "e4m3", 32, "f32", "n"),
+    synth.Problem(144, 80, 72, 2, "e4m3", "e5m2", 32, "f32", "n", a_major="m", b_major="n"),
+    synth.Problem(48, 136, 64, 1, "e4m3", "e4m3", 32, "f32", "n", a_major="m"),
+    synth.Problem(130, 70, 96, 2, "e2m1", "e2m1", 16, "f32", "n", sf_dtype="e4m3"),
+]
+
+
+@pytest.mark.parametrize("p", SAMPLE_CASES, ids=lambda p: f"{p.a_dtype}-{p.a_major}{p.b_major}-{p.sf_dtype}")
+def test_sample_matches_full(p):
+    """The point-by-point form gives the full form's sums bit for bit, for
+    every operand layout and scale type the full form takes."""
+    lo, hi = (0x30, 0x40) if p.sf_dtype == "e4m3" else (124, 130)
+    inp = synth.uniform_codes(p, 16, lo, hi)
     C, S, _ = run_oracle(inp)
     pts = synth.sample_points(p, 300, 1)
     c, s = oracle.gemm_sample(p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv, inp.A, inp.B,
-                              inp.SFA, inp.SFB, pts)
+                              inp.SFA, inp.SFB, pts, sf_dtype=p.sf_dtype, a_major=p.a_major,
+                              b_major=p.b_major)
     np.testing.assert_array_equal(c, C[pts[:, 2], pts[:, 0], pts[:, 1]])
     np.testing.assert_array_equal(s, S[pts[:, 2], pts[:, 0], pts[:, 1]])
 
