@@ -148,9 +148,10 @@ bsg_status bsg_workspace_init(const bsg_plan *plan, void *workspace, size_t ws_b
 /* One launch of the GEMM + Amax on `stream` (a cudaStream_t; NULL is the
  * legacy default stream) -- the analogue of execute() ("Class API").
  * A, B, SFA, SFB, C, amax and workspace are device pointers of the plan's
- * device.  Checks pointers, alignment and the workspace size, then launches
- * exactly one kernel.  Allocates nothing, never synchronises.  Runs sharing
- * one workspace must not overlap on the device. */
+ * device, which must be the calling thread's current device
+ * (BSG_ERR_INVALID_ARG otherwise).  Checks pointers, alignment and the
+ * workspace size, then launches exactly one kernel.  Allocates nothing, never
+ * synchronises.  Runs sharing one workspace must not overlap on the device. */
 bsg_status bsg_run(const bsg_plan *plan, const void *A, const void *B, const void *SFA,
                    const void *SFB, void *C, float *amax, void *workspace, size_t ws_bytes,
                    void *stream);
