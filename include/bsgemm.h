@@ -52,9 +52,10 @@
  * only.  Rows of A, B and C must be 16-byte aligned along their contiguous
  * dimension (K bytes of a k-major operand, M or N bytes of an MN-major one,
  * an E2M1 C row of N/2 bytes with N even), every pointer 16-byte aligned.
- * Everything else returns BSG_ERR_UNSUPPORTED or BSG_ERR_INVALID_ARG before
- * any launch (errors are reported before launch, as "Grouped GEMM (SM100
- * BF16)", "Scheduling, caching, and errors", does).
+ * M, N, K and L are at least 1 (an empty problem is BSG_ERR_INVALID_ARG)
+ * and below 2^31.  Everything else returns BSG_ERR_UNSUPPORTED or
+ * BSG_ERR_INVALID_ARG before any launch (errors are reported before launch,
+ * as "Grouped GEMM (SM100 BF16)", "Scheduling, caching, and errors", does).
  *
  * Ownership: the caller owns every device buffer (A, B, SFA, SFB, C, Amax,
  * workspace).  A plan owns host memory only.  No entry point allocates
