@@ -4,9 +4,7 @@ waits run out; the kernel records it in the workspace error word, abandons
 its pipeline, drains its own copies and MMAs, frees tensor memory and
 returns.  The host reads BSG_ERR_DEVICE_TIMEOUT, and the same context then
 runs a normal plan correctly."""
-import os
 
-import numpy as np
 import pytest
 import torch
 

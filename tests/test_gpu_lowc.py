@@ -6,7 +6,6 @@ result rounded to nearest even with saturation; the oracle rounds its double
 sum the same way and the per-element bound |C_gpu - C_ref| <= 1e-5 S + ulp_c
 (one step of the output format) covers a sum that lands on the other side of
 a rounding boundary.  Amax is max |stored C|, bit for bit."""
-import numpy as np
 import pytest
 
 import block_scaled_precision_04_gb300 as bsg
