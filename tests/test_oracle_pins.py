@@ -135,6 +135,27 @@ def test_unit_scales_reduce_to_plain_gemm():
     np.testing.assert_array_equal(C, plain)
 
 
+def test_the_pages_usage_example():
+    """The example of "GEMM + Amax (SM100)", section "Using JAX arrays": m=512,
+    n=256, k=256, sf_vec_size 32, E5M2 operands made by casting standard
+    normal draws (here torch's float8_e5m2 cast of a seeded draw), every scale
+    1.0 (E8M0 byte 127) in the physical atom shape (1, m/128, k/128, 32, 4, 4),
+    fp32 C.  With unit scales the result is the plain product of the decoded
+    operands; E5M2 products and their 256-term sums are exact in double, so
+    the two agree bit for bit."""
+    m, n, k, sfv = 512, 256, 256, 32
+    g = torch.Generator().manual_seed(512)
+    A = torch.randn(1, m, k, generator=g).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    B = torch.randn(1, n, k, generator=g).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    SFA = np.full((1, m // 128, k // (4 * sfv), 32, 4, 4), 127, dtype=np.uint8)
+    SFB = np.full((1, n // 128, k // (4 * sfv), 32, 4, 4), 127, dtype=np.uint8)
+    C, _, _ = oracle.gemm(m, n, k, 1, "e5m2", "e5m2", sfv, A, B, SFA, SFB)
+    a, b = lib_decode(A, "e5m2")[0], lib_decode(B, "e5m2")[0]
+    np.testing.assert_array_equal(C[0], a @ b.T)
+    ref = oracle.reference(m, n, k, 1, "e5m2", "e5m2", sfv, A, B, SFA, SFB, "f32")
+    assert ref["amax"] == np.abs(np.float32(a @ b.T)).max()
+
+
 def test_one_scale_step_doubles_exactly_one_block():
     """Raising one scale byte by one doubles exactly that (row, K-block)
     term: C' - C equals the block's partial dot product (to double rounding)."""
