@@ -85,3 +85,21 @@ def test_reference_arm_prints_one_contract_line(args):
     assert d["metric"] == (bench.QMETRIC if "quantize" in args else bench.METRIC)
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_traffic_key_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    """The ncu traffic reported in the roofline is keyed by a hash of the
+    kernel source without comments and whitespace: editing a comment keeps the
+    captured counters valid, changing code makes the lookup miss (null)."""
+    src = os.path.join(bench.ROOT, "block_scaled_precision_04_gb300", "csrc", "bsgemm.cu")
+    text = open(src).read()
+    csrc = tmp_path / "block_scaled_precision_04_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (csrc / "bsgemm.cu").write_text(text)
+    h0 = bench.kernel_source_hash()
+    (csrc / "bsgemm.cu").write_text("// a new comment\n" + text.replace("\n", "\n  ", 3))
+    assert bench.kernel_source_hash() == h0
+    (csrc / "bsgemm.cu").write_text(text.replace("kRnd = 4", "kRnd = 2", 1))
+    assert bench.kernel_source_hash() != h0
+    assert all(len(k[0]) == 16 for k in bench.TRAFFIC)
