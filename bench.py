@@ -334,7 +334,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": f"{p.a_dtype}x{p.b_dtype} codes, e8m0 scales, fp32 accumulate",
+            "dtype": f"{p.a_dtype}x{p.b_dtype} codes, "
+                     f"{'e8m0' if p.sf_dtype == 'ue8m0' else p.sf_dtype} scales, fp32 accumulate",
             "data": "synthetic (seeded; see synth)", "config": config_of(args.workload, p, name),
             "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps,
             "clocks": clk.summary(), "wall_s_timed_region": round(wall, 4),
