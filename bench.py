@@ -135,6 +135,21 @@ def config_of(number: int, p: synth.Problem, name: str) -> dict:
             "l2": L2_NOTE}
 
 
+def host_cost_us(launch, torch, dev, n: int = 200):
+    """Host time of one launch through the Python binding (argument
+    marshalling, the C ABI's checks and the kernel launch), outside the timed
+    region: the wall time of a burst of n launches enqueued without waiting,
+    per launch.  The class API of the pages is quoted at ~15 us of CPU per
+    launch ("GEMM + Amax (SM100)", "Using JAX arrays")."""
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        launch()
+    us = (time.perf_counter() - t0) / n * 1e6
+    torch.cuda.synchronize(dev)
+    return round(us, 2)
+
+
 # ------------------------------------------------------------ CPU oracle leg
 
 def oracle_sample(inp, target_s: float, max_rows: int | None = None):
@@ -288,6 +303,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     total_ms = max_over_ranks(sum(times_ms), dist, dev)
     ms = total_ms / args.steps
     value = whole_job_tflops(nums["flops"], args.steps, world, total_ms)
+    host_us = host_cost_us(launch, torch, dev)
+    bsg.check(op.device_status(), "device status (host-cost burst)")
 
     # end to end through the C ABI with host buffers (pinned), copies included
     e2e = None
@@ -339,6 +356,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "data": "synthetic (seeded; see synth)", "config": config_of(args.workload, p, name),
             "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps,
             "clocks": clk.summary(), "wall_s_timed_region": round(wall, 4),
+            "host_us_per_launch": host_us,
             "plan": {k: info[k] for k in ("tile_m", "tile_n", "stages", "grid", "smem_bytes",
                                           "num_tiles")},
             "step_ms_min": round(min(times_ms), 5), "step_ms_median": round(statistics.median(times_ms), 5)}

@@ -103,3 +103,14 @@ def test_traffic_key_ignores_comments_but_not_code(tmp_path, monkeypatch):
     (csrc / "bsgemm.cu").write_text(text.replace("kRnd = 4", "kRnd = 2", 1))
     assert bench.kernel_source_hash() != h0
     assert all(len(k[0]) == 16 for k in bench.TRAFFIC)
+
+
+def test_host_cost_is_a_burst_of_launches():
+    """The host cost per launch is the wall time of n launches enqueued back
+    to back, divided by n, with the device synchronised on both sides."""
+    import types
+    calls, syncs = [], []
+    fake_torch = types.SimpleNamespace(cuda=types.SimpleNamespace(synchronize=lambda d: syncs.append(d)))
+    us = bench.host_cost_us(lambda: calls.append(1), fake_torch, "dev", n=50)
+    assert len(calls) == 50 and syncs == ["dev", "dev"]
+    assert isinstance(us, float) and 0.0 <= us < 1e4
