@@ -279,3 +279,38 @@ def test_c_ulp(dtype, spacing_at_1, emax):
         if lo >= 2.0 ** (emax - 3):   # normal range: the spacing right above lo
             assert oracle.ulp(lo, dtype) == hi - lo or lo >= 2.0 ** emax
     assert oracle.ulp(tab[-1] * 4, dtype) == oracle.ulp(tab[-1], dtype)
+
+
+# per-element error of one MX quantisation, from the formats alone: at most
+# REL |x| (saturation of the top binade, or half a step relative to the value)
+# plus ABS 2^e (half the subnormal step, in the block's scale 2^e)
+ERR = {"e4m3": (0.125, 2.0 ** -10), "e5m2": (0.125, 2.0 ** -17), "e2m1": (0.25, 0.25)}
+
+
+@pytest.mark.parametrize("dtype,sfv", [("e4m3", 32), ("e5m2", 32), ("e2m1", 32), ("e2m1", 16)])
+def test_quantize_then_gemm_within_the_formats_error(dtype, sfv):
+    """The quantizer's codes and scale atoms, read back by the GEMM oracle,
+    give the product of the original real matrices within the error the two
+    quantisations allow: |C - A B^T| <= sum_k |a| eb + ea |b| + ea eb, with
+    e = REL |x| + ABS 2^(floor(log2 blockmax) - emax).  A scale written to the
+    wrong atom position, row or K block, or a wrong binade, breaks it."""
+    M, N, K, L = 200, 136, 384, 2
+    A = synth.real_blocks(L, M, K, seed=41, block=sfv).astype(np.float64)
+    B = synth.real_blocks(L, N, K, seed=42, block=sfv).astype(np.float64)
+    qa, sa = oracle.quantize(A, dtype, sfv)
+    qb, sb = oracle.quantize(B, dtype, sfv)
+    C, _, _ = oracle.gemm(M, N, K, L, dtype, dtype, sfv, qa, qb, sa, sb)
+    rel, ab = ERR[dtype]
+
+    def err(X):
+        bm = np.abs(X).reshape(L, X.shape[1], K // sfv, sfv).max(axis=-1, keepdims=True)
+        unit = np.where(bm > 0, 2.0 ** (np.floor(np.log2(np.where(bm > 0, bm, 1.0))) - EMAX[dtype]), 0.0)
+        return (rel * np.abs(X).reshape(bm.shape[:-1] + (sfv,)) + ab * unit).reshape(X.shape)
+
+    ea, eb = err(A), err(B)
+    exact = np.einsum("lmk,lnk->lmn", A, B)
+    bound = (np.einsum("lmk,lnk->lmn", np.abs(A), eb) + np.einsum("lmk,lnk->lmn", ea, np.abs(B)) +
+             np.einsum("lmk,lnk->lmn", ea, eb))
+    assert np.all(np.abs(C - exact) <= bound * (1 + 1e-12) + 1e-300)
+    # and the bound is not vacuous: the quantised product is close in bulk
+    assert np.median(np.abs(C - exact) / np.maximum(bound, 1e-300)) < 0.5
