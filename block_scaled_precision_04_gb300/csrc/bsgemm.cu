@@ -149,17 +149,6 @@ __device__ __forceinline__ void tma_load_3d_to_leader(uint32_t dst, const CUtens
       : "memory");
 }
 
-// The same box into the same smem offset of every CTA in `mask`; each
-// destination CTA's mbarrier at `bar`'s offset receives the bytes it got.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                               int z, uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(mask)
-      : "memory");
-}
-
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -192,17 +181,6 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
 }
-
-// Arrive on the mbarrier at `bar`'s offset in every CTA of `mask` once
-// this thread's earlier tcgen05 operations complete.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
-
 
 // cta_group::2 forms: issued by the leader CTA of a pair, acting on both CTAs
 __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
@@ -539,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kAStage = kASlice * KSL;            // smem bytes per stage
   // PAIR: a 2-CTA pair runs 256 x TILE_N MMAs (cta_group::2); each CTA holds
   // its 128 rows of A and half (TILE_N/2 rows) of the B tile
-  static_assert(!PAIR || CM == 2, "a CTA pair is a cluster of two");
+  static_assert((CM == 1 && !PAIR) || (CM == 2 && PAIR), "a CTA alone or a cta_group::2 pair");
   constexpr int kBRows = PAIR ? TILE_N / 2 : TILE_N;
   // B is loaded in boxes of whole 128-row groups: a 112-row box (a 224-wide
   // pair's half) streams markedly slower through the TMA unit, so the half
@@ -555,10 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kSfCol0 = NUM_ACC * TILE_N;
   constexpr int kMmasPerStage = kSB / kMmaKBytes;
   constexpr int kMmasPerSlice = kStageKBytes / kMmaKBytes;
-  // B tile shared by the cluster's CM CTAs: each loads TILE_N / CM rows and
-  // multicasts them to all
-  constexpr int kBPartRows = PAIR ? kBRows : TILE_N / CM;
-  constexpr uint32_t kBPart = kBPartRows * kStageKBytes;
+  // both CTAs of a pair: the targets of the leader's commit arrivals
   constexpr uint16_t kMask = static_cast<uint16_t>((1u << CM) - 1u);
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -593,9 +568,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the producer's expect_tx and the four scale warps (of both CTAs of a
       // pair; only the leader's barrier is used then)
       mbar_init(full0 + 8u * s, 1 + (PAIR ? 8 : 4));
-      // freed by the MMA commit of every CTA of a multicast cluster, or by the
-      // single (multicast) commit of a pair's leader
-      mbar_init(empty0 + 8u * s, PAIR ? 1 : CM);
+      // freed by the MMA commit (in a pair, the leader's commit arrives in
+      // both CTAs)
+      mbar_init(empty0 + 8u * s, 1);
       mbar_init(sff0 + 8u * s, 1);
     }
     for (int b = 0; b < NUM_ACC; ++b) {
@@ -633,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (CM > 1) cluster_sync();  // peers' barriers initialised before any multicast
+  if (CM > 1) cluster_sync();  // the peer's barriers initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
@@ -691,12 +666,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int kx = ks * kSB + sl * kStageKBytes;
               tma_load_3d(a_dst0 + stage * kAStage + sl * kASlice, &tmap_a, a_mn ? m0 : kx,
                           a_mn ? kx : m0, tc.l, bar);
-              const uint32_t bdst = b_dst0 + stage * kBStage + sl * kBSlice;
-              if (CM == 1 || PAIR)
-                tma_load_3d(bdst, &tmap_b, b_mn ? n0 : kx, b_mn ? kx : n0, tc.l, bar);
-              else  // k-major B only (the host rejects MN-major B here)
-                tma_load_3d_mc(bdst + crank * kBPart, &tmap_b, kx, n0 + crank * kBPartRows, tc.l,
-                               bar, kMask);
+              tma_load_3d(b_dst0 + stage * kBStage + sl * kBSlice, &tmap_b, b_mn ? n0 : kx,
+                          b_mn ? kx : n0, tc.l, bar);
             }
           }
           if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -769,12 +740,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         (j != 0 || ks != 0) ? 1u : 0u);
             }
           }
-          // frees the smem stage (in every CTA of the cluster) once these MMAs
+          // frees the smem stage (in both CTAs of a pair) once these MMAs
           // finish; issued at once, since the ring is latency-bound and every
           // cycle of delay here delays the stage's refill
           if (PAIR) tc_commit_pair_mc(empty0 + 8u * stage, kMask);
-          else if (CM == 1) tc_commit(empty0 + 8u * stage);
-          else tc_commit_mc(empty0 + 8u * stage, kMask);
+          else tc_commit(empty0 + 8u * stage);
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
@@ -1146,7 +1116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (CM > 1) cluster_sync();  // no peer multicasts or arrives into this CTA any more
+  if (CM > 1) cluster_sync();  // the peer arrives into this CTA no more
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
@@ -1177,7 +1147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #undef BSG_WAIT_SLEEP
 
 // Kernel variants: MMA kind x (TILE_N, accumulator buffers) x cluster along M
-// (cm 1 alone, 2 a cta_group::2 pair, 4 a quad multicasting the B tile)
+// (cm 1: a CTA alone; 2: a cta_group::2 pair)
 struct Variant {
   int kind, tile_n, num_acc, cm, pair, kslices;
   const void* fn;
@@ -1194,7 +1164,6 @@ void add_kind(Variant* out, int& n) {
   out[n++] = make_variant<KIND, 128, 2, 1, 0>();
   out[n++] = make_variant<KIND, 256, 1, 1, 0>();
   out[n++] = make_variant<KIND, 256, 1, 2, 1>();
-  out[n++] = make_variant<KIND, 256, 1, 4, 0>();
 }
 
 const Variant* find_variant(int kind, int tile_n, int num_acc, int cm, int kslices) {
@@ -1263,7 +1232,7 @@ struct bsg_plan {
   const void* kernel;    // the chosen kernel variant
   int kind;
   int num_acc;
-  int cluster_m;         // CTAs per cluster along M sharing the B tile
+  int cluster_m;         // CTAs per cluster along M: 1, or 2 for a cta_group::2 pair
   int kslices;           // 128-byte K slices per pipeline stage
   int pair;              // 1: the cluster is a cta_group::2 pair (256-row MMAs)
   int grid;
@@ -1331,11 +1300,13 @@ bsg_status bsg_problem_check(const bsg_problem* p) {
   const int cl[2] = {p->cluster_m, p->cluster_n};
   for (int c : cl)
     if (c != 0 && c != 1 && c != 2 && c != 4) return BSG_ERR_INVALID_ARG;
+  // clusters: one CTA, or a cta_group::2 pair along M.  Larger clusters (the
+  // page's cluster shapes that share a tile between CTAs by multicast) and
+  // clusters along N are not built.
+  if (p->cluster_m == 4 || p->cluster_n > 1) return BSG_ERR_UNSUPPORTED;
   // an n-major B tile is loaded whole by one CTA (single 128-wide tiles) or
-  // in halves by a CTA pair; B split over a cluster of four, or 256 columns
-  // in one CTA, are k-major only
-  if (b_mn && (p->cluster_m == 4 || (p->cluster_m == 1 && p->tile_n > 128)))
-    return BSG_ERR_UNSUPPORTED;
+  // in halves by a CTA pair; 256 columns in one CTA are k-major only
+  if (b_mn && p->cluster_m == 1 && p->tile_n > 128) return BSG_ERR_UNSUPPORTED;
   const int64_t row_bytes = a4 ? p->K / 2 : p->K;
   if (a4 && (p->K % 2)) return BSG_ERR_ALIGNMENT;
   // the contiguous extent of each operand: K bytes, or M (N) bytes per K
@@ -1405,8 +1376,7 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   }
   int num_acc = k.tile_n == 256 ? 1 : 2;
   // 224- and 256-wide tiles run as cta_group::2 pairs by default (hint 1:
-  // single CTAs, 4: clusters of four multicasting the B tile; 224 is pairs
-  // only); the 128-wide variant runs alone
+  // single CTAs; 224 is pairs only); the 128-wide variant runs alone
   int cm = 1;
   if (k.tile_n == 256) cm = prob->cluster_m == 0 ? 2 : prob->cluster_m;
   if (k.tile_n == 224) cm = 2;
@@ -1418,7 +1388,6 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
     k.tile_n = 128;
     num_acc = 2;
   }
-  if (b_mn && cm > 2) { delete plan; return BSG_ERR_UNSUPPORTED; }
   // FP8 pairs with 256-wide tiles take 256-byte K stages (8 MMAs per
   // barrier check); each CTA's half tiles keep three such stages in smem
   const int ksl = kind == kKindF8F6F4 && k.tile_n == 256 && cm == 2 ? 2 : 1;
@@ -1591,18 +1560,36 @@ static bool encode_scales(CUtensorMap* map, const void* ptr, int64_t t_k, int64_
   return r == CUDA_SUCCESS;
 }
 
-bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const void* SFA,
-                   const void* SFB, void* C, float* amax, void* ws, size_t ws_bytes,
-                   void* stream) {
-  if (!cplan || !A || !B || !SFA || !SFB || !C || !amax) return BSG_ERR_INVALID_ARG;
-  if (!ws || ws_bytes < kWorkspaceBytes || !aligned16(ws)) return BSG_ERR_WORKSPACE;
+}  // extern "C"
+
+namespace {
+
+// The checks bsg_run makes on its tensor arguments before anything is
+// enqueued: pointers present and aligned, and the plan's device current.
+bsg_status check_run_args(const bsg_plan* plan, const void* A, const void* B, const void* SFA,
+                          const void* SFB, const void* C, const float* amax) {
+  if (!plan || !A || !B || !SFA || !SFB || !C || !amax) return BSG_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(SFA) || !aligned16(SFB) || !aligned16(C) ||
       (reinterpret_cast<uintptr_t>(amax) & 3u))
     return BSG_ERR_ALIGNMENT;
-  bsg_plan* plan = const_cast<bsg_plan*>(cplan);
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return BSG_ERR_CUDA; }
   if (dev != plan->device) return BSG_ERR_INVALID_ARG;
+  return BSG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const void* SFA,
+                   const void* SFB, void* C, float* amax, void* ws, size_t ws_bytes,
+                   void* stream) {
+  if (!cplan) return BSG_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < kWorkspaceBytes || !aligned16(ws)) return BSG_ERR_WORKSPACE;
+  const bsg_status arg_st = check_run_args(cplan, A, B, SFA, SFB, C, amax);
+  if (arg_st != BSG_OK) return arg_st;
+  bsg_plan* plan = const_cast<bsg_plan*>(cplan);
   const bsg_problem& pr = plan->prob;
   const int64_t row_bytes = plan->base.k_bytes;
   Params k = plan->base;
@@ -1622,7 +1609,7 @@ bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const vo
       plan->map_a_ptr = A;
     }
     if (plan->map_b_ptr != B) {
-      const int b_box = plan->pair ? (k.tile_n / 2 + 127) / 128 * 128 : k.tile_n / plan->cluster_m;
+      const int b_box = plan->pair ? (k.tile_n / 2 + 127) / 128 * 128 : k.tile_n;
       if (!encode_operand(&plan->map_b, B, row_bytes, pr.N, pr.L, b_box, k.b_mn != 0)) {
         plan->map_b_ptr = nullptr;
         return BSG_ERR_CUDA;
@@ -1683,9 +1670,10 @@ bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const vo
 // rejected with BSG_ERR_WORKSPACE.
 static constexpr size_t kNoAllocScratchBytes = 4096;
 
-// Loaded (zero-filled) on every GPU that loads this library, held until exit.
-// Host code must not hand this name to a kernel: on the host it is only a
-// stand-in; the device address comes from cudaGetSymbolAddress below.
+// Loaded (zero, having no initialiser) on every GPU that loads this library,
+// held until exit.  Host code must not hand this name to a kernel: on the
+// host it is only a stand-in; the device address comes from
+// cudaGetSymbolAddress below.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 static constexpr int kNoAllocMaxDevices = 64;
@@ -1693,18 +1681,15 @@ static std::mutex g_noalloc_mu;
 static void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
 
 // Device address of the array on the current device, looked up once per
-// device (the first call on a device; it also zero-fills the array,
-// synchronously).
+// device (the first call on a device).  Nothing is written here: the array
+// is zero when the module loads, and every call clears the words a run
+// reads on its own stream.
 static bsg_status noalloc_scratch(int device, void** out) {
   if (device < 0 || device >= kNoAllocMaxDevices) return BSG_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (!g_noalloc_ptr[device]) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
-      cudaGetLastError();
-      return BSG_ERR_CUDA;
-    }
-    if (cudaMemset(ptr, 0, kNoAllocScratchBytes) != cudaSuccess) {
       cudaGetLastError();
       return BSG_ERR_CUDA;
     }
@@ -1721,10 +1706,12 @@ bsg_status bsg_run_noalloc(const bsg_plan* plan, const void* A, const void* B, c
   bsg_status st = bsg_plan_workspace_size(plan, &need);
   if (st != BSG_OK) return st;
   if (need > kNoAllocScratchBytes) return BSG_ERR_WORKSPACE;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return BSG_ERR_CUDA; }
+  // the checks bsg_run makes, before the array is looked up or cleared, so
+  // that a bad pointer or the wrong current device touches no device state
+  st = check_run_args(plan, A, B, SFA, SFB, C, amax);
+  if (st != BSG_OK) return st;
   void* scratch = nullptr;
-  st = noalloc_scratch(dev, &scratch);
+  st = noalloc_scratch(plan->device, &scratch);
   if (st != BSG_OK) return st;
   // the array keeps the previous call's words: clear the Amax slot, the
   // arrival counter and the error word before this launch

@@ -45,7 +45,7 @@
  *
  * Support ("Support surface and constraints"): A/B k-major, or m-major A /
  * n-major B for FP8 (M, N a multiple of 16; an n-major B runs on CTA pairs
- * or 128-wide tiles, not on clusters of four or one 256-wide CTA); A/B both FP8
+ * or 128-wide tiles, not on one 256-wide CTA); A/B both FP8
  * (E4M3/E5M2, each on its own) with sf_vec_size 32 and E8M0 scales, or both
  * E2M1 with sf_vec_size 32 and E8M0 scales or sf_vec_size 16 and E8M0 or
  * E4M3 scales; C fp32/fp16/bf16 always, E4M3/E5M2/E2M1 with E2M1 operands
@@ -94,11 +94,14 @@ typedef enum {
 } bsg_dtype;
 
 /* Problem statement, after the page's constructor arguments ("Common
- * parameters", "Class-specific parameters").  tile_* and cluster_* are
- * hints only: 0 lets the library choose; otherwise tile_m must be 128,
- * tile_n 128, 224 or 256 (224: FP8 operands and M > 128 only, else
- * BSG_ERR_UNSUPPORTED), cluster_* 1, 2 or 4 (cluster_m 2 is a pair of CTAs
- * running 256-row MMAs, the default for tile_n 224 and 256). */
+ * parameters", "Class-specific parameters": mma_tiler_mn, cluster_shape_mn).
+ * tile_* and cluster_* are hints only: 0 lets the library choose; otherwise
+ * tile_m must be 128, tile_n 128, 224 or 256 (224: FP8 operands and M > 128
+ * only, else BSG_ERR_UNSUPPORTED), cluster_m 1 or 2 (2 is a pair of CTAs
+ * running 256-row MMAs, the default for tile_n 224 and 256) and cluster_n 1.
+ * cluster_m 4 and cluster_n 2 or 4 (shapes whose CTAs would share a tile by
+ * multicast) are accepted values that this library does not build:
+ * BSG_ERR_UNSUPPORTED; any other value is BSG_ERR_INVALID_ARG. */
 typedef struct {
     int64_t M, N, K, L;
     int32_t a_dtype, b_dtype;   /* bsg_dtype */
@@ -123,7 +126,7 @@ typedef struct {
     int32_t smem_bytes;                    /* dynamic shared memory per CTA */
     int32_t num_tiles;                     /* output tiles per launch */
     int32_t mma_kind;                      /* 0 mxf8f6f4 1X, 1 mxf4nvf4 4X, 2 mxf4nvf4 2X */
-    int32_t cluster_m;                     /* CTAs per cluster sharing one B tile */
+    int32_t cluster_m;                     /* 1: CTAs alone; 2: cta_group::2 pairs */
     char kernel_name[64];
 } bsg_plan_info;
 
@@ -138,11 +141,15 @@ bsg_status bsg_problem_check(const bsg_problem *problem);
 bsg_status bsg_plan_create(const bsg_problem *problem, int device, bsg_plan **out);
 
 /* Bytes of device workspace a run of this plan needs (a small fixed
- * amount: a cross-CTA amax slot, an arrival counter and an error word). */
+ * amount: a cross-CTA amax slot, an arrival counter and an error word).
+ * The workspace lives in the caller's allocator, as the workspaces of
+ * "Grouped GEMM (SM100 BF16)", section "Using JAX arrays", do. */
 bsg_status bsg_plan_workspace_size(const bsg_plan *plan, size_t *bytes);
 
 /* Zero a workspace on `stream` (cudaMemsetAsync).  Must be called once
- * before a workspace is first used; every run leaves it zeroed again. */
+ * before a workspace is first used; every run leaves it zeroed again
+ * (caller-allocator workspaces: "Grouped GEMM (SM100 BF16)", "Using JAX
+ * arrays"). */
 bsg_status bsg_workspace_init(const bsg_plan *plan, void *workspace, size_t ws_bytes,
                               void *stream);
 
@@ -162,10 +169,14 @@ bsg_status bsg_run(const bsg_plan *plan, const void *A, const void *B, const voi
  * cudaMalloc is not permitted).  The pages have no counterpart: it is a
  * convenience of this library.  The workspace comes from a fixed array
  * inside the library (4096 bytes on every GPU that loads it, kept until the
- * process exits); a plan needing more returns BSG_ERR_WORKSPACE.  The first
- * call on a device looks the array up and zero-fills it synchronously, so
- * make that first call before any stream capture.  Each call clears the
- * array's first 16 bytes on `stream`, then launches exactly as bsg_run.  All
+ * process exits; zero when the library is loaded); a plan needing more
+ * returns BSG_ERR_WORKSPACE.  The arguments are checked first, exactly as
+ * bsg_run checks them, so a bad pointer or the wrong current device returns
+ * its status before anything is enqueued.  The first call on a device then
+ * looks up the array's device address (cudaGetSymbolAddress, host side
+ * only), so make that first call before any stream capture.  Each call
+ * clears the array's first 16 bytes with cudaMemsetAsync on `stream`, then
+ * launches exactly as bsg_run.  All
  * calls share the one array: calls that overlap on the device race and
  * give wrong results.  A device-side wait timeout is not reported here (use
  * bsg_run with a workspace and bsg_check_device_status for that).  Nothing
@@ -181,7 +192,9 @@ typedef struct {
     size_t ws_bytes;
 } bsg_device_buffers;
 
-/* End-to-end form of bsg_run over HOST buffers (preferably pinned): copies
+/* End-to-end form of bsg_run over HOST buffers (preferably pinned).  The
+ * pages have no counterpart; it is this library's own, the form the
+ * end-to-end measurement uses.  It copies
  * hA, hB, hSFA, hSFB to the device buffers, runs, and copies C and Amax back
  * to hC and h_amax, all enqueued on `stream` (one cudaMemcpyAsync per
  * tensor).  Asynchronous like bsg_run: synchronise the stream before reading
@@ -192,16 +205,20 @@ bsg_status bsg_run_host(const bsg_plan *plan, const void *hA, const void *hB, co
 
 /* Synchronise `stream`, then read and clear the workspace's device error
  * word.  Returns BSG_ERR_DEVICE_TIMEOUT if a kernel of an earlier run gave
- * up on a pipeline wait (its outputs are then invalid), else BSG_OK. */
+ * up on a pipeline wait (its outputs are then invalid), else BSG_OK.  The
+ * pages have no counterpart: the bounded waits and their error word are
+ * this library's own. */
 bsg_status bsg_check_device_status(const bsg_plan *plan, void *workspace, void *stream);
 
-/* Fill *info with the plan's choices. */
+/* Fill *info with the plan's choices (this library's own; no page
+ * counterpart). */
 bsg_status bsg_plan_describe(const bsg_plan *plan, bsg_plan_info *info);
 
-/* Free a plan (host memory only).  NULL is ignored. */
+/* Free a plan (host memory only).  NULL is ignored.  The class API's
+ * object lifetime ("Class API") in C form. */
 void bsg_plan_destroy(bsg_plan *plan);
 
-/* Static text for a status code. */
+/* Static text for a status code (this library's own). */
 const char *bsg_status_string(bsg_status status);
 
 #ifdef __cplusplus

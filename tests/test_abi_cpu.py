@@ -107,7 +107,7 @@ OK_CASES = [
     dict(M=8, N=16, K=64, L=1, b_major="n", a_dtype="e5m2"),
     dict(M=256, N=512, K=256, L=1, b_major="n", tile_n=256, cluster_m=2),
     dict(M=256, N=512, K=256, L=1, b_major="n", tile_n=128),
-    dict(M=256, N=512, K=256, L=1, a_major="m", tile_n=256, cluster_m=4),
+    dict(M=256, N=512, K=256, L=1, a_major="m", tile_n=256, cluster_m=1),
 ]
 
 
@@ -152,8 +152,12 @@ BAD_CASES = [
     (dict(M=16, N=16, K=32, L=1, b_major="m"), bsg.BSG_ERR_INVALID_ARG, "B m-major"),
     (dict(M=16, N=16, K=64, L=1, a_dtype="e2m1", b_dtype="e2m1", sf_vec_size=16, a_major="m"),
      bsg.BSG_ERR_UNSUPPORTED, "FP4 m-major"),
-    (dict(M=256, N=512, K=256, L=1, b_major="n", tile_n=256, cluster_m=4),
-     bsg.BSG_ERR_UNSUPPORTED, "n-major B over a cluster of four"),
+    (dict(M=256, N=512, K=256, L=1, tile_n=256, cluster_m=4),
+     bsg.BSG_ERR_UNSUPPORTED, "cluster of four (tiles shared by multicast) not built"),
+    (dict(M=256, N=512, K=256, L=1, a_major="m", tile_n=256, cluster_m=4),
+     bsg.BSG_ERR_UNSUPPORTED, "cluster of four, m-major A"),
+    (dict(M=256, N=512, K=256, L=1, cluster_n=2), bsg.BSG_ERR_UNSUPPORTED, "cluster along N"),
+    (dict(M=256, N=512, K=256, L=1, cluster_n=4), bsg.BSG_ERR_UNSUPPORTED, "cluster of 4 along N"),
     (dict(M=256, N=512, K=256, L=1, b_major="n", tile_n=256, cluster_m=1),
      bsg.BSG_ERR_UNSUPPORTED, "n-major B 256 wide in one CTA"),
     (dict(M=4, N=4, K=32, L=1, a_major="x"), bsg.BSG_ERR_INVALID_ARG, "bad major"),

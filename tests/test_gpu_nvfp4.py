@@ -51,7 +51,7 @@ def test_e4m3_scales(p, lo, hi):
     assert_parity(inp, c, amax)
 
 
-@pytest.mark.parametrize("tile_n,cluster_m", [(128, 0), (256, 1), (256, 2), (256, 4)])
+@pytest.mark.parametrize("tile_n,cluster_m", [(128, 0), (256, 1), (256, 2)])
 def test_e4m3_scales_tiles(tile_n, cluster_m):
     """Every tile width and cluster shape of the FP4 kernel, with the pipeline
     ring and the accumulator hand-off wrapping."""

@@ -264,13 +264,12 @@ CLUSTER_CASES = [
 ]
 
 
-@pytest.mark.parametrize("cluster_m", [1, 2, 4])
+@pytest.mark.parametrize("cluster_m", [1, 2])
 @pytest.mark.parametrize("p", CLUSTER_CASES, ids=[f"{p.M}x{p.N}x{p.K}L{p.L}{p.a_dtype}sfv{p.sfv}{p.c_major}" for p in CLUSTER_CASES])
-def test_cluster_multicast(p, cluster_m):
-    """Single CTAs (cluster 1), a cta_group::2 pair (cluster 2, the default:
-    256-row MMAs, each CTA holding half the
-    B tile) or a cluster of 4 CTAs sharing each B tile by TMA multicast;
-    M-tile counts that do not divide by the cluster give ghost tiles."""
+def test_cluster_shapes(p, cluster_m):
+    """Single CTAs (cluster 1) or a cta_group::2 pair (cluster 2, the
+    default: 256-row MMAs, each CTA holding half the B tile); M-tile counts
+    that do not divide by two give a ghost tile in the last pair."""
     inp = synth.uniform_codes(p, p.M * 3 + p.N + p.K + cluster_m, 123, 131)
     c, amax, _, op, guard_ok = run_gpu(inp, guard=4096, tile_n=256, cluster_m=cluster_m)
     info = op.describe()

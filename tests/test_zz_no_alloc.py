@@ -35,11 +35,12 @@ def _run_both(inp):
     a_new = torch.full((1,), -1.0, device="cuda:0")
     s = torch.cuda.current_stream().cuda_stream
     op.run(A, B, SFA, SFB, c_ref, a_ref)
+    # the reference launch's own workspace: its pipeline waits all completed
+    assert op.device_status() == bsg.BSG_OK
     st = bsg.bsg_run_noalloc(op.plan, A.data_ptr(), B.data_ptr(), SFA.data_ptr(), SFB.data_ptr(),
                              c_new.data_ptr(), a_new.data_ptr(), s)
     assert st == bsg.BSG_OK, bsg.bsg_status_string(st)
     torch.cuda.synchronize()
-    assert op.device_status() == bsg.BSG_OK
     return c_ref, a_ref, c_new, a_new
 
 
@@ -73,3 +74,5 @@ def test_noalloc_rejects_bad_arguments():
     op = bsg.GemmAmax(problem_of(p))
     assert bsg.bsg_run_noalloc(None, 1, 1, 1, 1, 1, 1, 0) == bsg.BSG_ERR_INVALID_ARG
     assert bsg.bsg_run_noalloc(op.plan, 0, 16, 16, 16, 16, 16, 0) == bsg.BSG_ERR_INVALID_ARG
+    # checked before the array is touched: a misaligned pointer enqueues nothing
+    assert bsg.bsg_run_noalloc(op.plan, 8, 16, 16, 16, 16, 16, 0) == bsg.BSG_ERR_ALIGNMENT
