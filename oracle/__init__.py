@@ -19,6 +19,9 @@ functions follow the page's section "Equations":
   codes + E8M0 scales in the atom layout ("GEMM + RoPE + MXFP8 Projection
   (SM100)", "Equations"; the block-scale rule is the reading stated in
   bsg_oracle.c); ``quantize_value`` rounds one scaled value
+* ``quantize_colwise`` -- the same rule with blocks down the rows (the
+  page's S-direction), codes in X's layout = the GEMM's MN-major operand,
+  scales in the atom layout keyed by column
 
 Parity unpinned: the split of a row index mn = m0 + 32*m1 inside a 128-row
 scale atom is the column-major reading of the atom's shape (32, 4); the pages
@@ -96,6 +99,9 @@ def _load():
     lib.bsgo_quantize.argtypes = [dp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                   ctypes.c_int, ctypes.c_int, u8p, u8p]
     lib.bsgo_quantize.restype = ctypes.c_int
+    lib.bsgo_quantize_colwise.argtypes = [dp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                          ctypes.c_int, ctypes.c_int, u8p, u8p]
+    lib.bsgo_quantize_colwise.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -270,3 +276,30 @@ def quantize(X: np.ndarray, out_dtype: str, sfv: int):
     t_k = -(-(cols // sfv) // 4)
     return (codes.reshape(L, rows, -1), sf.reshape(L, t_r, t_k, 32, 4, 4))
 
+
+
+def quant_colwise_sizes(rows: int, cols: int, L: int) -> tuple[int, int]:
+    """Bytes of the columnwise codes and of its padded scale atom tensor
+    (blocks of 32 rows; scale atoms over ceil(cols/128) x ceil(rows/128))."""
+    return L * rows * cols, L * (-(-cols // 128)) * (-(-(rows // 32) // 4)) * 512
+
+
+def quantize_colwise(X: np.ndarray, out_dtype: str, sfv: int = 32):
+    """X (L, rows, cols) real values, blocks of sfv rows down each column ->
+    (codes uint8 (L, rows, cols), scales uint8 (L, t_c, t_k, 32, 4, 4)) with
+    t_c = ceil(cols/128), t_k = ceil(rows/sfv/4).  Read as a GEMM operand the
+    codes are MN-major (rows = K, cols = M or N)."""
+    X = np.ascontiguousarray(X, dtype=np.float64)
+    if X.ndim == 2:
+        X = X[None]
+    L, rows, cols = X.shape
+    code_bytes, sf_bytes = quant_colwise_sizes(rows, cols, L)
+    codes = np.zeros(code_bytes, dtype=np.uint8)
+    sf = np.zeros(sf_bytes, dtype=np.uint8)
+    rc = _load().bsgo_quantize_colwise(_ptr(X), int(rows), int(cols), int(L),
+                                       DTYPES[out_dtype], int(sfv), _ptr(codes), _ptr(sf))
+    if rc != 0:
+        raise ValueError("unsupported columnwise quantize request")
+    t_c = -(-cols // 128)
+    t_k = -(-(rows // sfv) // 4)
+    return codes.reshape(L, rows, cols), sf.reshape(L, t_c, t_k, 32, 4, 4)

@@ -634,3 +634,73 @@ int bsgo_quantize(const double *X, int64_t rows, int64_t cols, int64_t L, int ou
             }
     return 0;
 }
+
+/* ------------------------------------------------ MX quantizer, columnwise */
+/*
+ * The columnwise direction of the same quantizer ("GEMM + RoPE + MXFP8
+ * Projection (SM100)", sections "Overview" and "Equations": the output is
+ * quantized in both the rowwise (D-direction) and the columnwise
+ * (S-direction) layouts; MXFP8_S has its blocks along the tokens, the
+ * non-contiguous dimension).  X is (rows, cols, L), cols contiguous, as for
+ * the rowwise form, but a block is sf_vec_size consecutive ROWS of one
+ * column.  The codes keep X's layout (element (l, r, c) at
+ * (l*rows + r)*cols + c), which is the GEMM's MN-major operand layout when
+ * rows play K and cols play M (or N): strides (1, cols, cols*rows).  The
+ * scale of column c, block b = r / sfv sits where the GEMM reads the scale
+ * of row mn = c, K-block kb = b: bsgo_sf_offset(c, b, l, ceil(cols/128),
+ * ceil(rows/sfv/4)).  The pages print the S-direction scales as a plain
+ * (tokens/32, ..., HEAD_DIM) array; this library writes them in the atom
+ * layout its GEMM consumes (the same bytes, rearranged).
+ * Per block the rule is the rowwise one: amax, e = floor(log2 amax) - emax,
+ * clamp, nearest code ties to even, saturate, specials as above.  FP8 codes
+ * only (E4M3 / E5M2): the GEMM takes MN-major operands in FP8 alone.
+ * Returns 0, or -1 for an unsupported request (not FP8, sfv not 32, rows
+ * not a multiple of sfv).
+ */
+int bsgo_quantize_colwise(const double *X, int64_t rows, int64_t cols, int64_t L,
+                          int out_dtype, int sfv, uint8_t *codes, uint8_t *sf)
+{
+    int emax;
+    unsigned maxc, sign, nanc;
+    double tab[256];
+    int64_t nblk, t_c, t_k, l, c, b, r;
+    if (out_dtype != BSGO_E4M3 && out_dtype != BSGO_E5M2) return -1;
+    if (quant_format(out_dtype, &emax, &maxc, &sign, &nanc) != 0) return -1;
+    if (sfv != 32 || rows < 1 || cols < 1 || L < 1 || rows % sfv != 0) return -1;
+    bsgo_decode_table(out_dtype, tab);
+    nblk = rows / sfv;
+    t_c = ceil_div(cols, 128);
+    t_k = ceil_div(nblk, 4);
+    memset(sf, 127, (size_t)(L * t_c * t_k * 512));
+    for (l = 0; l < L; l++)
+        for (c = 0; c < cols; c++)
+            for (b = 0; b < nblk; b++) {
+                /* the block: rows b*sfv .. b*sfv + sfv - 1 of column c */
+                const double *x0 = X + (l * rows + b * sfv) * cols + c;
+                double amax = 0.0, scale = 1.0;
+                int nonfinite = 0, e = 0, E;
+                unsigned byte = 127u;
+                for (r = 0; r < sfv; r++) {
+                    const double v = x0[r * cols];
+                    if (isnan(v) || isinf(v)) nonfinite = 1;
+                    else if (fabs(v) > amax) amax = fabs(v);
+                }
+                if (nonfinite) {
+                    byte = 0xFFu;
+                } else if (amax > 0.0) {
+                    frexp(amax, &E);            /* amax = f * 2^E, f in [0.5, 1) */
+                    e = (E - 1) - emax;         /* floor(log2 amax) - emax */
+                    if (e < -127) e = -127;
+                    if (e > 127) e = 127;
+                    byte = (unsigned)(e + 127);
+                    scale = ldexp(1.0, e);
+                }
+                sf[bsgo_sf_offset(c, b, l, t_c, t_k)] = (uint8_t)byte;
+                for (r = 0; r < sfv; r++) {
+                    const double v = x0[r * cols];
+                    codes[(l * rows + b * sfv + r) * cols + c] =
+                        (uint8_t)(nonfinite ? nanc : nearest_code(v / scale, tab, maxc, sign));
+                }
+            }
+    return 0;
+}

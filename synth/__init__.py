@@ -382,6 +382,16 @@ def real_blocks(L: int, rows: int, cols: int, seed: int, block: int = 32, spread
     return x
 
 
+
+def real_blocks_colwise(L: int, rows: int, cols: int, seed: int, block: int = 32,
+                        spread: int = 30, specials: bool = False) -> np.ndarray:
+    """real_blocks with the runs down the columns: float32 (L, rows, cols),
+    cols contiguous, every `block` consecutive rows of a column scaled by its
+    own 2^j (the input shape of the columnwise quantizer).  rows must be a
+    multiple of `block`; cols is free."""
+    x = real_blocks(L, cols, rows, seed, block=block, spread=spread, specials=specials)
+    return np.ascontiguousarray(x.transpose(0, 2, 1))
+
 def device_real_blocks(L: int, rows: int, cols: int, seed: int, device, block: int = 32,
                        spread: int = 30):
     """real_blocks' recipe drawn on a CUDA device by torch's seeded generator,

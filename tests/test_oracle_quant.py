@@ -87,6 +87,114 @@ def test_golden_blocks(name):
         assert int(sf.reshape(-1)[oracle.sf_offset(r, b, 0, t_r, t_k)]) == v, (name, r, b)
 
 
+@pytest.mark.parametrize("name", golden_names("cq"))
+def test_golden_columnwise_blocks(name):
+    """Hand-worked columnwise blocks (blocks of 32 down each column)."""
+    with open(os.path.join(GOLDEN, name)) as f:
+        g = json.load(f)
+    X = np.zeros((1, g["rows"], g["cols"]))
+    for r, c, v in g["x_set_rc"]:
+        X[0, r, c] = float(v)
+    codes, sf = oracle.quantize_colwise(X, g["out_dtype"], g["sfv"])
+    for r, c, v in g["expect_codes_rc"]:
+        assert int(codes[0, r, c]) == v, (name, r, c)
+    t_c, t_k = sf.shape[1], sf.shape[2]
+    flat = sf.reshape(-1)
+    seen = set()
+    for c, b, v in g["expect_scale_bytes"]:
+        off = oracle.sf_offset(c, b, 0, t_c, t_k)
+        seen.add(off)
+        assert int(flat[off]) == v, (name, c, b)
+    rest = np.array([flat[i] for i in range(flat.size) if i not in seen])
+    assert np.all(rest == g["expect_padding_byte"])
+
+
+@pytest.mark.parametrize("dtype", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("L,rows,cols", [(1, 32, 16), (2, 96, 48), (1, 160, 272), (3, 256, 130)])
+def test_columnwise_is_rowwise_of_the_transpose(dtype, L, rows, cols):
+    """Blocks down the columns of X are blocks along the rows of X^T: the
+    columnwise codes are the rowwise codes of X^T transposed back, and the
+    scale of (column c, block b) is the rowwise scale of (row c, block b) --
+    the same atom tensor byte for byte, padding included.  Ragged shapes
+    (rows not a multiple of 128, cols not a multiple of 128) and special
+    blocks are included."""
+    X = synth.real_blocks_colwise(L, rows, cols, seed=rows + cols + L, block=32)
+    X = X.astype(np.float64)
+    X[0, 0:32, 0] = 0.0                           # a zero block
+    X[L - 1, rows - 32 + 5, cols - 1] = np.nan    # a NaN block in the last corner
+    if cols > 2:
+        X[0, 32 % rows, 1] = np.inf
+    cc, sc = oracle.quantize_colwise(X, dtype, 32)
+    cr, sr = oracle.quantize(np.ascontiguousarray(X.transpose(0, 2, 1)), dtype, 32)
+    np.testing.assert_array_equal(cc, cr.transpose(0, 2, 1))
+    np.testing.assert_array_equal(sc, sr)
+
+
+def test_columnwise_block_properties():
+    """Each column block's maximum lands in the top binade of E4M3 (its code
+    is 0x78..0x7E in magnitude), and no code of a block exceeds it."""
+    X = synth.real_blocks_colwise(1, 128, 64, seed=5, block=32).astype(np.float64)
+    X = X * np.exp2(np.random.default_rng(6).integers(-20, 20, size=(1, 1, 64)))  # columns differ
+    codes, sf = oracle.quantize_colwise(X, "e4m3", 32)
+    for c in range(64):
+        for b in range(4):
+            col = codes[0, 32 * b:32 * b + 32, c].astype(np.int64) & 0x7F
+            blk = X[0, 32 * b:32 * b + 32, c]
+            top = col[np.argmax(np.abs(blk))]
+            assert 0x78 <= top <= 0x7E, (c, b, top)
+            assert col.max() == top
+
+
+@pytest.mark.parametrize("bad", [dict(dtype="e2m1"), dict(sfv=16), dict(rows=48)])
+def test_columnwise_rejects(bad):
+    rows = bad.get("rows", 64)
+    X = np.ones((1, rows, 16))
+    with pytest.raises(ValueError):
+        oracle.quantize_colwise(X, bad.get("dtype", "e4m3"), bad.get("sfv", 32))
+
+
+@pytest.mark.parametrize("dtype", ["e4m3", "e5m2"])
+def test_columnwise_quantize_then_mn_major_gemm_within_the_formats_error(dtype):
+    """A (K x M) and B (K x N) stored with M (N) contiguous, quantized
+    columnwise (blocks of 32 along K), are an m-major A and an n-major B
+    with their scale atoms; the GEMM oracle on them gives the product of the
+    original matrices within the error the two quantisations allow (the
+    bound of the rowwise test, with blocks along K).  A scale keyed by the
+    wrong column or block, or codes read as k-major, break it."""
+    M, N, K, L = 144, 200, 320, 2
+    At = synth.real_blocks_colwise(L, K, M, seed=51, block=32).astype(np.float64)  # (L, K, M)
+    Bt = synth.real_blocks_colwise(L, K, N, seed=52, block=32).astype(np.float64)
+    At *= np.exp2(np.random.default_rng(53).integers(-6, 6, size=(L, 1, M)))
+    qa, sa = oracle.quantize_colwise(At, dtype, 32)
+    qb, sb = oracle.quantize_colwise(Bt, dtype, 32)
+    C, _, _ = oracle.gemm(M, N, K, L, dtype, dtype, 32, qa, qb, sa, sb, a_major="m", b_major="n")
+    rel, ab = ERR[dtype]
+
+    def err(Xt):  # Xt (L, K, MN): blocks of 32 along K
+        Lx, Kx, MNx = Xt.shape
+        blk = np.abs(Xt).reshape(Lx, Kx // 32, 32, MNx)
+        bm = blk.max(axis=2, keepdims=True)
+        unit = np.where(bm > 0, 2.0 ** (np.floor(np.log2(np.where(bm > 0, bm, 1.0))) - EMAX[dtype]), 0.0)
+        return (rel * blk + ab * unit).reshape(Xt.shape)
+
+    ea, eb = err(At), err(Bt)
+    exact = np.einsum("lkm,lkn->lmn", At, Bt)
+    bound = (np.einsum("lkm,lkn->lmn", np.abs(At), eb) + np.einsum("lkm,lkn->lmn", ea, np.abs(Bt)) +
+             np.einsum("lkm,lkn->lmn", ea, eb))
+    assert np.all(np.abs(C - exact) <= bound * (1 + 1e-12) + 1e-300)
+    assert np.median(np.abs(C - exact) / np.maximum(bound, 1e-300)) < 0.5
+    # the same bytes read as k-major, or A's scales of the two column atoms
+    # swapped, break the bound
+    Cw, _, _ = oracle.gemm(M, N, K, L, dtype, dtype, 32,
+                           np.ascontiguousarray(qa.reshape(L, M, K)),
+                           np.ascontiguousarray(qb.reshape(L, N, K)), sa, sb)
+    assert not np.all(np.abs(Cw - exact) <= bound * (1 + 1e-12))
+    sa_swapped = np.ascontiguousarray(sa[:, ::-1])
+    Cs, _, _ = oracle.gemm(M, N, K, L, dtype, dtype, 32, qa, qb, sa_swapped, sb,
+                           a_major="m", b_major="n")
+    assert not np.all(np.abs(Cs - exact) <= bound * (1 + 1e-12))
+
+
 @pytest.mark.parametrize("dtype,tdt", [("e4m3", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)])
 def test_element_rounding_matches_torch(dtype, tdt):
     rng = np.random.default_rng(7)
