@@ -265,6 +265,152 @@ __global__ void __launch_bounds__(kThreads) bsq_quantize_kernel(const QParams p)
   }
 }
 
+// ------------------------------------------------------------ columnwise
+//
+// The S-direction of the same rule ("GEMM + RoPE + MXFP8 Projection (SM100)",
+// sections "Overview" and "Equations": blocks along the tokens, the
+// non-contiguous dimension): X (L, rows, cols), cols contiguous, one E8M0
+// scale per 32 consecutive rows of a column.  The codes keep X's layout --
+// the GEMM's MN-major operand with rows as K -- and the scale of (column c,
+// block b) goes where the GEMM reads row mn = c, K-block kb = b of the atom
+// tensor (L, ceil(cols/128), ceil(rows/128), 32, 4, 4).  FP8 codes only.
+//
+// A unit is one 128-row atom of K by 8 warps x kColsPerWarp columns.  Within
+// a 32-row block, lane t of a warp holds rows t/8 + 4i (i < 8) of the 16-byte
+// column chunk t%8, so each load instruction reads four rows of 128
+// contiguous bytes; the four lanes sharing a chunk combine their column
+// maxima by two shuffles.  After the unit's four blocks, lanes 0..7 write
+// each column's four scale bytes (K-blocks 0..3 of the atom) as one 32-bit
+// word; columns past `cols` and blocks past rows/32 keep byte 127.
+
+struct QCParams {
+  const uint8_t* x;
+  uint8_t* codes;
+  uint8_t* sf;
+  uint32_t rows, cols, L;
+  uint32_t nblk, t_c, t_k;  // blocks per column (rows / 32); atoms along cols and rows
+  uint32_t num_units;       // L * t_k * col_units
+  FastDiv cu_div;           // column units per atom row: ceil(cols / unit columns)
+  FastDiv tk_div;           // t_k
+};
+
+template <int IN_BF16>
+struct ColTile {
+  static constexpr int kE = IN_BF16 ? 8 : 4;           // columns per 16-byte chunk
+  static constexpr int kColsPerWarp = 8 * kE;           // 8 chunk lanes x kE
+  static constexpr int kUnitCols = 8 * kColsPerWarp;    // 8 warps
+};
+
+template <int IN_BF16, int OUT>
+__global__ void __launch_bounds__(kThreads) bsq_quantize_colwise_kernel(const QCParams p) {
+  using T = ColTile<IN_BF16>;
+  constexpr int E = T::kE;
+  constexpr int kInBytes = IN_BF16 ? 2 : 4;
+  using F = OutFmt<OUT>;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int chunk = lane & 7, rg = lane >> 3;  // column chunk of the warp, row group
+
+  for (uint32_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    const uint32_t lk = fdiv(u, p.cu_div);  // l * t_k + kt
+    const uint32_t cu = u - lk * p.cu_div.d;
+    const uint32_t l = fdiv(lk, p.tk_div);
+    const uint32_t kt = lk - l * p.t_k;
+    const uint32_t c0 = cu * T::kUnitCols + warp * T::kColsPerWarp + chunk * E;
+    const bool col_ok = c0 < p.cols;  // cols % 16 == 0: a chunk is wholly in or out
+    const uint32_t nb = min(4u, p.nblk - kt * 4);
+    uint32_t sfw[E];  // per column: the scale bytes of K-blocks 0..3 of this atom
+#pragma unroll
+    for (int j = 0; j < E; ++j) sfw[j] = 0x7F7F7F7Fu;
+    for (uint32_t b = 0; b < nb; ++b) {
+      const uint32_t row0 = kt * 128 + b * 32 + rg;
+      uint4 raw[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const size_t e = (static_cast<size_t>(l) * p.rows + row0 + 4 * i) * p.cols + c0;
+        raw[i] = col_ok ? __ldcs(reinterpret_cast<const uint4*>(p.x + e * kInBytes))
+                        : make_uint4(0u, 0u, 0u, 0u);
+      }
+      // per column: max of the magnitude bits over this lane's 8 rows, then
+      // over the 4 row groups (NaN and infinity order above every finite value)
+      uint32_t amax[E];
+#pragma unroll
+      for (int j = 0; j < E; ++j) amax[j] = 0u;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+          const uint32_t bits = IN_BF16 ? ((j & 1) ? (w[j / 2] & 0xFFFF0000u) : (w[j / 2] << 16))
+                                        : w[j];
+          amax[j] = max(amax[j], bits & 0x7FFFFFFFu);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < E; ++j) {
+        amax[j] = max(amax[j], __shfl_xor_sync(0xFFFFFFFFu, amax[j], 8));
+        amax[j] = max(amax[j], __shfl_xor_sync(0xFFFFFFFFu, amax[j], 16));
+      }
+      if (!col_ok) continue;
+      float inv[E];
+      bool nonfinite[E];
+#pragma unroll
+      for (int j = 0; j < E; ++j) {
+        uint32_t byte = 127u;
+        inv[j] = 1.0f;
+        nonfinite[j] = amax[j] >= 0x7F800000u;
+        if (nonfinite[j]) {
+          byte = 0xFFu;
+        } else if (amax[j] != 0u) {
+          int e = floor_log2_bits(amax[j]) - F::kEmax;
+          e = min(max(e, -127), 127);
+          byte = static_cast<uint32_t>(e + 127);
+          inv[j] = -e >= -126 ? __uint_as_float(static_cast<uint32_t>(127 - e) << 23)
+                              : __uint_as_float(0x00400000u);
+        }
+        sfw[j] = (sfw[j] & ~(0xFFu << (8 * b))) | (byte << (8 * b));
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+        float v[E];
+#pragma unroll
+        for (int j = 0; j < E; ++j)
+          v[j] = __uint_as_float(IN_BF16 ? ((j & 1) ? (w[j / 2] & 0xFFFF0000u) : (w[j / 2] << 16))
+                                         : w[j]);
+        uint32_t out[E / 4];
+#pragma unroll
+        for (int k = 0; k < E / 4; ++k) out[k] = 0u;
+#pragma unroll
+        for (int j = 0; j < E; j += 2) {
+          // exact products (powers of two), then two codes per conversion
+          uint32_t c2 = cvt2<OUT>(v[j] * inv[j], v[j + 1] * inv[j + 1]);
+          if (nonfinite[j]) c2 = (c2 & 0xFF00u) | F::kNan;
+          if (nonfinite[j + 1]) c2 = (c2 & 0x00FFu) | (F::kNan << 8);
+          out[j / 4] |= c2 << (16 * ((j / 2) % 2));
+        }
+        uint8_t* dst = p.codes + (static_cast<size_t>(l) * p.rows + row0 + 4 * i) * p.cols + c0;
+        if (E == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(out[0], out[E / 4 - 1]);
+        else *reinterpret_cast<uint32_t*>(dst) = out[0];
+      }
+    }
+    // the unit's scale words: lanes of row group 0, one word per column of a
+    // real atom (columns past `cols` in the last atom: padding 127)
+    if (rg == 0) {
+#pragma unroll
+      for (int j = 0; j < E; ++j) {
+        const uint32_t c = c0 + j;
+        const uint32_t atom = c >> 7;
+        if (atom < p.t_c) {
+          const uint32_t off = (((l * p.t_c + atom) * p.t_k + kt) << 9) + (c & 31) * 16 +
+                               ((c & 127) >> 5) * 4;
+          *reinterpret_cast<uint32_t*>(p.sf + off) = sfw[j];
+        }
+      }
+    }
+  }
+}
+
 template <int IN_BF16, int OUT, int SFV>
 const void* kernel_of() {
   return reinterpret_cast<const void*>(&bsq_quantize_kernel<IN_BF16, OUT, SFV>);
@@ -273,6 +419,16 @@ const void* kernel_of() {
 // variant index for the per-device occupancy cache: [in_bf16][E4M3, E5M2, E2M1/16, E2M1/32]
 int variant_of(int in_bf16, int out, int sfv) {
   return in_bf16 * 4 + (out == kOutE2M1 ? (sfv == 16 ? 2 : 3) : out);
+}
+
+template <int IN_BF16, int OUT>
+const void* colwise_kernel_of() {
+  return reinterpret_cast<const void*>(&bsq_quantize_colwise_kernel<IN_BF16, OUT>);
+}
+
+const void* pick_colwise_kernel(int in_bf16, int out) {
+  if (out == kOutE4M3) return in_bf16 ? colwise_kernel_of<1, kOutE4M3>() : colwise_kernel_of<0, kOutE4M3>();
+  return in_bf16 ? colwise_kernel_of<1, kOutE5M2>() : colwise_kernel_of<0, kOutE5M2>();
 }
 
 const void* pick_kernel(int in_bf16, int out, int sfv) {
@@ -288,7 +444,58 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
 int g_dev_sms[kMaxDevices] = {};   // 0: not queried yet; -1: not an sm_103 device
-int g_dev_occ[kMaxDevices][8] = {};  // resident CTAs per SM of each variant; 0: not queried
+// resident CTAs per SM of each variant (0: not queried): rowwise [0, 8) as
+// variant_of, columnwise 8 + in_bf16 * 2 + out (E4M3 0, E5M2 1)
+int g_dev_occ[kMaxDevices][12] = {};
+
+// One launch of the columnwise kernel (the request already checked).
+bsg_status launch_colwise(const bsg_quant_problem* q, const void* X, void* codes, void* sf,
+                          void* stream, int dev, int sms) {
+  QCParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int in_bf16 = q->in_dtype == BSG_BF16 ? 1 : 0;
+  const int out = q->out_dtype == BSG_E4M3 ? kOutE4M3 : kOutE5M2;
+  p.x = static_cast<const uint8_t*>(X);
+  p.codes = static_cast<uint8_t*>(codes);
+  p.sf = static_cast<uint8_t*>(sf);
+  p.rows = static_cast<uint32_t>(q->rows);
+  p.cols = static_cast<uint32_t>(q->cols);
+  p.L = static_cast<uint32_t>(q->L);
+  p.nblk = p.rows / 32;
+  p.t_c = static_cast<uint32_t>(cdiv(q->cols, 128));
+  p.t_k = static_cast<uint32_t>(cdiv(p.nblk, 4));
+  const int64_t unit_cols = in_bf16 ? ColTile<1>::kUnitCols : ColTile<0>::kUnitCols;
+  const int64_t col_units = cdiv(q->cols, unit_cols);
+  const int64_t units = q->L * static_cast<int64_t>(p.t_k) * col_units;
+  if (units > (int64_t(1) << 31) - 1) return BSG_ERR_INVALID_ARG;
+  p.num_units = static_cast<uint32_t>(units);
+  p.cu_div = make_fastdiv(static_cast<uint32_t>(col_units));
+  p.tk_div = make_fastdiv(p.t_k);
+  const void* fn = pick_colwise_kernel(in_bf16, out);
+  int occ;
+  {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    int& slot = g_dev_occ[dev][8 + in_bf16 * 2 + out];
+    if (slot == 0) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, 0) != cudaSuccess) {
+        cudaGetLastError();
+        return BSG_ERR_CUDA;
+      }
+      slot = n < 1 ? 1 : (n > 8 ? 8 : n);
+    }
+    occ = slot;
+  }
+  int64_t grid = static_cast<int64_t>(sms) * occ;
+  if (grid > p.num_units) grid = p.num_units;
+  void* args[1] = {&p};
+  if (cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(kThreads), args, 0,
+                       static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return BSG_ERR_CUDA;
+  }
+  return BSG_OK;
+}
 
 }  // namespace
 
@@ -300,6 +507,22 @@ bsg_status bsg_quant_check(const bsg_quant_problem* q) {
   if (q->rows < 1 || q->cols < 1 || q->L < 1) return BSG_ERR_INVALID_ARG;
   if (q->rows > lim || q->cols > lim || q->L > lim || q->rows * q->L > lim)
     return BSG_ERR_INVALID_ARG;
+  if (q->direction != BSG_QUANT_ROWWISE && q->direction != BSG_QUANT_COLWISE)
+    return BSG_ERR_INVALID_ARG;
+  if (q->direction == BSG_QUANT_COLWISE) {
+    // blocks of 32 rows down each column; FP8 codes (the GEMM's MN-major
+    // operands are FP8 only); code rows of `cols` bytes 16-byte aligned
+    if (q->in_dtype != BSG_F32 && q->in_dtype != BSG_BF16) return BSG_ERR_INVALID_ARG;
+    if (q->out_dtype != BSG_E4M3 && q->out_dtype != BSG_E5M2 && q->out_dtype != BSG_E2M1)
+      return BSG_ERR_INVALID_ARG;
+    if (q->sf_vec_size != 16 && q->sf_vec_size != 32) return BSG_ERR_INVALID_ARG;
+    if (q->out_dtype == BSG_E2M1 || q->sf_vec_size != 32) return BSG_ERR_UNSUPPORTED;
+    if (q->rows % 32 != 0) return BSG_ERR_UNSUPPORTED;  // whole blocks only
+    if (q->cols % 16 != 0) return BSG_ERR_ALIGNMENT;
+    const int64_t sf_bytes = q->L * ((q->cols + 127) / 128) * ((q->rows / 32 + 3) / 4) * 512;
+    if (sf_bytes > lim || q->L * q->rows * q->cols / 16 > lim) return BSG_ERR_INVALID_ARG;
+    return BSG_OK;
+  }
   // the scale atom tensor is indexed with 32-bit offsets
   if (q->sf_vec_size == 16 || q->sf_vec_size == 32) {
     const int64_t sf_bytes =
@@ -319,6 +542,11 @@ bsg_status bsg_quant_sizes(const bsg_quant_problem* q, size_t* code_bytes, size_
   const bsg_status st = bsg_quant_check(q);
   if (st != BSG_OK) return st;
   if (!code_bytes || !sf_bytes) return BSG_ERR_INVALID_ARG;
+  if (q->direction == BSG_QUANT_COLWISE) {
+    *code_bytes = static_cast<size_t>(q->L * q->rows * q->cols);
+    *sf_bytes = static_cast<size_t>(q->L * cdiv(q->cols, 128) * cdiv(q->rows / 32, 4) * 512);
+    return BSG_OK;
+  }
   const int64_t per_row = q->out_dtype == BSG_E2M1 ? q->cols / 2 : q->cols;
   *code_bytes = static_cast<size_t>(q->L * q->rows * per_row);
   *sf_bytes = static_cast<size_t>(q->L * cdiv(q->rows, 128) * cdiv(q->cols / q->sf_vec_size, 4) * 512);
@@ -352,6 +580,7 @@ bsg_status bsg_quantize(const bsg_quant_problem* q, const void* X, void* codes, 
     sms = g_dev_sms[dev];
   }
   if (sms < 0) return BSG_ERR_ARCH;
+  if (q->direction == BSG_QUANT_COLWISE) return launch_colwise(q, X, codes, sf, stream, dev, sms);
   QParams p;
   std::memset(&p, 0, sizeof(p));
   const int in_bf16 = q->in_dtype == BSG_BF16 ? 1 : 0;

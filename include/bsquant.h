@@ -34,6 +34,26 @@
  *          byte is written: padding positions (rows >= rows, blocks >=
  *          cols/sfv) get 127.  Device memory, 16-byte aligned.
  *
+ * Columnwise (direction BSG_QUANT_COLWISE; "GEMM + RoPE + MXFP8 Projection
+ * (SM100)", sections "Overview" and "Equations": MXFP8_S, blocks along the
+ * tokens, the non-contiguous dimension): the same rule with each block 32
+ * consecutive ROWS of one column.
+ *   X      as above.  cols a multiple of 16, rows a multiple of 32.
+ *   codes  (L, rows, cols) FP8 bytes in X's layout.  Read by the GEMM with
+ *          rows as K and cols as M (or N), this is its m-major A (n-major
+ *          B): strides (1, cols, cols*rows).
+ *   SF     the GEMM's atom tensor for that operand: (L, ceil(cols/128),
+ *          ceil(rows/128), 32, 4, 4); the scale of column c, block b sits
+ *          where the GEMM reads row mn = c, K-block kb = b.  Padding
+ *          positions (columns >= cols, blocks >= rows/32) get 127.  (The
+ *          page prints its S-direction scales as a plain (tokens/32, ...,
+ *          D) array; these are the same bytes in the atom layout the GEMM
+ *          consumes.)
+ *   E4M3 or E5M2 codes and sf_vec_size 32 only (the GEMM's MN-major
+ *   operands are FP8): E2M1 or sf_vec_size 16 is BSG_ERR_UNSUPPORTED, rows
+ *   not a multiple of 32 BSG_ERR_UNSUPPORTED, cols not a multiple of 16
+ *   BSG_ERR_ALIGNMENT.
+ *
  * Ownership: the caller owns X, codes and SF.  bsg_quantize allocates
  * nothing, never synchronises and enqueues one kernel on `stream` (a
  * cudaStream_t, NULL for the legacy default stream).
@@ -57,11 +77,19 @@
 extern "C" {
 #endif
 
+/* Direction of the scale blocks ("GEMM + RoPE + MXFP8 Projection (SM100)",
+ * "Overview": rowwise (D-direction) and columnwise (S-direction)). */
+typedef enum {
+  BSG_QUANT_ROWWISE = 0,  /* blocks along each row (the contiguous cols) */
+  BSG_QUANT_COLWISE = 1   /* blocks down each column (32 consecutive rows) */
+} bsg_quant_direction;
+
 typedef struct {
   int64_t rows, cols, L;  /* X is (L, rows, cols), cols contiguous */
   bsg_dtype in_dtype;     /* BSG_F32 or BSG_BF16 */
-  bsg_dtype out_dtype;    /* BSG_E4M3, BSG_E5M2 or BSG_E2M1 */
+  bsg_dtype out_dtype;    /* BSG_E4M3, BSG_E5M2 or BSG_E2M1 (rowwise only) */
   int sf_vec_size;        /* 32; or 16 for BSG_E2M1 */
+  int direction;          /* bsg_quant_direction; 0 (rowwise) for zero-initialised requests */
 } bsg_quant_problem;
 
 /* Host-only validation of a request against the rules above. */
@@ -70,7 +98,8 @@ bsg_status bsg_quant_check(const bsg_quant_problem* q);
 /* Bytes of the code tensor and of the (padded) scale atom tensor. */
 bsg_status bsg_quant_sizes(const bsg_quant_problem* q, size_t* code_bytes, size_t* sf_bytes);
 
-/* Quantize X into codes and SF (one launch on `stream`). */
+/* Quantize X into codes and SF in the request's direction (one launch on
+ * `stream`). */
 bsg_status bsg_quantize(const bsg_quant_problem* q, const void* X, void* codes, void* sf,
                         void* stream);
 
