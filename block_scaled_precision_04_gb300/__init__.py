@@ -64,13 +64,18 @@ class bsg_plan_info(ctypes.Structure):
                 ("grid", ctypes.c_int32), ("threads", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("num_tiles", ctypes.c_int32),
                 ("mma_kind", ctypes.c_int32), ("cluster_m", ctypes.c_int32),
-                ("kernel_name", ctypes.c_char * 64)]
+                ("kernel_name", ctypes.c_char * 64), ("half_tiles", ctypes.c_int32)]
+
+
+BSG_QUANT_ROWWISE = 0
+BSG_QUANT_COLWISE = 1
+DIRECTION = {"row": BSG_QUANT_ROWWISE, "col": BSG_QUANT_COLWISE}
 
 
 class bsg_quant_problem(ctypes.Structure):
     _fields_ = [("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("L", ctypes.c_int64),
                 ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
-                ("sf_vec_size", ctypes.c_int)]
+                ("sf_vec_size", ctypes.c_int), ("direction", ctypes.c_int)]
 
 
 class bsg_device_buffers(ctypes.Structure):
@@ -284,10 +289,13 @@ class GemmAmax:
 # ------------------------------------------------------------- quantizer
 
 def make_quant_problem(rows, cols, L=1, in_dtype="f32", out_dtype="e4m3",
-                       sf_vec_size=32) -> bsg_quant_problem:
+                       sf_vec_size=32, direction="row") -> bsg_quant_problem:
+    """A bsg_quant_problem; ``direction`` is "row" (blocks along each row) or
+    "col" (blocks of 32 down each column), or the enum value."""
     d = lambda x: DTYPE[x] if isinstance(x, str) else int(x)
+    dr = DIRECTION[direction] if isinstance(direction, str) else int(direction)
     return bsg_quant_problem(int(rows), int(cols), int(L), d(in_dtype), d(out_dtype),
-                             int(sf_vec_size))
+                             int(sf_vec_size), dr)
 
 
 def bsg_quant_check(q: bsg_quant_problem) -> int:
@@ -304,10 +312,13 @@ def bsg_quantize(q: bsg_quant_problem, X: int, codes: int, sf: int, stream: int 
     return library().bsg_quantize(ctypes.byref(q), X, codes, sf, stream)
 
 
-def quantize(X, out_dtype="e4m3", sf_vec_size=32, codes=None, sf=None, stream=None):
+def quantize(X, out_dtype="e4m3", sf_vec_size=32, codes=None, sf=None, stream=None,
+             direction="row"):
     """Quantize a contiguous CUDA tensor X (L, rows, cols) or (rows, cols) of
     float32 or bfloat16 into (codes, sf) uint8 tensors (allocated when not
-    given); one launch on torch's current stream."""
+    given); one launch on torch's current stream.  ``direction="col"`` puts
+    the blocks down the columns: the codes are then the GEMM's MN-major
+    operand (rows = K) and sf its scale atoms."""
     import torch
     if not X.is_cuda or not X.is_contiguous():
         raise ValueError("X must be a contiguous CUDA tensor")
@@ -315,7 +326,8 @@ def quantize(X, out_dtype="e4m3", sf_vec_size=32, codes=None, sf=None, stream=No
     in_dtype = {torch.float32: "f32", torch.bfloat16: "bf16"}.get(X.dtype)
     if in_dtype is None:
         raise ValueError("X must be float32 or bfloat16")
-    q = make_quant_problem(shape[1], shape[2], shape[0], in_dtype, out_dtype, sf_vec_size)
+    q = make_quant_problem(shape[1], shape[2], shape[0], in_dtype, out_dtype, sf_vec_size,
+                           direction)
     st, (cb, sb) = bsg_quant_sizes(q)
     check(st, "bsg_quant_sizes")
     if codes is None:

@@ -45,6 +45,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <type_traits>
 
 #include "bsgemm.h"
 
@@ -58,7 +59,7 @@ constexpr int kMmaKBytes = 32;     // bytes of K per tcgen05.mma (32 FP8 or 64 F
 // quarter), 14 scale producer (tensor copies of the scale atoms).
 constexpr int kSfWarp0 = 2;
 constexpr int kEpiWarp0 = 6;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 8;  // (epi_barrier_and counts their 256 threads)
 constexpr int kSfProdWarp = kEpiWarp0 + kEpiWarps;
 constexpr int kThreads = 32 * (kSfProdWarp + 1);
 constexpr int kAtomBytes = 512;    // one scale atom: 128 rows x 4 K-blocks
@@ -74,7 +75,8 @@ struct Params {
   int M, N, K, L;
   int tiles_m, tiles_n, num_tiles;
   int tiles_mc;           // groups of cluster_m consecutive M tiles: ceil(tiles_m / cluster_m)
-  int num_units;          // scheduling units (one per cluster): L * tiles_mc * tiles_n
+  int num_units;          // scheduling units (one per cluster): full_units + 2 * split tiles
+  int full_units;         // units that are whole tiles; the rest are half-width tiles
   int k_bytes;            // bytes per operand row
   int k_stages;           // ceil(k_bytes / 128)
   int t_m, t_n, t_k;      // scale atoms: ceil(M/128), ceil(N/128), ceil(K/(4 sfv))
@@ -84,6 +86,7 @@ struct Params {
   int c_major;            // 0 = n-major, 1 = m-major
   int a_mn, b_mn;         // 1: A m-major / B n-major (FP8), tiles stored MN-contiguous
   uint32_t idesc;         // instruction descriptor, scale ids zero
+  uint32_t idesc_half;    // the same with N = TILE_N / 2 (half-width units)
   uint32_t smem_a, smem_b, smem_sfa, smem_sfb, smem_epi, smem_bar;  // offsets in dynamic smem
   const uint8_t* sfa;
   const uint8_t* sfb;
@@ -147,6 +150,15 @@ __device__ __forceinline__ void tma_load_3d_to_leader(uint32_t dst, const CUtens
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
+}
+
+// True in exactly one lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -331,13 +343,23 @@ struct KindTraits<kKindF4x2X> {  // FP4, block 32: two scale bytes per K=64 MMA
 
 struct Tile {
   int l, mt, nt;
+  int half;  // -1: the whole tile; 0 / 1: its left / right half (N = TILE_N / 2)
 };
 
 // Unit u (one per cluster) -> (l, group of cluster_m M tiles, N tile); the
 // CTA of rank `rank` takes M tile group * cm + rank (past tiles_m: a ghost
 // tile whose rows are all masked, kept so the cluster stays in lockstep).
+// Units from full_units on split the last tiles in two halves: the schedule's
+// final wave is then half-width tiles, so a partly filled last wave costs half
+// a tile time instead of a whole one.
 __device__ __forceinline__ Tile tile_coords(const Params& p, int u, int cm, int rank) {
   Tile r;
+  r.half = -1;
+  if (u >= p.full_units) {
+    const int hu = u - p.full_units;
+    u = p.full_units + (hu >> 1);
+    r.half = hu & 1;
+  }
   const int per_batch = p.tiles_mc * p.tiles_n;
   r.l = u / per_batch;
   const int rem = u - r.l * per_batch;
@@ -394,6 +416,19 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Para
       }
     }
   }
+}
+
+// AND of `v` over the 256 threads of the 8 epilogue warps, at named barrier 1
+// (every epilogue thread must arrive, with no other thread using the id).
+__device__ __forceinline__ uint32_t epi_barrier_and(uint32_t v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+      "barrier.cta.red.and.pred po, 1, 256, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(v)
+      : "memory");
+  return r;
 }
 
 // Fast path inline: one test_wait; the bounded loop only when the phase is open.
@@ -497,10 +532,14 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 
 // --------------------------------------------------------------- kernel
 
-template <int KIND, int TILE_N, int NUM_ACC, int CM, int PAIR, int KSL>
+// LOWC: the epilogue writes low-precision C (E4M3, E5M2 or packed E2M1; FP4
+// operands only); a kernel of its own, since that path's registers would
+// otherwise spill in every FP4 kernel.
+template <int KIND, int TILE_N, int NUM_ACC, int CM, int PAIR, int KSL, int LOWC>
 __global__ void __launch_bounds__(kThreads, 1)
     bsg_gemm_amax_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b,
+                         const __grid_constant__ CUtensorMap tmap_bh,
                          const __grid_constant__ CUtensorMap tmap_sfa,
                          const __grid_constant__ CUtensorMap tmap_sfb, const __grid_constant__ Params p) {
   using KT = KindTraits<KIND>;
@@ -535,6 +574,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kMmasPerSlice = kStageKBytes / kMmaKBytes;
   // both CTAs of a pair: the targets of the leader's commit arrivals
   constexpr uint16_t kMask = static_cast<uint16_t>((1u << CM) - 1u);
+  // half-width units (the split last wave) exist for 256-wide pairs only:
+  // each CTA then loads 64 rows of B (the tmap_bh box) and the MMA runs N = 128
+  constexpr bool kHalves = PAIR && TILE_N == 256;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // align the dynamic window to 1024 bytes (128-byte swizzle atoms)
@@ -630,8 +672,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool a_mn = KIND == kKindF8F6F4 && p.a_mn, b_mn = KIND == kKindF8F6F4 && p.b_mn;
       for (int u = unit0; u < p.num_units && ok; u += unit_step) {
         const Tile tc = tile_coords(p, u, CM, crank);
-        const int m0 = tc.mt * kTileM, n0 = tc.nt * TILE_N;
-        const int atom0 = n0 / 128;  // first scale atom of B covering this tile
+        const bool hu = kHalves && tc.half >= 0;
+        const int m0 = tc.mt * kTileM;
+        const int n0 = tc.nt * TILE_N + (hu ? tc.half * (TILE_N / 2) : 0);
+        const int atom0 = n0 / 128;  // first scale atom of B covering this unit
+        // B rows per CTA of this unit, their tensor map and the stage's bytes
+        const int brows = hu ? kBRows / 2 : kBRows;
+        const CUtensorMap* const bmap = hu ? &tmap_bh : &tmap_b;
+        const uint32_t b_stage_bytes = hu ? kBStage / 2 : kBStage;
         for (int ks = 0; ks < p.k_stages; ++ks) {
           if (!BSG_WAIT(empty0 + 8u * stage, phase ^ 1u, scales ? 12 : 1)) { ok = false; break; }
           const uint32_t bar = bar_base + 8u * stage;
@@ -651,22 +699,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int sl = 0; sl < KSL; ++sl) {
               const int kx = ks * kSB + sl * kStageKBytes;
-              const int nb = n0 + kBRows;
+              const int nb = n0 + brows;
               // a k-major box is (K bytes, rows); an MN-major one (MN, K rows)
               tma_load_3d_to_leader(a_dst0 + stage * kAStage + sl * kASlice, &tmap_a,
                                     a_mn ? m0 : kx, a_mn ? kx : m0, tc.l, lbar);
-              tma_load_3d_to_leader(b_dst0 + stage * kBStage + sl * kBSlice, &tmap_b,
+              tma_load_3d_to_leader(b_dst0 + stage * kBStage + sl * kBSlice, bmap,
                                     b_mn ? nb : kx, b_mn ? kx : nb, tc.l, lbar);
             }
           } else {
             // a pair's leader expects the bytes of both CTAs
-            mbar_arrive_expect_tx(bar, (PAIR ? 2u : 1u) * (kAStage + kBStage));
+            mbar_arrive_expect_tx(bar, (PAIR ? 2u : 1u) * (kAStage + b_stage_bytes));
 #pragma unroll
             for (int sl = 0; sl < KSL; ++sl) {
               const int kx = ks * kSB + sl * kStageKBytes;
               tma_load_3d(a_dst0 + stage * kAStage + sl * kASlice, &tmap_a, a_mn ? m0 : kx,
                           a_mn ? kx : m0, tc.l, bar);
-              tma_load_3d(b_dst0 + stage * kBStage + sl * kBSlice, &tmap_b, b_mn ? n0 : kx,
+              tma_load_3d(b_dst0 + stage * kBStage + sl * kBSlice, bmap, b_mn ? n0 : kx,
                           b_mn ? kx : n0, tc.l, bar);
             }
           }
@@ -689,8 +737,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
-    // (in a CTA pair only the leader issues, for both CTAs)
-    if (lane == 0 && (!PAIR || crank == 0)) {
+    // (in a CTA pair only the leader issues, for both CTAs).  The whole warp
+    // walks the loop, so the descriptors and addresses stay warp-uniform, and
+    // one elected lane issues the MMAs and commits: issuing from a
+    // single-lane branch measured ~120 cycles per tcgen05.mma against ~63
+    // this way, which left the tensor pipe idle between stages.
+    if (!PAIR || crank == 0) {
+      const bool elected = elect_one();
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -722,12 +775,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!BSG_WAIT(acce0 + 8u * acc, acc_phase ^ 1u, 2)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * TILE_N;
+        // a half-width unit runs N = TILE_N / 2 from the first half of each
+        // CTA's B rows into the first TILE_N / 2 accumulator columns
+        const uint32_t id_u = kHalves && u >= p.full_units ? p.idesc_half : idesc;
         for (int ks = 0; ks < p.k_stages; ++ks) {
           // operands in smem and this stage's scales in tensor memory
           if (!BSG_WAIT(full0 + 8u * stage, phase, 3)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sfb_t = sfa_t + 4 * kCps;
           const int nm = ks == last ? last_nmma : kMmasPerStage;
+          if (elected) {
 #pragma unroll
           for (int j = 0; j < kMmasPerStage; ++j) {
             if (j < nm) {
@@ -736,7 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int sl = j / kMmasPerSlice, jj = j % kMmasPerSlice;
               mma_issue(d_tmem, ad + ((sl * kASlice) >> 4) + jj * a_kstep,
                         bd + ((sl * kBSlice) >> 4) + jj * b_kstep,
-                        idesc | (sf_id << 29) | (sf_id << 4), sfa_t + 4 * c, sfb_t + 4 * G * c,
+                        id_u | (sf_id << 29) | (sf_id << 4), sfa_t + 4 * c, sfb_t + 4 * G * c,
                         (j != 0 || ks != 0) ? 1u : 0u);
             }
           }
@@ -745,6 +802,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // cycle of delay here delays the stage's refill
           if (PAIR) tc_commit_pair_mc(empty0 + 8u * stage, kMask);
           else tc_commit(empty0 + 8u * stage);
+          }
+          __syncwarp();
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
@@ -759,14 +818,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         // accumulator ready for the epilogue (of both CTAs of a pair)
-        if (PAIR) tc_commit_pair_mc(accf0 + 8u * acc, kMask);
-        else tc_commit(accf0 + 8u * acc);
+        if (elected) {
+          if (PAIR) tc_commit_pair_mc(accf0 + 8u * acc, kMask);
+          else tc_commit(accf0 + 8u * acc);
+        }
+        __syncwarp();
         if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1u; }
       }
-      // drain: all MMAs issued by this thread complete before exit
-      if (PAIR) tc_commit_pair(drain_bar);
-      else tc_commit(drain_bar);
-      drain_wait(drain_bar, 0, p, 11u, globaltimer());
+      // drain: all MMAs issued by this warp complete before exit
+      if (elected) {
+        if (PAIR) tc_commit_pair(drain_bar);
+        else tc_commit(drain_bar);
+        drain_wait(drain_bar, 0, p, 11u, globaltimer());
+      }
+      __syncwarp();
     }
   } else if (warp >= kSfWarp0 && warp < kSfWarp0 + 4) {
     // --------------------------------------------------------- scale warps
@@ -843,8 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // released after the last chunk, and the stores overlap the next tile's
     // MMAs.  fp32 C: two passes of TILE_N/4 columns, released after the
     // second pass's loads.
-    constexpr int kCols = TILE_N / 2;
-    constexpr int kCh16 = kCols / 16;  // 16-column chunks of this warp
+    constexpr int kCols = TILE_N / 2;  // columns of this warp in a whole tile
     constexpr int kRnd = 4;            // chunks per round of tensor-memory loads
     const int q = warp & 3;
     const int h = (warp - kEpiWarp0) >> 2;
@@ -858,19 +922,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int u = unit0; u < p.num_units; u += unit_step) {
       const Tile tc = tile_coords(p, u, CM, crank);
-      // one lane waits, the warp follows its verdict (tcgen05.ld is warp-collective)
-      int ready = 0;
-      if (lane == 0) ready = BSG_WAIT_SLEEP(accf0 + 8u * acc, acc_phase, 4) ? 1 : 0;
-      ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
-      if (!ready) break;
+      // one lane of one warp spins on the accumulator; the 8 epilogue warps
+      // take its verdict at a named barrier, which also wakes them at once
+      // (napping warps added up to a nap's length to every hand-off)
+      uint32_t ready = 1;
+      if (warp == kEpiWarp0 && lane == 0) ready = BSG_WAIT(accf0 + 8u * acc, acc_phase, 4) ? 1u : 0u;
+      if (!epi_barrier_and(ready)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * TILE_N + h * kCols;
+      // a half-width unit (N = TILE_N / 2 in the first accumulator columns)
+      // gives each warp half as many columns
+      const bool hu = kHalves && tc.half >= 0;
+      const int ucol0 = tc.nt * TILE_N + (hu ? tc.half * (TILE_N / 2) : 0);
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * TILE_N;
       const int row = tc.mt * kTileM + q * 32 + lane;
       const bool row_ok = row < p.M;
       const size_t batch_off = static_cast<size_t>(tc.l) * p.M * p.N;
-      const int n0 = tc.nt * TILE_N + h * kCols;
-      // columns of this warp's half stored in this lane's row
-      const int lim = row_ok ? p.N - n0 : 0;
       const uint32_t release_bar = acce0 + 8u * acc;
       if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1u; }
       auto release = [&]() {
@@ -881,223 +947,245 @@ __global__ void __launch_bounds__(kThreads, 1)
           else mbar_arrive(release_bar);
         }
       };
-      // packed rounded values of the 16- and 8-bit paths, and one round of
-      // tensor-memory loads
-      uint32_t pk[kCols / 2];
-      uint32_t rb[kRnd][16];
-      if (KIND != kKindF8F6F4 &&
-          (p.c_dtype == BSG_E4M3 || p.c_dtype == BSG_E5M2 || p.c_dtype == BSG_E2M1)) {
-        // FP8 or packed E2M1 C (FP4 operands only): each 16-column chunk is
-        // converted as it leaves tensor memory; Amax is the rounded value of
-        // the largest stored magnitude (the rounding is monotone in |x|).
-        // pk: four FP8 codes per register (E2M1: eight, the first kCols/8)
-        const bool fp4 = p.c_dtype == BSG_E2M1, e5 = p.c_dtype == BSG_E5M2;
-#pragma unroll
-        for (int c0 = 0; c0 < kCh16; c0 += kRnd) {
-#pragma unroll
-          for (int i = 0; i < kRnd; ++i)
-            if (c0 + i < kCh16) tc_ld_32x32b_x16(taddr + (c0 + i) * 16, rb[i]);
-          tc_wait_ld();
-#pragma unroll
-          for (int i = 0; i < kRnd; ++i) {
-            if (c0 + i >= kCh16) continue;
-            const int cc = (c0 + i) * 16;
-            const uint32_t* r = rb[i];
-            if (lim >= cc + 16) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                uint32_t a = r[j] & 0x7FFFFFFFu;
-                if (fp4 && a > 0x7F800000u) a = 0u;  // stored as +0
-                vmax = max(vmax, a);
-              }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                uint32_t a = r[j] & 0x7FFFFFFFu;
-                if (fp4 && a > 0x7F800000u) a = 0u;
-                if (cc + j >= lim) a = 0u;
-                vmax = max(vmax, a);
-              }
-            }
-            if (fp4) {
-              uint32_t w0 = 0u, w1 = 0u;
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const uint32_t b = cvt2_e2m1(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                if (j < 4) w0 |= b << (8 * j);
-                else w1 |= b << (8 * (j - 4));
-              }
-              pk[cc / 8] = w0;
-              pk[cc / 8 + 1] = w1;
-            } else {
-#pragma unroll
-              for (int j = 0; j < 8; j += 2) {
-                const float a0 = __uint_as_float(r[2 * j]), a1 = __uint_as_float(r[2 * j + 1]);
-                const float b0 = __uint_as_float(r[2 * j + 2]), b1 = __uint_as_float(r[2 * j + 3]);
-                const uint32_t lo = e5 ? cvt2_e5m2(a0, a1) : cvt2_e4m3(a0, a1);
-                const uint32_t hi = e5 ? cvt2_e5m2(b0, b1) : cvt2_e4m3(b0, b1);
-                pk[cc / 4 + j / 2] = lo | (hi << 16);
-              }
-            }
-          }
-        }
-        release();
-        uint8_t* const cbase = static_cast<uint8_t*>(p.c) + (fp4 ? batch_off / 2 : batch_off);
-        if (p.c_major == 0) {
+      // the unit's stores: CW accumulator columns per warp, a compile-time
+      // width (a runtime one spilled registers in these unrolled loops)
+      auto unit = [&](auto cw_tag) {
+        constexpr int CW = decltype(cw_tag)::value;  // columns of this warp in this unit
+        constexpr int kChU = CW / 16;                 // its 16-column chunks
+        const int n_end = min(p.N, ucol0 + 2 * CW);   // one past the unit's last stored column
+        const uint32_t taddr = tbase + h * CW;
+        const int n0 = ucol0 + h * CW;
+        // columns of this warp's part stored in this lane's row (may be <= 0)
+        const int lim = row_ok ? n_end - n0 : 0;
+        // one round of tensor-memory loads
+        uint32_t rb[kRnd][16];
+        if constexpr (LOWC) {
+          // FP8 or packed E2M1 C (FP4 operands only): each round of kRnd
+          // 16-column chunks is converted as it leaves tensor memory and
+          // stored at once (holding every code of the warp's columns until
+          // the end spilled registers); Amax is the rounded value of the
+          // largest stored magnitude (the rounding is monotone in |x|)
+          const bool fp4 = p.c_dtype == BSG_E2M1, e5 = p.c_dtype == BSG_E5M2;
+          constexpr int kRc = kRnd * 16;  // columns per round
+          uint8_t* const cbase = static_cast<uint8_t*>(p.c) + (fp4 ? batch_off / 2 : batch_off);
           const int row0 = tc.mt * kTileM + q * 32;
-          if (fp4) {
-            // kCols / 2 bytes per row: one staged chunk
-            char* const g0 = reinterpret_cast<char*>(cbase + static_cast<size_t>(row0) * (p.N / 2) + n0 / 2);
-            // (an FP8-operand kernel never takes this branch; its width only
-            // has to name a valid chunk)
-            constexpr int kW4 = (kCols / 8 == 8 || kCols / 8 == 16) ? kCols / 8 : 8;
-            store_rows_coalesced<kW4>(stg, pk, lane, g0, static_cast<size_t>(p.N / 2), p.M - row0,
-                                      (p.N - n0) / 2);
-          } else {
-            char* const g0 = reinterpret_cast<char*>(cbase + static_cast<size_t>(row0) * p.N + n0);
+          const int ncols = row_ok ? min(CW, n_end - n0) : 0;  // m-major: stored columns
 #pragma unroll
-            for (int cc = 0; cc + 64 <= kCols; cc += 64)
-              store_rows_coalesced<16>(stg, pk + cc / 4, lane, g0 + cc, static_cast<size_t>(p.N),
-                                       p.M - row0, p.N - n0 - cc);
-          }
-        } else {
-          // m-major FP8: column by column, the 32 lanes write 32 consecutive rows
-          uint8_t* dst = cbase + static_cast<size_t>(n0) * p.M + row;
-          const int ncols = row_ok ? min(kCols, p.N - n0) : 0;
+          for (int c0 = 0; c0 < kChU; c0 += kRnd) {
 #pragma unroll
-          for (int j = 0; j < kCols; ++j) {
-            if (j < ncols) *dst = static_cast<uint8_t>(pk[j / 4] >> (8 * (j % 4)));
-            dst += p.M;
-          }
-        }
-      } else if (p.c_dtype != BSG_F32) {
-        // pk: two rounded 16-bit values per register
-        const bool bf = p.c_dtype == BSG_BF16;
-        // rounds of kRnd 16-column loads: all of a round in flight at once,
-        // one wait, then its conversions (fewer waits than one load ahead)
+            for (int i = 0; i < kRnd; ++i)
+              if (c0 + i < kChU) tc_ld_32x32b_x16(taddr + (c0 + i) * 16, rb[i]);
+            tc_wait_ld();
+            // the last round's loads have landed: free the accumulator before
+            // converting them (the MMAs of the next unit wait for this)
+            if (c0 + kRnd >= kChU) release();
+            // the round's codes: four FP8 per word, or eight E2M1 (the first
+            // kRc / 8 words)
+            uint32_t pr[kRc / 4];
 #pragma unroll
-        for (int c0 = 0; c0 < kCh16; c0 += kRnd) {
+            for (int i = 0; i < kRnd; ++i) {
+              const int cc = (c0 + i) * 16;
+              const uint32_t* r = rb[i];
+              if (lim >= cc + 16) {
 #pragma unroll
-          for (int i = 0; i < kRnd; ++i)
-            if (c0 + i < kCh16) tc_ld_32x32b_x16(taddr + (c0 + i) * 16, rb[i]);
-          tc_wait_ld();
-#pragma unroll
-          for (int i = 0; i < kRnd; ++i) {
-            if (c0 + i >= kCh16) continue;
-            const int cc = (c0 + i) * 16;
-            const uint32_t* r = rb[i];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float f0 = __uint_as_float(r[2 * j]), f1 = __uint_as_float(r[2 * j + 1]);
-              // two round-to-nearest-even conversions in one: low half column
-              // cc + 2j, high half column cc + 2j + 1
-              uint32_t h;
-              if (bf) {
-                const __nv_bfloat162 v = __floats2bfloat162_rn(f0, f1);
-                h = *reinterpret_cast<const uint32_t*>(&v);
-              } else {
-                const __half2 v = __floats2half2_rn(f0, f1);
-                h = *reinterpret_cast<const uint32_t*>(&v);
-              }
-              pk[cc / 2 + j] = h;
-            }
-            // only stored elements count toward Amax: a whole chunk without
-            // per-element tests (which made the drain four times slower),
-            // the ragged edge with them
-            if (lim >= cc + 16) {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) vmax = __vmaxu2(vmax, pk[cc / 2 + j] & 0x7FFF7FFFu);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                uint32_t m = pk[cc / 2 + j] & 0x7FFF7FFFu;
-                if (cc + 2 * j >= lim) m &= 0xFFFF0000u;
-                if (cc + 2 * j + 1 >= lim) m &= 0x0000FFFFu;
-                vmax = __vmaxu2(vmax, m);
-              }
-            }
-          }
-        }
-        release();
-        uint16_t* const cbase = static_cast<uint16_t*>(p.c) + batch_off;
-        if (p.c_major == 0) {
-          // 32-column chunks (64 bytes per row) through the staging buffer;
-          // a 112-column half ends with a 16-column chunk
-          const int row0 = tc.mt * kTileM + q * 32;
-          char* const g0 = reinterpret_cast<char*>(cbase + static_cast<size_t>(row0) * p.N + n0);
-          const size_t pitch = static_cast<size_t>(p.N) * 2;
-#pragma unroll
-          for (int cc = 0; cc + 32 <= kCols; cc += 32)
-            store_rows_coalesced<16>(stg, pk + cc / 2, lane, g0 + cc * 2, pitch, p.M - row0,
-                                     (p.N - n0 - cc) * 2);
-          if (kCols % 32 == 16)
-            store_rows_coalesced<8>(stg, pk + (kCols - 16) / 2, lane, g0 + (kCols - 16) * 2, pitch,
-                                    p.M - row0, (p.N - n0 - (kCols - 16)) * 2);
-        } else {
-          // m-major: column by column, the 32 lanes write 32 consecutive rows
-          uint16_t* dst = cbase + static_cast<size_t>(n0) * p.M + row;
-          const int ncols = row_ok ? min(kCols, p.N - n0) : 0;
-#pragma unroll
-          for (int j = 0; j < kCols; ++j) {
-            if (j < ncols)
-              *dst = static_cast<uint16_t>((j & 1) ? (pk[j / 2] >> 16) : (pk[j / 2] & 0xFFFFu));
-            dst += p.M;
-          }
-        }
-      } else {
-        float* const cbase = static_cast<float*>(p.c) + batch_off;
-        constexpr int kCh = kCols / 16;        // 16-column chunks of this warp
-        constexpr int kP1 = (kCh + 1) / 2;     // chunks of the first pass
-#pragma unroll
-        for (int pass = 0; pass < 2; ++pass) {
-          const int c0 = pass ? kP1 : 0;
-          const int cn = pass ? kCh - kP1 : kP1;
-          uint32_t r[kP1 * 16];
-#pragma unroll
-          for (int i = 0; i < kP1; ++i)
-            if (i < cn) tc_ld_32x32b_x16(taddr + (c0 + i) * 16, r + 16 * i);
-          tc_wait_ld();
-          if (pass == 1) release();
-          const int nb = n0 + c0 * 16;
-          if (p.c_major == 0) {
-            // each 16-column chunk (64 bytes per row) through the staging buffer
-            const int row0 = tc.mt * kTileM + q * 32;
-            char* const g0 = reinterpret_cast<char*>(cbase + static_cast<size_t>(row0) * p.N + nb);
-            const size_t pitch = static_cast<size_t>(p.N) * 4;
-#pragma unroll
-            for (int i = 0; i < kP1; ++i) {
-              if (i < cn) {
-                // only stored elements count toward Amax
-                if (row_ok && nb + 16 * i + 16 <= p.N) {
-#pragma unroll
-                  for (int j = 0; j < 16; ++j) vmax = max(vmax, r[16 * i + j] & 0x7FFFFFFFu);
-                } else {
-#pragma unroll
-                  for (int j = 0; j < 16; ++j)
-                    if (row_ok && nb + 16 * i + j < p.N) vmax = max(vmax, r[16 * i + j] & 0x7FFFFFFFu);
+                for (int j = 0; j < 16; ++j) {
+                  uint32_t a = r[j] & 0x7FFFFFFFu;
+                  if (fp4 && a > 0x7F800000u) a = 0u;  // stored as +0
+                  vmax = max(vmax, a);
                 }
-                store_rows_coalesced<16>(stg, r + 16 * i, lane, g0 + 16 * i * 4, pitch, p.M - row0,
-                                         (p.N - nb - 16 * i) * 4);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  uint32_t a = r[j] & 0x7FFFFFFFu;
+                  if (fp4 && a > 0x7F800000u) a = 0u;
+                  if (cc + j >= lim) a = 0u;
+                  vmax = max(vmax, a);
+                }
+              }
+              if (fp4) {
+                uint32_t w0 = 0u, w1 = 0u;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const uint32_t b = cvt2_e2m1(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                  if (j < 4) w0 |= b << (8 * j);
+                  else w1 |= b << (8 * (j - 4));
+                }
+                pr[2 * i] = w0;
+                pr[2 * i + 1] = w1;
+              } else {
+#pragma unroll
+                for (int j = 0; j < 8; j += 2) {
+                  const float a0 = __uint_as_float(r[2 * j]), a1 = __uint_as_float(r[2 * j + 1]);
+                  const float b0 = __uint_as_float(r[2 * j + 2]), b1 = __uint_as_float(r[2 * j + 3]);
+                  const uint32_t lo = e5 ? cvt2_e5m2(a0, a1) : cvt2_e4m3(a0, a1);
+                  const uint32_t hi = e5 ? cvt2_e5m2(b0, b1) : cvt2_e4m3(b0, b1);
+                  pr[4 * i + j / 2] = lo | (hi << 16);
+                }
               }
             }
-          } else {
-            float* dst = cbase + static_cast<size_t>(nb) * p.M + row;
-            const int ncols = row_ok ? min(cn * 16, p.N - nb) : 0;
-#pragma unroll
-            for (int j = 0; j < kP1 * 16; ++j) {
-              if (j < ncols) {
-                const float f = __uint_as_float(r[j]);
-                *dst = f;
-                vmax = max(vmax, abs_bits_f32(f));
+            const int cr = c0 * 16;  // the round's first column in this warp's part
+            if (p.c_major == 0) {
+              if (fp4) {
+                // kRc / 2 bytes per row: one staged chunk of 8 words
+                char* const g = reinterpret_cast<char*>(
+                    cbase + static_cast<size_t>(row0) * (p.N / 2) + (n0 + cr) / 2);
+                store_rows_coalesced<kRc / 8>(stg, pr, lane, g, static_cast<size_t>(p.N / 2),
+                                              p.M - row0, (n_end - n0 - cr) / 2);
+              } else {
+                char* const g = reinterpret_cast<char*>(cbase + static_cast<size_t>(row0) * p.N + n0 + cr);
+                store_rows_coalesced<kRc / 4>(stg, pr, lane, g, static_cast<size_t>(p.N), p.M - row0,
+                                              n_end - n0 - cr);
               }
+            } else {
+              // m-major FP8: column by column, the 32 lanes write 32 consecutive rows
+              uint8_t* dst = cbase + static_cast<size_t>(n0 + cr) * p.M + row;
+#pragma unroll
+              for (int j = 0; j < kRc; ++j) {
+                if (cr + j < ncols) *dst = static_cast<uint8_t>(pr[j / 4] >> (8 * (j % 4)));
+                dst += p.M;
+              }
+            }
+          }
+        } else if (p.c_dtype != BSG_F32) {
+          uint32_t pk[CW / 2];
+          // pk: two rounded 16-bit values per register
+          const bool bf = p.c_dtype == BSG_BF16;
+          // rounds of kRnd 16-column loads: all of a round in flight at once,
+          // one wait, then its conversions (fewer waits than one load ahead)
+#pragma unroll
+          for (int c0 = 0; c0 < kChU; c0 += kRnd) {
+#pragma unroll
+            for (int i = 0; i < kRnd; ++i)
+              if (c0 + i < kChU) tc_ld_32x32b_x16(taddr + (c0 + i) * 16, rb[i]);
+            tc_wait_ld();
+            // the last round's loads have landed: free the accumulator before
+            // converting them (the MMAs of the next unit wait for this)
+            if (c0 + kRnd >= kChU) release();
+#pragma unroll
+            for (int i = 0; i < kRnd; ++i) {
+              if (c0 + i >= kChU) continue;
+              const int cc = (c0 + i) * 16;
+              const uint32_t* r = rb[i];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float f0 = __uint_as_float(r[2 * j]), f1 = __uint_as_float(r[2 * j + 1]);
+                // two round-to-nearest-even conversions in one: low half column
+                // cc + 2j, high half column cc + 2j + 1
+                uint32_t h;
+                if (bf) {
+                  const __nv_bfloat162 v = __floats2bfloat162_rn(f0, f1);
+                  h = *reinterpret_cast<const uint32_t*>(&v);
+                } else {
+                  const __half2 v = __floats2half2_rn(f0, f1);
+                  h = *reinterpret_cast<const uint32_t*>(&v);
+                }
+                pk[cc / 2 + j] = h;
+              }
+              // only stored elements count toward Amax: a whole chunk without
+              // per-element tests (which made the drain four times slower),
+              // the ragged edge with them
+              if (lim >= cc + 16) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) vmax = __vmaxu2(vmax, pk[cc / 2 + j] & 0x7FFF7FFFu);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  uint32_t m = pk[cc / 2 + j] & 0x7FFF7FFFu;
+                  if (cc + 2 * j >= lim) m &= 0xFFFF0000u;
+                  if (cc + 2 * j + 1 >= lim) m &= 0x0000FFFFu;
+                  vmax = __vmaxu2(vmax, m);
+                }
+              }
+            }
+          }
+          uint16_t* const cbase = static_cast<uint16_t*>(p.c) + batch_off;
+          if (p.c_major == 0) {
+            // 32-column chunks (64 bytes per row) through the staging buffer;
+            // a 112-column half ends with a 16-column chunk
+            const int row0 = tc.mt * kTileM + q * 32;
+            char* const g0 = reinterpret_cast<char*>(cbase + static_cast<size_t>(row0) * p.N + n0);
+            const size_t pitch = static_cast<size_t>(p.N) * 2;
+#pragma unroll
+            for (int cc = 0; cc + 32 <= CW; cc += 32)
+              if (cc < CW)
+                store_rows_coalesced<16>(stg, pk + cc / 2, lane, g0 + cc * 2, pitch, p.M - row0,
+                                         (n_end - n0 - cc) * 2);
+            if (CW % 32 == 16)  // (never a half-width unit: those come from 256-wide tiles)
+              store_rows_coalesced<8>(stg, pk + (CW - 16) / 2, lane, g0 + (CW - 16) * 2, pitch,
+                                      p.M - row0, (n_end - n0 - (CW - 16)) * 2);
+          } else {
+            // m-major: column by column, the 32 lanes write 32 consecutive rows
+            uint16_t* dst = cbase + static_cast<size_t>(n0) * p.M + row;
+            const int ncols = row_ok ? min(CW, n_end - n0) : 0;
+#pragma unroll
+            for (int j = 0; j < CW; ++j) {
+              if (j < ncols)
+                *dst = static_cast<uint16_t>((j & 1) ? (pk[j / 2] >> 16) : (pk[j / 2] & 0xFFFFu));
               dst += p.M;
             }
           }
+        } else {
+          float* const cbase = static_cast<float*>(p.c) + batch_off;
+          constexpr int kCh = CW / 16;         // 16-column chunks of this warp
+          constexpr int kP1 = (kCh + 1) / 2;   // chunks held in registers at once
+          constexpr int kP2 = kCh - kP1;       // the rest, loaded as the first go out
+          // chunk ci (its 16 values in rr): Amax of the stored elements, then
+          // the stores -- n-major through the staging buffer (64 bytes per
+          // row), m-major column by column (32 consecutive rows per store)
+          auto chunk_out = [&](int ci, const uint32_t* rr) {
+            const int nb = n0 + 16 * ci;
+            if (row_ok && nb + 16 <= n_end) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) vmax = max(vmax, rr[j] & 0x7FFFFFFFu);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (row_ok && nb + j < n_end) vmax = max(vmax, rr[j] & 0x7FFFFFFFu);
+            }
+            if (p.c_major == 0) {
+              const int row0 = tc.mt * kTileM + q * 32;
+              char* const g = reinterpret_cast<char*>(cbase + static_cast<size_t>(row0) * p.N + nb);
+              store_rows_coalesced<16>(stg, rr, lane, g, static_cast<size_t>(p.N) * 4, p.M - row0,
+                                       (n_end - nb) * 4);
+            } else {
+              float* dst = cbase + static_cast<size_t>(nb) * p.M + row;
+              const int ncols = row_ok ? min(16, n_end - nb) : 0;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                if (j < ncols) *dst = __uint_as_float(rr[j]);
+                dst += p.M;
+              }
+            }
+          };
+          uint32_t r[kP1 * 16];
+#pragma unroll
+          for (int i = 0; i < kP1; ++i) tc_ld_32x32b_x16(taddr + i * 16, r + 16 * i);
+          tc_wait_ld();
+          if (kP2 == 0) release();
+          // each first chunk out, then the second half's chunk loaded into its
+          // registers: the loads overlap the stores, and the accumulator is
+          // freed as soon as the last of them lands
+#pragma unroll
+          for (int i = 0; i < kP1; ++i) {
+            chunk_out(i, r + 16 * i);
+            if (i < kP2) tc_ld_32x32b_x16(taddr + (kP1 + i) * 16, r + 16 * i);
+          }
+          if (kP2 > 0) {
+            tc_wait_ld();
+            release();
+#pragma unroll
+            for (int i = 0; i < kP2; ++i) chunk_out(kP1 + i, r + 16 * i);
+          }
         }
+      };
+      if constexpr (kHalves) {
+        if (hu) unit(std::integral_constant<int, kCols / 2>{});
+        else unit(std::integral_constant<int, kCols>{});
+      } else {
+        unit(std::integral_constant<int, kCols>{});
       }
     }
-    if (KIND != kKindF8F6F4 &&
-        (p.c_dtype == BSG_E4M3 || p.c_dtype == BSG_E5M2 || p.c_dtype == BSG_E2M1)) {
+    if constexpr (LOWC) {
       // the stored magnitude of the largest |C|: round it like the stores did
       const float mx = __uint_as_float(vmax);
       const uint32_t code = p.c_dtype == BSG_E2M1 ? cvt2_e2m1(mx, 0.0f) & 0xFu
@@ -1149,38 +1237,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Kernel variants: MMA kind x (TILE_N, accumulator buffers) x cluster along M
 // (cm 1: a CTA alone; 2: a cta_group::2 pair)
 struct Variant {
-  int kind, tile_n, num_acc, cm, pair, kslices;
+  int kind, tile_n, num_acc, cm, pair, kslices, lowc;
   const void* fn;
 };
 
-template <int KIND, int TN, int NACC, int CM, int PAIR, int KSL = 1>
+template <int KIND, int TN, int NACC, int CM, int PAIR, int LOWC = 0, int KSL = 1>
 Variant make_variant() {
-  return Variant{KIND, TN, NACC, CM, PAIR, KSL,
-                 reinterpret_cast<const void*>(&bsg_gemm_amax_kernel<KIND, TN, NACC, CM, PAIR, KSL>)};
+  return Variant{KIND, TN, NACC, CM, PAIR, KSL, LOWC,
+                 reinterpret_cast<const void*>(
+                     &bsg_gemm_amax_kernel<KIND, TN, NACC, CM, PAIR, KSL, LOWC>)};
 }
 
-template <int KIND>
+template <int KIND, int LOWC>
 void add_kind(Variant* out, int& n) {
-  out[n++] = make_variant<KIND, 128, 2, 1, 0>();
-  out[n++] = make_variant<KIND, 256, 1, 1, 0>();
-  out[n++] = make_variant<KIND, 256, 1, 2, 1>();
+  out[n++] = make_variant<KIND, 128, 2, 1, 0, LOWC>();
+  out[n++] = make_variant<KIND, 256, 1, 1, 0, LOWC>();
+  out[n++] = make_variant<KIND, 256, 1, 2, 1, LOWC>();
 }
 
-const Variant* find_variant(int kind, int tile_n, int num_acc, int cm, int kslices) {
-  static Variant table[14];
+const Variant* find_variant(int kind, int tile_n, int num_acc, int cm, int kslices, int lowc) {
+  static Variant table[16];
   static int n = 0;
   static std::once_flag once;
   std::call_once(once, [] {
-    add_kind<kKindF8F6F4>(table, n);
+    add_kind<kKindF8F6F4, 0>(table, n);
     table[n++] = make_variant<kKindF8F6F4, 224, 2, 2, 1>();  // 256 x 224 pairs, two accumulators
-    table[n++] = make_variant<kKindF8F6F4, 256, 1, 2, 1, 2>();  // pairs, 256-byte K stages
-    add_kind<kKindF4x4X>(table, n);
-    add_kind<kKindF4x2X>(table, n);
+    add_kind<kKindF4x4X, 0>(table, n);
+    add_kind<kKindF4x2X, 0>(table, n);
+    add_kind<kKindF4x4X, 1>(table, n);  // FP4 operands with E4M3 / E5M2 / E2M1 C
+    add_kind<kKindF4x2X, 1>(table, n);
   });
   for (int i = 0; i < n; ++i) {
     const Variant& v = table[i];
     if (v.kind == kind && v.tile_n == tile_n && v.num_acc == num_acc && v.cm == cm &&
-        v.kslices == kslices)
+        v.kslices == kslices && v.lowc == lowc)
       return &v;
   }
   return nullptr;
@@ -1235,6 +1325,7 @@ struct bsg_plan {
   int cluster_m;         // CTAs per cluster along M: 1, or 2 for a cta_group::2 pair
   int kslices;           // 128-byte K slices per pipeline stage
   int pair;              // 1: the cluster is a cta_group::2 pair (256-row MMAs)
+  int half_tiles;        // tiles of the last wave run as two half-width units
   int grid;
   int smem_bytes;
   // tensor maps for the last A/B pointers seen
@@ -1243,8 +1334,10 @@ struct bsg_plan {
   const void* map_b_ptr = nullptr;
   const void* map_sfa_ptr = nullptr;
   const void* map_sfb_ptr = nullptr;
+  const void* map_bh_ptr = nullptr;
   CUtensorMap map_a;
   CUtensorMap map_b;
+  CUtensorMap map_bh;    // B with the half-width units' 64-row box
   CUtensorMap map_sfa;
   CUtensorMap map_sfb;
 };
@@ -1388,12 +1481,15 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
     k.tile_n = 128;
     num_acc = 2;
   }
-  // FP8 pairs with 256-wide tiles take 256-byte K stages (8 MMAs per
-  // barrier check); each CTA's half tiles keep three such stages in smem
-  const int ksl = kind == kKindF8F6F4 && k.tile_n == 256 && cm == 2 ? 2 : 1;
+  // 128-byte K stages throughout: with the MMAs issued warp-wide the
+  // per-stage cost is small, and more, smaller stages keep more operand
+  // bytes in flight (256-byte stages measured 10 % slower at 4096^3)
+  const int ksl = 1;
   const int stage_k_bytes = kStageKBytes * ksl;
   k.k_stages = static_cast<int>(cdiv(k.k_bytes, stage_k_bytes));
-  const Variant* var = find_variant(kind, k.tile_n, num_acc, cm, ksl);
+  const int lowc = prob->c_dtype == BSG_E4M3 || prob->c_dtype == BSG_E5M2 ||
+                   prob->c_dtype == BSG_E2M1;
+  const Variant* var = find_variant(kind, k.tile_n, num_acc, cm, ksl, lowc);
   if (!var) { delete plan; return BSG_ERR_UNSUPPORTED; }
   plan->kslices = ksl;
   plan->kernel = var->fn;
@@ -1405,6 +1501,7 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   k.num_tiles = k.tiles_m * k.tiles_n * k.L;
   k.tiles_mc = static_cast<int>(cdiv(k.tiles_m, cm));
   k.num_units = k.tiles_mc * k.tiles_n * k.L;
+  k.full_units = k.num_units;
   k.t_m = static_cast<int>(cdiv(prob->M, 128));
   k.t_n = static_cast<int>(cdiv(prob->N, 128));
   k.t_k = static_cast<int>(cdiv(prob->K, 4 * sfv));
@@ -1423,6 +1520,7 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
             (static_cast<uint32_t>(k.b_mn) << 16) | (static_cast<uint32_t>(k.tile_n >> 3) << 17) |
             (prob->sf_dtype == BSG_UE8M0 ? 1u << 23 : 0u) /* scale type: 1 UE8M0, 0 UE4M3 */ |
             (static_cast<uint32_t>(mma_m >> 4) << 24);
+  k.idesc_half = (k.idesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>(k.tile_n >> 4) << 17);
   k.c_dtype = prob->c_dtype;
   k.c_major = prob->c_major == 'm' ? 1 : 0;
 
@@ -1491,15 +1589,27 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
       delete plan;
       return BSG_ERR_CUDA;
     }
+    // The last wave: when the tiles left over after the full waves fill at
+    // most half of the resident pairs, each runs as two half-width units
+    // (256 x 128), so the final wave takes half a tile time.  256-wide pairs
+    // with k-major B only (a 64-row box of an MN-major B is not a whole
+    // 128-byte swizzle span).
+    const int tail = k.num_units % max_clusters;
+    if (plan->pair && k.tile_n == 256 && !b_mn && tail != 0 && 2 * tail <= max_clusters) {
+      plan->half_tiles = tail;
+      k.full_units = k.num_units - tail;
+      k.num_units = k.full_units + 2 * tail;
+    }
     const int clusters = k.num_units < max_clusters ? k.num_units : max_clusters;
     plan->grid = cm * clusters;
   }
   if (std::getenv("BSG_LOG"))
     std::fprintf(stderr,
                  "[bsgemm] M=%lld N=%lld K=%lld L=%lld tile=128x%d stages=%d grid=%d smem=%d "
-                 "kind=%d tiles=%d cluster_m=%d\n",
+                 "kind=%d tiles=%d cluster_m=%d half_tiles=%d\n",
                  (long long)prob->M, (long long)prob->N, (long long)prob->K, (long long)prob->L,
-                 k.tile_n, stages, plan->grid, plan->smem_bytes, kind, k.num_tiles, cm);
+                 k.tile_n, stages, plan->grid, plan->smem_bytes, kind, k.num_tiles, cm,
+                 plan->half_tiles);
   *out = plan;
   return BSG_OK;
 }
@@ -1598,7 +1708,7 @@ bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const vo
   k.c = C;
   k.amax = amax;
   k.ws = static_cast<uint32_t*>(ws);
-  CUtensorMap ma, mb, msfa, msfb;
+  CUtensorMap ma, mb, mbh, msfa, msfb;
   {
     std::lock_guard<std::mutex> lock(plan->mu);
     if (plan->map_a_ptr != A) {
@@ -1615,6 +1725,14 @@ bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const vo
         return BSG_ERR_CUDA;
       }
       plan->map_b_ptr = B;
+    }
+    if (plan->half_tiles && plan->map_bh_ptr != B) {
+      // each CTA of a pair loads 64 rows of a half-width unit's B
+      if (!encode_operand(&plan->map_bh, B, row_bytes, pr.N, pr.L, k.tile_n / 4, false)) {
+        plan->map_bh_ptr = nullptr;
+        return BSG_ERR_CUDA;
+      }
+      plan->map_bh_ptr = B;
     }
     const int chunks = plan->kind == kKindF8F6F4 ? 1 : (plan->kind == kKindF4x4X ? 4 : 2);
     const int k_atoms = chunks * plan->kslices;
@@ -1635,10 +1753,11 @@ bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const vo
     }
     ma = plan->map_a;
     mb = plan->map_b;
+    mbh = plan->half_tiles ? plan->map_bh : plan->map_b;
     msfa = plan->map_sfa;
     msfb = plan->map_sfb;
   }
-  void* args[5] = {&ma, &mb, &msfa, &msfb, &k};
+  void* args[6] = {&ma, &mb, &mbh, &msfa, &msfb, &k};
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(plan->grid);
@@ -1786,6 +1905,7 @@ bsg_status bsg_plan_describe(const bsg_plan* plan, bsg_plan_info* info) {
   info->num_tiles = plan->base.num_tiles;
   info->mma_kind = plan->kind;
   info->cluster_m = plan->cluster_m;
+  info->half_tiles = plan->half_tiles;
   std::snprintf(info->kernel_name, sizeof(info->kernel_name), "bsg_gemm_amax_kernel");
   return BSG_OK;
 }

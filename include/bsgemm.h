@@ -128,6 +128,8 @@ typedef struct {
     int32_t mma_kind;                      /* 0 mxf8f6f4 1X, 1 mxf4nvf4 4X, 2 mxf4nvf4 2X */
     int32_t cluster_m;                     /* 1: CTAs alone; 2: cta_group::2 pairs */
     char kernel_name[64];
+    int32_t half_tiles;                    /* tiles of the last wave run as two 256 x 128
+                                              half-width units (0: none) */
 } bsg_plan_info;
 
 /* Host-only validation of a problem against the support surface; touches

@@ -54,8 +54,8 @@ int main(void) {
   printf("%zu %zu %zu %zu %zu\n", sizeof(bsg_problem), offsetof(bsg_problem, a_major),
          offsetof(bsg_problem, sf_vec_size), offsetof(bsg_problem, cluster_n), sizeof(bsg_plan_info));
   printf("%zu %zu\n", sizeof(bsg_device_buffers), offsetof(bsg_device_buffers, ws_bytes));
-  printf("%zu %zu %zu\n", sizeof(bsg_quant_problem), offsetof(bsg_quant_problem, in_dtype),
-         offsetof(bsg_quant_problem, sf_vec_size));
+  printf("%zu %zu %zu %zu\n", sizeof(bsg_quant_problem), offsetof(bsg_quant_problem, in_dtype),
+         offsetof(bsg_quant_problem, sf_vec_size), offsetof(bsg_quant_problem, direction));
   return 0;
 }
 ''')
@@ -71,7 +71,7 @@ int main(void) {
     assert b == [ctypes.sizeof(bsg.bsg_device_buffers), bsg.bsg_device_buffers.ws_bytes.offset]
     c = [int(x) for x in lines[2].split()]
     assert c == [ctypes.sizeof(bsg.bsg_quant_problem), bsg.bsg_quant_problem.in_dtype.offset,
-                 bsg.bsg_quant_problem.sf_vec_size.offset]
+                 bsg.bsg_quant_problem.sf_vec_size.offset, bsg.bsg_quant_problem.direction.offset]
 
 
 def test_status_strings(lib):
@@ -210,6 +210,9 @@ QUANT_OK = [
     dict(rows=16384, cols=8192, in_dtype="bf16", out_dtype="e2m1", sf_vec_size=16),
     dict(rows=130, cols=96, L=3, out_dtype="e5m2"),
     dict(rows=7, cols=64, out_dtype="e2m1", sf_vec_size=32),
+    dict(rows=32, cols=16, direction="col"),
+    dict(rows=16384, cols=8192, in_dtype="bf16", out_dtype="e5m2", direction="col"),
+    dict(rows=96, cols=144, L=3, direction="col"),
 ]
 
 
@@ -228,6 +231,15 @@ QUANT_BAD = [
     (dict(rows=4, cols=32, sf_vec_size=64), bsg.BSG_ERR_INVALID_ARG, "sfv 64"),
     (dict(rows=4, cols=32, out_dtype="e4m3", sf_vec_size=16), bsg.BSG_ERR_UNSUPPORTED, "FP8 sfv 16"),
     (dict(rows=4, cols=48), bsg.BSG_ERR_UNSUPPORTED, "partial block"),
+    (dict(rows=4, cols=32, direction=2), bsg.BSG_ERR_INVALID_ARG, "unknown direction"),
+    (dict(rows=64, cols=32, out_dtype="e2m1", sf_vec_size=32, direction="col"),
+     bsg.BSG_ERR_UNSUPPORTED, "columnwise E2M1"),
+    (dict(rows=64, cols=32, out_dtype="e2m1", sf_vec_size=16, direction="col"),
+     bsg.BSG_ERR_UNSUPPORTED, "columnwise sfv 16"),
+    (dict(rows=48, cols=32, direction="col"), bsg.BSG_ERR_UNSUPPORTED, "columnwise partial block"),
+    (dict(rows=64, cols=24, direction="col"), bsg.BSG_ERR_ALIGNMENT, "columnwise row of 24 B"),
+    (dict(rows=64, cols=32, in_dtype="f16", direction="col"), bsg.BSG_ERR_INVALID_ARG,
+     "columnwise fp16 input"),
 ]
 
 
@@ -240,6 +252,9 @@ def test_quant_sizes(lib):
     st, (cb, sb) = bsg.bsg_quant_sizes(bsg.make_quant_problem(130, 256, 2, "bf16", "e2m1", 16))
     assert st == bsg.BSG_OK and cb == 2 * 130 * 128 and sb == 2 * 2 * 4 * 512
     assert lib.bsg_quantize(None, None, None, None, None) == bsg.BSG_ERR_INVALID_ARG
+    # columnwise: codes in X's layout; atoms over ceil(cols/128) x ceil(rows/128)
+    st, (cb, sb) = bsg.bsg_quant_sizes(bsg.make_quant_problem(160, 272, 2, "f32", "e4m3", 32, "col"))
+    assert st == bsg.BSG_OK and cb == 2 * 160 * 272 and sb == 2 * 3 * 2 * 512
 
 
 
