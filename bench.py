@@ -8,14 +8,23 @@ between steps.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
-  python bench.py --op quantize [--qworkload 1|2]  # the MX quantizer (HBM GB/s)
+  python bench.py --op quantize [--qworkload 1..4]  # the MX quantizer (HBM GB/s);
+                                                    # 3, 4: columnwise blocks
 
-Under torchrun (N > 1) every rank runs its own replica of the workload on its
-own GPU (no data exchanged); rank 0 prints the max-over-ranks timing.
+Under torchrun (N > 1) the ranks share one problem, one process per GPU
+(block_scaled_precision_04_gb300.shard): by default (--shard batches) the
+workload's batches are repeated N times and every rank computes its own L of
+them -- fixed work per GPU, "weak" scaling; --shard rows splits the workload
+itself by 128-row scale atoms -- fixed total work, "strong" scaling.  The one
+exchange, the 4-byte max of the per-rank Amax over NCCL, is inside every timed
+step.  `--gpus N` without torchrun re-launches this script under
+torch.distributed.run with N processes; under torchrun it must equal
+WORLD_SIZE.  Rank 0 prints the max-over-ranks timing.
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -73,9 +82,14 @@ TRAFFIC_Q = {
 }
 
 QMETRIC = "MX quantize GB/s on 1 GB300 (X read + codes and scales written); % of HBM copy bandwidth"
+# name, rows, cols, input dtype, code dtype, sf_vec_size, direction ("row":
+# blocks along each row; "col": blocks of 32 down each column, the page's
+# S-direction, whose codes are the GEMM's MN-major operand)
 QWORKLOADS = {
-    1: ("quantize-f32-16384x8192-e4m3-sfv32", 16384, 8192, "f32", "e4m3", 32),
-    2: ("quantize-bf16-16384x8192-e2m1-sfv16", 16384, 8192, "bf16", "e2m1", 16),
+    1: ("quantize-f32-16384x8192-e4m3-sfv32", 16384, 8192, "f32", "e4m3", 32, "row"),
+    2: ("quantize-bf16-16384x8192-e2m1-sfv16", 16384, 8192, "bf16", "e2m1", 16, "row"),
+    3: ("quantize-colwise-f32-16384x8192-e4m3-sfv32", 16384, 8192, "f32", "e4m3", 32, "col"),
+    4: ("quantize-colwise-bf16-16384x8192-e4m3-sfv32", 16384, 8192, "bf16", "e4m3", 32, "col"),
 }
 
 
@@ -104,6 +118,43 @@ def max_over_ranks(value: float, dist=None, device=None) -> float:
 def whole_job_tflops(flops_per_step: float, steps: int, world: int, total_ms: float) -> float:
     """Work of every replica (one per rank) over the slowest rank's time."""
     return world * flops_per_step * steps / (total_ms / 1e3) / 1e12
+
+
+def batch_seed(number: int, rank: int) -> int:
+    """Seed of the batches rank `rank` owns in a batch-sharded run: rank 0's
+    are the workload itself (seed 1000 + number), every other rank's batches
+    are drawn with the same recipe from a seed of their own."""
+    return 1000 + number + 7919 * rank
+
+
+def local_piece(number: int, world: int, rank: int, mode: str):
+    """(global problem, this rank's synth.Inputs, its shard or None).
+
+    batches: the global problem repeats the workload's L batches `world`
+    times; rank r owns batches [r L, (r+1) L), drawn with batch_seed(r).
+    rows: the global problem is the workload; rank r owns the rows that
+    shard.shard_of gives it (whole 128-row scale atoms), as a view of the
+    workload's tensors (a rank with no rows gets None)."""
+    from block_scaled_precision_04_gb300 import shard as sh
+    name, p = synth.WORKLOADS[number]
+    if world == 1:
+        return p, synth.workload(number), None
+    if mode == "batches":
+        g = dataclasses.replace(p, L=p.L * world)
+        s = sh.shard_of(g.M, g.L, world, rank)
+        assert (s.l0, s.l1, s.m0, s.m1) == (rank * p.L, (rank + 1) * p.L, 0, p.M)
+        return g, synth.workload(number, seed=batch_seed(number, rank)), s
+    if mode != "rows":
+        raise ValueError(mode)
+    s = sh.shard_of(p.M, p.L, world, rank)
+    if s.empty:
+        return p, None, s
+    full = synth.workload(number)
+    C = np.empty(synth.c_shape(p), dtype=np.uint8)  # a stand-in: C views are not kept
+    a, b, sfa, sfb, _ = sh.local_views(s, full.A, full.B, full.SFA, full.SFB, C, M=p.M,
+                                       a_major=p.a_major, c_major=p.c_major)
+    lp = sh.local_problem(p, s)
+    return p, synth.Inputs(lp, *(np.ascontiguousarray(x) for x in (a, b, sfa, sfb))), s
 
 
 def workload_numbers(p: synth.Problem):
@@ -251,9 +302,16 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    name, p = synth.WORKLOADS[args.workload]
-    inp = synth.workload(args.workload)
+    name, _ = synth.WORKLOADS[args.workload]
+    # the global problem and this rank's piece of it (the whole workload at N = 1)
+    g, inp, piece = local_piece(args.workload, world, rank, args.shard)
+    if inp is None:
+        raise SystemExit(f"rank {rank}: no rows of the workload left for this rank; "
+                         f"use fewer GPUs or --shard batches")
+    p = inp.problem
     nums = workload_numbers(p)
+    global_flops = 2.0 * g.M * g.N * g.K * g.L
+    from block_scaled_precision_04_gb300 import shard as sh
     op = bsg.GemmAmax(bsg.make_problem(p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv,
                                        p.c_dtype, p.c_major, sf_dtype=p.sf_dtype,
                                        a_major=p.a_major, b_major=p.b_major),
@@ -274,9 +332,16 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                               SFB.data_ptr(), C.data_ptr(), amax.data_ptr(),
                               op.workspace.data_ptr(), op.ws_bytes, s), "bsg_run")
 
+    def step():
+        # one pass of the path: this rank's launch, then (N > 1) the one
+        # exchange, the max of the per-rank Amax over the ranks
+        launch()
+        if world > 1:
+            sh.allreduce_amax(amax)
+
     for _ in range(args.warmup):
         flush_l2(flush)
-        launch()
+        step()
     torch.cuda.synchronize(dev)
     bsg.check(op.device_status(), "device status (warm-up)")
 
@@ -292,7 +357,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         for e0, e1 in evs:
             flush_l2(flush)
             e0.record(stream)
-            launch()
+            step()
             e1.record(stream)
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - wall0
@@ -302,7 +367,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     times_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
     total_ms = max_over_ranks(sum(times_ms), dist, dev)
     ms = total_ms / args.steps
-    value = whole_job_tflops(nums["flops"], args.steps, world, total_ms)
+    # the whole job's work (every rank's piece) over the slowest rank's time
+    value = whole_job_tflops(global_flops, args.steps, 1, total_ms)
     host_us = host_cost_us(launch, torch, dev)
     bsg.check(op.device_status(), "device status (host-cost burst)")
 
@@ -315,9 +381,13 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         bufs = bsg.bsg_device_buffers(A.data_ptr(), B.data_ptr(), SFA.data_ptr(), SFB.data_ptr(),
                                       C.data_ptr(), amax.data_ptr(), op.workspace.data_ptr(),
                                       op.ws_bytes)
-        run_host = lambda: bsg.check(bsg.bsg_run_host(
-            op.plan, pA.data_ptr(), pB.data_ptr(), pSFA.data_ptr(), pSFB.data_ptr(),
-            pC.data_ptr(), pamax.data_ptr(), bufs, s), "bsg_run_host")
+        def run_host():
+            bsg.check(bsg.bsg_run_host(
+                op.plan, pA.data_ptr(), pB.data_ptr(), pSFA.data_ptr(), pSFB.data_ptr(),
+                pC.data_ptr(), pamax.data_ptr(), bufs, s), "bsg_run_host")
+            if world > 1:  # the global Amax: reduced on the device, then read back
+                sh.allreduce_amax(amax)
+                pamax.copy_(amax, non_blocking=True)
         for _ in range(max(1, args.warmup)):
             run_host()
         torch.cuda.synchronize(dev)
@@ -328,9 +398,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
-        e2e = {"value": world * nums["flops"] / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": global_flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": nums["h2d"],
-               "d2h_bytes_per_step": nums["d2h"]}
+               "d2h_bytes_per_step": nums["d2h"] + (4 if world > 1 else 0)}
 
     bf16, hbm, source = peaks()
     peak = bf16 * NOMINAL_RATIO[nums["kind"]]
@@ -350,16 +420,24 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "higher_is_better": True,
+            "scaling": "strong" if world > 1 and args.shard == "rows" else "weak",
+            "vs_baseline": None,
             "dtype": f"{p.a_dtype}x{p.b_dtype} codes, "
                      f"{'e8m0' if p.sf_dtype == 'ue8m0' else p.sf_dtype} scales, fp32 accumulate",
-            "data": "synthetic (seeded; see synth)", "config": config_of(args.workload, p, name),
+            "data": "synthetic (seeded; see synth)", "config": config_of(args.workload, g, name),
             "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps,
             "clocks": clk.summary(), "wall_s_timed_region": round(wall, 4),
             "host_us_per_launch": host_us,
             "plan": {k: info[k] for k in ("tile_m", "tile_n", "stages", "grid", "smem_bytes",
                                           "num_tiles")},
             "step_ms_min": round(min(times_ms), 5), "step_ms_median": round(statistics.median(times_ms), 5)}
+    if world > 1:
+        line["config"]["shard"] = {
+            "mode": args.shard, "ranks": world,
+            "rank0_piece": {"l0": piece.l0, "l1": piece.l1, "m0": piece.m0, "m1": piece.m1},
+            "exchange": "all-reduce (int32 max of the fp32 Amax bits) over NCCL, inside every "
+                        "timed step"}
     if rank == 0 and not args.no_cpu:
         cb, _, _ = oracle_sample(inp, args.cpu_seconds)
         line["cpu_baseline"] = cb
@@ -368,23 +446,31 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     return line
 
 
-def quant_numbers(rows, cols, in_dtype, out_dtype, sfv):
+def quant_numbers(rows, cols, in_dtype, out_dtype, sfv, direction="row"):
     x = rows * cols * (4 if in_dtype == "f32" else 2)
     codes = rows * cols // (2 if out_dtype == "e2m1" else 1)
-    sf = -(-rows // 128) * -(-(cols // sfv) // 4) * 512
+    if direction == "col":
+        sf = -(-cols // 128) * -(-(rows // sfv) // 4) * 512
+    else:
+        sf = -(-rows // 128) * -(-(cols // sfv) // 4) * 512
     return {"bytes": x + codes + sf, "h2d": x, "d2h": codes + sf}
 
 
-def quant_oracle_sample(X32, out_dtype, sfv, target_s: float):
-    """The oracle's quantizer (single thread), timed on the first r rows,
-    r sized for about target_s seconds."""
+def quant_oracle_sample(X32, out_dtype, sfv, target_s: float, direction="row"):
+    """The oracle's quantizer (single thread), timed on the first r rows
+    (whole 32-row blocks for the columnwise form), r sized for about
+    target_s seconds."""
     import oracle
+    step = 32 if direction == "col" else 1
+    fn = ((lambda x: oracle.quantize_colwise(x, out_dtype, sfv)) if direction == "col" else
+          (lambda x: oracle.quantize(x, out_dtype, sfv)))
     rows = min(X32.shape[1], 64)
     for attempt in range(3):
         t0 = time.perf_counter()
-        oracle.quantize(X32[:, :rows].astype(np.float64), out_dtype, sfv)
+        fn(X32[:, :rows].astype(np.float64))
         t = time.perf_counter() - t0
         want = int(min(X32.shape[1], max(1, (target_s / max(t, 1e-3)) * rows)))
+        want = max(step, want // step * step)
         if t >= 0.5 * target_s or want <= rows or attempt == 2:
             break
         rows = want
@@ -397,17 +483,18 @@ def run_quant(args, rank: int, world: int, local_rank: int):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    name, rows, cols, in_dtype, out_dtype, sfv = QWORKLOADS[args.qworkload]
-    X32 = synth.real_blocks(1, rows, cols, seed=1500 + args.qworkload, block=sfv)
+    name, rows, cols, in_dtype, out_dtype, sfv, direction = QWORKLOADS[args.qworkload]
+    gen = synth.real_blocks_colwise if direction == "col" else synth.real_blocks
+    X32 = gen(1, rows, cols, seed=1500 + args.qworkload, block=sfv)
     tdt = {"f32": torch.float32, "bf16": torch.bfloat16}[in_dtype]
     hX = torch.from_numpy(X32).to(tdt)
     X = hX.to(dev)
-    q = bsg.make_quant_problem(rows, cols, 1, in_dtype, out_dtype, sfv)
+    q = bsg.make_quant_problem(rows, cols, 1, in_dtype, out_dtype, sfv, direction)
     st, (cb, sb) = bsg.bsg_quant_sizes(q)
     bsg.check(st, "bsg_quant_sizes")
     codes = torch.empty(cb, dtype=torch.uint8, device=dev)
     sf = torch.empty(sb, dtype=torch.uint8, device=dev)
-    nums = quant_numbers(rows, cols, in_dtype, out_dtype, sfv)
+    nums = quant_numbers(rows, cols, in_dtype, out_dtype, sfv, direction)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
     s = stream.cuda_stream
@@ -472,23 +559,25 @@ def run_quant(args, rank: int, world: int, local_rank: int):
                 "unit": "GB/s", "frac": round(achieved / hbm, 4),
                 "traffic": TRAFFIC_Q.get((kernel_source_hash("quant.cu"), args.qworkload)),
                 "peak_source": f"{source} HBM copy bandwidth",
-                "kernel": "bsq_quantize_kernel"}
+                "kernel": "bsq_quantize_colwise_kernel" if direction == "col" else
+                          "bsq_quantize_kernel"}
     line = {"metric": QMETRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": f"{in_dtype} in, {out_dtype} codes + e8m0 scales out",
+            "dtype": f"{in_dtype} in, {out_dtype} codes + e8m0 scales out"
+                     f"{' (columnwise blocks)' if direction == 'col' else ''}",
             "data": "synthetic (seeded; see synth.real_blocks)",
             "config": {"workload": name, "rows": rows, "cols": cols, "L": 1, "in_dtype": in_dtype,
-                       "out_dtype": out_dtype, "sf_vec_size": sfv, "seed": 1500 + args.qworkload,
-                       "l2": L2_NOTE},
+                       "out_dtype": out_dtype, "sf_vec_size": sfv, "direction": direction,
+                       "seed": 1500 + args.qworkload, "l2": L2_NOTE},
             "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps,
             "clocks": clk.summary(), "wall_s_timed_region": round(wall, 4),
             "step_ms_min": round(min(times_ms), 5),
             "step_ms_median": round(statistics.median(times_ms), 5)}
     if rank == 0 and not args.no_cpu:
         r, t = quant_oracle_sample(X32 if in_dtype == "f32" else hX.float().numpy(), out_dtype, sfv,
-                                   args.cpu_seconds)
-        b = quant_numbers(r, cols, in_dtype, out_dtype, sfv)["bytes"]
+                                   args.cpu_seconds, direction)
+        b = quant_numbers(r, cols, in_dtype, out_dtype, sfv, direction)["bytes"]
         line["cpu_baseline"] = {"value": b / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
                                 "sample": f"rows 0..{r - 1} (all columns): {b / 1e6:.1f} MB "
                                           f"in {t:.1f} s, one thread, double precision"}
@@ -500,21 +589,23 @@ def run_quant(args, rank: int, world: int, local_rank: int):
 def run_quant_reference(args):
     """The oracle's quantizer, as it stands, on a bounded sample per step."""
     import oracle
-    name, rows, cols, in_dtype, out_dtype, sfv = QWORKLOADS[args.qworkload]
-    X32 = synth.real_blocks(1, rows, cols, seed=1500 + args.qworkload, block=sfv)
+    name, rows, cols, in_dtype, out_dtype, sfv, direction = QWORKLOADS[args.qworkload]
+    gen = synth.real_blocks_colwise if direction == "col" else synth.real_blocks
+    X32 = gen(1, rows, cols, seed=1500 + args.qworkload, block=sfv)
     if in_dtype == "bf16":
         import torch
         X32 = torch.from_numpy(X32).to(torch.bfloat16).float().numpy()
     per_step = max(0.5, args.ref_seconds / max(1, args.steps + args.warmup))
-    r, _ = quant_oracle_sample(X32, out_dtype, sfv, per_step)
+    r, _ = quant_oracle_sample(X32, out_dtype, sfv, per_step, direction)
     Xs = X32[:, :r].astype(np.float64)
+    fn = oracle.quantize_colwise if direction == "col" else oracle.quantize
     for _ in range(args.warmup):
-        oracle.quantize(Xs, out_dtype, sfv)
+        fn(Xs, out_dtype, sfv)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.quantize(Xs, out_dtype, sfv)
+        fn(Xs, out_dtype, sfv)
     t = time.perf_counter() - t0
-    b = quant_numbers(r, cols, in_dtype, out_dtype, sfv)["bytes"]
+    b = quant_numbers(r, cols, in_dtype, out_dtype, sfv, direction)["bytes"]
     value = b * args.steps / t / 1e9
     return {"metric": QMETRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t * 1e3 / args.steps, "higher_is_better": True,
@@ -561,12 +652,16 @@ def run_reference(args):
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=None,
+                    help="GPUs (one process each); unset: WORLD_SIZE, else 1")
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=2, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--op", choices=["gemm", "quantize"], default="gemm")
+    ap.add_argument("--shard", choices=["batches", "rows"], default="batches",
+                    help="N > 1: batches (each rank L batches of its own, weak scaling) or "
+                         "rows (the workload split in 128-row atoms, strong scaling)")
     ap.add_argument("--qworkload", type=int, default=1, choices=sorted(QWORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -576,9 +671,23 @@ def main(argv=None):
     if args.warmup < 3:
         args.warmup = 3  # timing rule: at least three warm-up steps
 
+    if "WORLD_SIZE" not in os.environ and (args.gpus or 1) > 1:
+        # one process per GPU: run this command under torch.distributed.run
+        import socket
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        argv = sys.argv[1:] if argv is None else list(argv)
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+               f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+               "--master-port", str(port), os.path.abspath(__file__), *argv]
+        return subprocess.call(cmd)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.gpus is not None and args.gpus != world:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+        return 2
 
     if args.impl == "reference":
         if rank == 0:

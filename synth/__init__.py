@@ -289,13 +289,16 @@ def quantized(p: Problem, seed: int, a_dist: str = "normal", b_dist: str = "norm
     return Inputs(p, to_major(A, p.a_major), to_major(B, p.b_major), SFA, SFB)
 
 
-def workload(number: int, **shape) -> Inputs:
+def workload(number: int, seed: int | None = None, **shape) -> Inputs:
     """Inputs of workload `number` (1..7).  Keyword overrides (M, N, K, L)
-    keep the recipe and change the shape (parity cases at reduced size)."""
+    keep the recipe and change the shape (parity cases at reduced size);
+    `seed` replaces the workload's own seed 1000 + number (the batches of
+    another rank of a sharded run)."""
     name, p = WORKLOADS[number]
     if shape:
         p = dataclasses.replace(p, **shape)
-    seed = 1000 + number
+    if seed is None:
+        seed = 1000 + number
     if number == 1:
         inp = uniform_codes(p, seed)
     elif number == 2:

@@ -114,3 +114,52 @@ def test_host_cost_is_a_burst_of_launches():
     us = bench.host_cost_us(lambda: calls.append(1), fake_torch, "dev", n=50)
     assert len(calls) == 50 and syncs == ["dev", "dev"]
     assert isinstance(us, float) and 0.0 <= us < 1e4
+
+
+def test_local_piece_single_gpu_is_the_workload():
+    import numpy as np
+    import synth
+    g, inp, piece = bench.local_piece(1, 1, 0, "batches")
+    assert piece is None and g == synth.WORKLOADS[1][1]
+    assert np.array_equal(inp.A, synth.workload(1).A)
+
+
+def test_local_piece_batches_weak_scaling():
+    """--shard batches: the global problem repeats the workload's L batches
+    once per rank; rank r owns batches [r L, (r+1) L), drawn from a seed of
+    its own (rank 0's are the workload itself)."""
+    import numpy as np
+    import synth
+    p = synth.WORKLOADS[1][1]
+    pieces = [bench.local_piece(1, 3, r, "batches") for r in range(3)]
+    for r, (g, inp, s) in enumerate(pieces):
+        assert g.L == 3 * p.L and (g.M, g.N, g.K) == (p.M, p.N, p.K)
+        assert (s.l0, s.l1, s.m0, s.m1) == (r * p.L, (r + 1) * p.L, 0, p.M)
+        assert inp.problem == p
+    assert np.array_equal(pieces[0][1].A, synth.workload(1).A)
+    assert not np.array_equal(pieces[0][1].A, pieces[1][1].A)
+    assert len({bench.batch_seed(1, r) for r in range(8)}) == 8
+
+
+def test_local_piece_rows_strong_scaling():
+    """--shard rows: the ranks split the workload's rows in whole 128-row
+    scale atoms; each piece is the workload's own rows and scale atoms."""
+    import numpy as np
+    import synth
+    full = synth.workload(1)
+    got = []
+    for r in range(2):
+        g, inp, s = bench.local_piece(1, 2, r, "rows")
+        assert g == full.problem and inp.problem.M == s.rows
+        assert np.array_equal(inp.A, full.A[:, s.m0:s.m1])
+        assert np.array_equal(inp.B, full.B) and np.array_equal(inp.SFB, full.SFB)
+        assert np.array_equal(inp.SFA, full.SFA[:, s.m0 // 128:-(-s.m1 // 128)])
+        got.append((s.m0, s.m1))
+    assert got == [(0, 128), (128, 256)]
+
+
+def test_gpus_flag_must_match_world_size(monkeypatch, capsys):
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "0")
+    assert bench.main(["--gpus", "4", "--impl", "reference"]) == 2
+    assert "WORLD_SIZE 2" in capsys.readouterr().err
