@@ -197,28 +197,15 @@ def test_run_host_end_to_end(p):
 # ------------------------------------------------------ full-size workloads
 
 @pytest.mark.parametrize("number", [1, 2, 3, 4, 5, 6, 7])
-def test_workload_full_size_sampled(number):
+def test_workload_full_size(number):
     """Each workload at its full size, in the benchmark's launch
-    configuration: the oracle at 4096 seeded points plus the corners, the
-    ragged tails and the GPU's argmax; Amax bit-equal to max |C_gpu|."""
+    configuration, against the whole oracle: every element of C within
+    tau = 1e-5 * sum_k |Ahat Bhat| + ulp_c(|C_ref|), Amax bit-equal to
+    max |C_gpu| and within max tau of the oracle's Amax.  (The oracle runs
+    over all host cores; 8192^3 FP4 takes about half a minute.)"""
     inp = synth.workload(number)
-    p = inp.problem
-    c, amax, *_ = run_gpu(inp)
-    assert np.float32(amax).view(np.uint32) == abs_max_bits(c)
-    arg = np.unravel_index(np.argmax(np.abs(c)), c.shape)  # (l, m, n)
-    extra = [(arg[1], arg[2], arg[0]), (p.M - 1, p.N - 1, p.L - 1), (p.M // 2, p.N - 1, 0)]
-    pts = synth.sample_points(p, 4096, 77 + number, extra)
-    cref, s = oracle.gemm_sample(p.M, p.N, p.K, p.L, p.a_dtype, p.b_dtype, p.sfv, inp.A,
-                                 inp.B, inp.SFA, inp.SFB, pts, sf_dtype=p.sf_dtype,
-                                 a_major=p.a_major, b_major=p.b_major)
-    cref = oracle.round_to(cref, p.c_dtype)
-    tau = oracle.tolerance(cref, s, p.c_dtype)
-    got = c[pts[:, 2], pts[:, 0], pts[:, 1]]
-    bad = ~(np.abs(got - cref) <= tau)
-    assert not bad.any(), [(tuple(pts[i]), got[i], cref[i], tau[i]) for i in np.flatnonzero(bad)[:8]]
-    # the GPU's maximum element is itself within tolerance of the oracle
-    i_arg = len(pts) - 3
-    assert abs(amax - abs(cref[i_arg])) <= tau[i_arg]
+    c, amax, _, op, _ = run_gpu(inp)
+    assert_parity(inp, c, amax)
 
 
 # ------------------------------------------------- tile-shape variants

@@ -3,6 +3,9 @@
 ABI into views of one C, then Amax reduced over the pieces.  The pieces are
 independent launches that never wait on one another.  The assembled C must
 pass the oracle parity check and the reduced Amax must equal max |C|."""
+import os
+import socket
+
 import numpy as np
 import pytest
 import torch
@@ -47,3 +50,36 @@ def test_sharded_pieces_assemble_the_whole(p, world):
     c_full = c_to_logical(C, p)
     assert np.float32(amax.item()).view(np.uint32) == abs_max_bits(c_full)
     assert_parity(inp, c_full, float(amax.item()))
+
+
+def _nccl_single_rank(rank, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    torch.cuda.set_device(0)
+    dist.init_process_group("nccl", rank=0, world_size=1, device_id=torch.device("cuda", 0))
+    try:
+        amax = torch.tensor([3.25], dtype=torch.float32, device="cuda:0")
+        sh.allreduce_amax(amax)
+        nan = torch.tensor([float("nan")], dtype=torch.float32, device="cuda:0")
+        sh.allreduce_amax(nan)
+        torch.cuda.synchronize()
+        out["amax"] = float(amax.item())
+        out["nan_bits"] = int(nan.view(torch.int32).item()) & 0xFFFFFFFF
+    finally:
+        dist.destroy_process_group()
+
+
+def test_nccl_allreduce_amax_single_rank():
+    """The multi-GPU exchange's own call path on NCCL: a one-rank group on
+    this GPU reduces the fp32 Amax as an int32 max in place (the value and a
+    NaN's bits come back unchanged).  Run in a spawned process so that the
+    group leaves no state behind."""
+    import torch.multiprocessing as mp
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    out = mp.get_context("spawn").Manager().dict()
+    mp.start_processes(_nccl_single_rank, args=(port, out), nprocs=1, join=True,
+                       start_method="spawn")
+    assert out["amax"] == 3.25
+    assert out["nan_bits"] == 0x7FC00000
