@@ -569,7 +569,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   // scale columns follow the accumulators, one set per smem stage, so that a
   // stage's tcgen05.st never rewrites columns an in-flight MMA still reads
   constexpr uint32_t kSfCols = 4 * kCps * (1 + G);
-  constexpr uint32_t kSfCol0 = NUM_ACC * TILE_N;
+  // FP8 256-wide tiles with one accumulator: consecutive units of a CTA
+  // alternate between two accumulator regions of tensor memory that share
+  // kOvlCols columns -- [kOvlCols, kOvlCols + 256) and [256, 512), the scale
+  // sets below them -- so the next unit's MMAs wait only until the epilogue
+  // has drained the shared columns, not the whole accumulator
+  constexpr bool kOvl = KIND == kKindF8F6F4 && TILE_N == 256 && NUM_ACC == 1;
+  constexpr uint32_t kOvlCols = 80;                       // 5 chunks of 16 columns
+  constexpr int kRegions = kOvl ? 2 : NUM_ACC;            // accumulator hand-off slots
+  constexpr uint32_t kSfCol0 = kOvl ? 0u : NUM_ACC * TILE_N;
+  static_assert(!kOvl || 2 * TILE_N <= kTmemCols, "regions fit");
+  // tensor-memory column of accumulator slot r
+  auto acc_col = [](int r) -> uint32_t {
+    return kOvl ? (r ? kTmemCols - TILE_N : kOvlCols) : static_cast<uint32_t>(r) * TILE_N;
+  };
   constexpr int kMmasPerStage = kSB / kMmaKBytes;
   constexpr int kMmasPerSlice = kStageKBytes / kMmaKBytes;
   // both CTAs of a pair: the targets of the leader's commit arrivals
@@ -597,10 +610,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // scale warp has put its scales in tensor memory), empty (stage free), sff
   // (scale bytes landed; issued first, off the A/B path)
   const uint32_t full0 = bar0, empty0 = bar0 + 8u * S, sff0 = bar0 + 16u * S;
-  const uint32_t accf0 = bar0 + 24u * S, acce0 = accf0 + 8u * NUM_ACC;
-  const uint32_t drain_bar = acce0 + 8u * NUM_ACC;
+  // per accumulator slot: accf (accumulator full), acce (fully drained),
+  // acco (its columns shared with the other region drained; kOvl only)
+  const uint32_t accf0 = bar0 + 24u * S, acce0 = accf0 + 8u * kRegions;
+  const uint32_t acco0 = acce0 + 8u * kRegions;
+  const uint32_t drain_bar = acco0 + 8u * kRegions;
   uint32_t* const misc =
-      reinterpret_cast<uint32_t*>(smem + p.smem_bar + 24u * S + 16u * NUM_ACC + 8u);
+      reinterpret_cast<uint32_t*>(smem + p.smem_bar + 24u * S + 24u * kRegions + 8u);
   uint32_t* const tmem_holder = misc + 0;
   volatile uint32_t* const abort_flag = misc + 1;
   uint32_t* const cta_amax = misc + 2;
@@ -615,9 +631,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(empty0 + 8u * s, 1);
       mbar_init(sff0 + 8u * s, 1);
     }
-    for (int b = 0; b < NUM_ACC; ++b) {
+    for (int b = 0; b < kRegions; ++b) {
       mbar_init(accf0 + 8u * b, 1);
       mbar_init(acce0 + 8u * b, PAIR ? 2 * kEpiWarps : kEpiWarps);  // one per epilogue warp
+      mbar_init(acco0 + 8u * b, PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0u;
@@ -771,10 +788,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int last = p.k_stages - 1;
       int last_nmma = (p.k_bytes - last * kSB + kMmaKBytes - 1) / kMmaKBytes;
       if (last_nmma > kMmasPerStage) last_nmma = kMmasPerStage;
+      uint32_t ovp0 = 0, ovp1 = 0;  // parity of the next shared-column release per slot
+      bool first_unit = true;
       for (int u = unit0; u < p.num_units && ok; u += unit_step) {
         if (!BSG_WAIT(acce0 + 8u * acc, acc_phase ^ 1u, 2)) { ok = false; break; }
+        if (kOvl && !first_unit) {
+          // the previous unit (in the other slot) has drained the columns the
+          // two regions share
+          const int other = acc ^ 1;
+          if (!BSG_WAIT(acco0 + 8u * other, other ? ovp1 : ovp0, 14)) { ok = false; break; }
+          if (other) ovp1 ^= 1u;
+          else ovp0 ^= 1u;
+        }
+        first_unit = false;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + acc * TILE_N;
+        const uint32_t d_tmem = tmem + acc_col(acc);
         // a half-width unit runs N = TILE_N / 2 from the first half of each
         // CTA's B rows into the first TILE_N / 2 accumulator columns
         const uint32_t id_u = kHalves && u >= p.full_units ? p.idesc_half : idesc;
@@ -823,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           else tc_commit(accf0 + 8u * acc);
         }
         __syncwarp();
-        if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1u; }
+        if (++acc == kRegions) { acc = 0; acc_phase ^= 1u; }
       }
       // drain: all MMAs issued by this warp complete before exit
       if (elected) {
@@ -933,223 +961,126 @@ __global__ void __launch_bounds__(kThreads, 1)
       // gives each warp half as many columns
       const bool hu = kHalves && tc.half >= 0;
       const int ucol0 = tc.nt * TILE_N + (hu ? tc.half * (TILE_N / 2) : 0);
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * TILE_N;
+      const int slot = acc;  // accumulator slot of this unit
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc_col(slot);
       const int row = tc.mt * kTileM + q * 32 + lane;
       const bool row_ok = row < p.M;
       const size_t batch_off = static_cast<size_t>(tc.l) * p.M * p.N;
-      const uint32_t release_bar = acce0 + 8u * acc;
-      if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1u; }
-      auto release = [&]() {
+      const uint32_t release_bar = acce0 + 8u * slot;
+      const uint32_t shared_bar = acco0 + 8u * slot;
+      if (++acc == kRegions) { acc = 0; acc_phase ^= 1u; }
+      // this warp is done reading the accumulator (release) or the columns
+      // its region shares with the other (release_shared, kOvl only)
+      auto arrive_on = [&](uint32_t bar) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if (PAIR) mbar_arrive_cluster(mapa_shared(release_bar, 0));
-          else mbar_arrive(release_bar);
+          if (PAIR) mbar_arrive_cluster(mapa_shared(bar, 0));
+          else mbar_arrive(bar);
         }
       };
-      // the unit's stores: CW accumulator columns per warp, a compile-time
-      // width (a runtime one spilled registers in these unrolled loops)
-      auto unit = [&](auto cw_tag) {
-        constexpr int CW = decltype(cw_tag)::value;  // columns of this warp in this unit
-        constexpr int kChU = CW / 16;                 // its 16-column chunks
-        const int n_end = min(p.N, ucol0 + 2 * CW);   // one past the unit's last stored column
-        const uint32_t taddr = tbase + h * CW;
-        const int n0 = ucol0 + h * CW;
-        // columns of this warp's part stored in this lane's row (may be <= 0)
-        const int lim = row_ok ? n_end - n0 : 0;
-        // one round of tensor-memory loads
-        uint32_t rb[kRnd][16];
-        if constexpr (LOWC) {
-          // FP8 or packed E2M1 C (FP4 operands only): each round of kRnd
-          // 16-column chunks is converted as it leaves tensor memory and
-          // stored at once (holding every code of the warp's columns until
-          // the end spilled registers); Amax is the rounded value of the
-          // largest stored magnitude (the rounding is monotone in |x|)
-          const bool fp4 = p.c_dtype == BSG_E2M1, e5 = p.c_dtype == BSG_E5M2;
-          constexpr int kRc = kRnd * 16;  // columns per round
-          uint8_t* const cbase = static_cast<uint8_t*>(p.c) + (fp4 ? batch_off / 2 : batch_off);
-          const int row0 = tc.mt * kTileM + q * 32;
-          const int ncols = row_ok ? min(CW, n_end - n0) : 0;  // m-major: stored columns
-#pragma unroll
-          for (int c0 = 0; c0 < kChU; c0 += kRnd) {
-#pragma unroll
-            for (int i = 0; i < kRnd; ++i)
-              if (c0 + i < kChU) tc_ld_32x32b_x16(taddr + (c0 + i) * 16, rb[i]);
-            tc_wait_ld();
-            // the last round's loads have landed: free the accumulator before
-            // converting them (the MMAs of the next unit wait for this)
-            if (c0 + kRnd >= kChU) release();
-            // the round's codes: four FP8 per word, or eight E2M1 (the first
-            // kRc / 8 words)
-            uint32_t pr[kRc / 4];
-#pragma unroll
-            for (int i = 0; i < kRnd; ++i) {
-              const int cc = (c0 + i) * 16;
-              const uint32_t* r = rb[i];
-              if (lim >= cc + 16) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  uint32_t a = r[j] & 0x7FFFFFFFu;
-                  if (fp4 && a > 0x7F800000u) a = 0u;  // stored as +0
-                  vmax = max(vmax, a);
-                }
-              } else {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  uint32_t a = r[j] & 0x7FFFFFFFu;
-                  if (fp4 && a > 0x7F800000u) a = 0u;
-                  if (cc + j >= lim) a = 0u;
-                  vmax = max(vmax, a);
-                }
-              }
-              if (fp4) {
-                uint32_t w0 = 0u, w1 = 0u;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const uint32_t b = cvt2_e2m1(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                  if (j < 4) w0 |= b << (8 * j);
-                  else w1 |= b << (8 * (j - 4));
-                }
-                pr[2 * i] = w0;
-                pr[2 * i + 1] = w1;
-              } else {
-#pragma unroll
-                for (int j = 0; j < 8; j += 2) {
-                  const float a0 = __uint_as_float(r[2 * j]), a1 = __uint_as_float(r[2 * j + 1]);
-                  const float b0 = __uint_as_float(r[2 * j + 2]), b1 = __uint_as_float(r[2 * j + 3]);
-                  const uint32_t lo = e5 ? cvt2_e5m2(a0, a1) : cvt2_e4m3(a0, a1);
-                  const uint32_t hi = e5 ? cvt2_e5m2(b0, b1) : cvt2_e4m3(b0, b1);
-                  pr[4 * i + j / 2] = lo | (hi << 16);
-                }
-              }
-            }
-            const int cr = c0 * 16;  // the round's first column in this warp's part
-            if (p.c_major == 0) {
-              if (fp4) {
-                // kRc / 2 bytes per row: one staged chunk of 8 words
-                char* const g = reinterpret_cast<char*>(
-                    cbase + static_cast<size_t>(row0) * (p.N / 2) + (n0 + cr) / 2);
-                store_rows_coalesced<kRc / 8>(stg, pr, lane, g, static_cast<size_t>(p.N / 2),
-                                              p.M - row0, (n_end - n0 - cr) / 2);
-              } else {
-                char* const g = reinterpret_cast<char*>(cbase + static_cast<size_t>(row0) * p.N + n0 + cr);
-                store_rows_coalesced<kRc / 4>(stg, pr, lane, g, static_cast<size_t>(p.N), p.M - row0,
-                                              n_end - n0 - cr);
-              }
-            } else {
-              // m-major FP8: column by column, the 32 lanes write 32 consecutive rows
-              uint8_t* dst = cbase + static_cast<size_t>(n0 + cr) * p.M + row;
-#pragma unroll
-              for (int j = 0; j < kRc; ++j) {
-                if (cr + j < ncols) *dst = static_cast<uint8_t>(pr[j / 4] >> (8 * (j % 4)));
-                dst += p.M;
-              }
-            }
-          }
-        } else if (p.c_dtype != BSG_F32) {
-          uint32_t pk[CW / 2];
-          // pk: two rounded 16-bit values per register
+      auto release = [&]() { arrive_on(release_bar); };
+      auto release_shared = [&]() { arrive_on(shared_bar); };
+      // kOvl units (FP8 operands, so 16-bit or fp32 C): warp h drains the
+      // unit's 16-column chunks h, h + 2, h + 4, ...; a whole unit in slot 0
+      // takes its chunks in the columns shared with slot 1 (its last 80:
+      // chunks 11..15) first, so that the first round of loads frees them
+      // (in slot 1 they are the first chunks already).  A half-width unit is
+      // always a CTA's last: no unit waits on its shared columns.
+      auto drain_overlapped = [&](auto cw_tag, int n_end) {
+        constexpr int CW = decltype(cw_tag)::value;
+        constexpr int kNch = CW / 16;  // chunks of this warp: 8, or 4 in a half-width unit
+        static_assert(kNch == 8 || kNch == 4, "whole or half 256-wide unit");
+        const int rot = (CW == kCols && slot == 0) ? (h ? 5 : 6) : 0;
+        // the unit column of drain slot s
+        auto col_of = [&](int s_) { return 16 * (2 * ((rot + s_) & (kNch - 1)) + h); };
+        const int row0 = tc.mt * kTileM + q * 32;
+        if (p.c_dtype != BSG_F32) {
+          // 16-bit C: each round of chunks rounded, packed and stored as it
+          // leaves tensor memory.  Only the first round's release (the shared
+          // columns) is on the next unit's path; the full release is needed
+          // one unit later, so the rounds need not all stay in registers.
+          uint32_t rb[kRnd][16];
           const bool bf = p.c_dtype == BSG_BF16;
-          // rounds of kRnd 16-column loads: all of a round in flight at once,
-          // one wait, then its conversions (fewer waits than one load ahead)
+          uint16_t* const cbase = static_cast<uint16_t*>(p.c) + batch_off;
 #pragma unroll
-          for (int c0 = 0; c0 < kChU; c0 += kRnd) {
+          for (int c0 = 0; c0 < kNch; c0 += kRnd) {
 #pragma unroll
-            for (int i = 0; i < kRnd; ++i)
-              if (c0 + i < kChU) tc_ld_32x32b_x16(taddr + (c0 + i) * 16, rb[i]);
+            for (int i = 0; i < kRnd; ++i) tc_ld_32x32b_x16(tbase + col_of(c0 + i), rb[i]);
             tc_wait_ld();
-            // the last round's loads have landed: free the accumulator before
-            // converting them (the MMAs of the next unit wait for this)
-            if (c0 + kRnd >= kChU) release();
+            if (c0 == 0) release_shared();
+            if (c0 + kRnd >= kNch) release();
 #pragma unroll
             for (int i = 0; i < kRnd; ++i) {
-              if (c0 + i >= kChU) continue;
-              const int cc = (c0 + i) * 16;
               const uint32_t* r = rb[i];
+              uint32_t w[8];
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
                 const float f0 = __uint_as_float(r[2 * j]), f1 = __uint_as_float(r[2 * j + 1]);
-                // two round-to-nearest-even conversions in one: low half column
-                // cc + 2j, high half column cc + 2j + 1
-                uint32_t h;
                 if (bf) {
                   const __nv_bfloat162 v = __floats2bfloat162_rn(f0, f1);
-                  h = *reinterpret_cast<const uint32_t*>(&v);
+                  w[j] = *reinterpret_cast<const uint32_t*>(&v);
                 } else {
                   const __half2 v = __floats2half2_rn(f0, f1);
-                  h = *reinterpret_cast<const uint32_t*>(&v);
+                  w[j] = *reinterpret_cast<const uint32_t*>(&v);
                 }
-                pk[cc / 2 + j] = h;
               }
-              // only stored elements count toward Amax: a whole chunk without
-              // per-element tests (which made the drain four times slower),
-              // the ragged edge with them
-              if (lim >= cc + 16) {
+              const int col = ucol0 + col_of(c0 + i);
+              // only stored elements count toward Amax
+              const int nv = row_ok ? n_end - col : 0;
+              if (nv >= 16) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) vmax = __vmaxu2(vmax, pk[cc / 2 + j] & 0x7FFF7FFFu);
+                for (int j = 0; j < 8; ++j) vmax = __vmaxu2(vmax, w[j] & 0x7FFF7FFFu);
               } else {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                  uint32_t m = pk[cc / 2 + j] & 0x7FFF7FFFu;
-                  if (cc + 2 * j >= lim) m &= 0xFFFF0000u;
-                  if (cc + 2 * j + 1 >= lim) m &= 0x0000FFFFu;
+                  uint32_t m = w[j] & 0x7FFF7FFFu;
+                  if (2 * j >= nv) m &= 0xFFFF0000u;
+                  if (2 * j + 1 >= nv) m &= 0x0000FFFFu;
                   vmax = __vmaxu2(vmax, m);
+                }
+              }
+              if (p.c_major == 0) {
+                // 32 rows x 32 bytes through the staging buffer
+                char* const g = reinterpret_cast<char*>(cbase + static_cast<size_t>(row0) * p.N + col);
+                store_rows_coalesced<8>(stg, w, lane, g, static_cast<size_t>(p.N) * 2, p.M - row0,
+                                        (n_end - col) * 2);
+              } else {
+                // m-major: column by column, the 32 lanes write 32 consecutive rows
+                uint16_t* dst = cbase + static_cast<size_t>(col) * p.M + row;
+                const int ncols = row_ok ? min(16, n_end - col) : 0;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  if (j < ncols)
+                    *dst = static_cast<uint16_t>((j & 1) ? (w[j / 2] >> 16) : (w[j / 2] & 0xFFFFu));
+                  dst += p.M;
                 }
               }
             }
           }
-          uint16_t* const cbase = static_cast<uint16_t*>(p.c) + batch_off;
-          if (p.c_major == 0) {
-            // 32-column chunks (64 bytes per row) through the staging buffer;
-            // a 112-column half ends with a 16-column chunk
-            const int row0 = tc.mt * kTileM + q * 32;
-            char* const g0 = reinterpret_cast<char*>(cbase + static_cast<size_t>(row0) * p.N + n0);
-            const size_t pitch = static_cast<size_t>(p.N) * 2;
-#pragma unroll
-            for (int cc = 0; cc + 32 <= CW; cc += 32)
-              if (cc < CW)
-                store_rows_coalesced<16>(stg, pk + cc / 2, lane, g0 + cc * 2, pitch, p.M - row0,
-                                         (n_end - n0 - cc) * 2);
-            if (CW % 32 == 16)  // (never a half-width unit: those come from 256-wide tiles)
-              store_rows_coalesced<8>(stg, pk + (CW - 16) / 2, lane, g0 + (CW - 16) * 2, pitch,
-                                      p.M - row0, (n_end - n0 - (CW - 16)) * 2);
-          } else {
-            // m-major: column by column, the 32 lanes write 32 consecutive rows
-            uint16_t* dst = cbase + static_cast<size_t>(n0) * p.M + row;
-            const int ncols = row_ok ? min(CW, n_end - n0) : 0;
-#pragma unroll
-            for (int j = 0; j < CW; ++j) {
-              if (j < ncols)
-                *dst = static_cast<uint16_t>((j & 1) ? (pk[j / 2] >> 16) : (pk[j / 2] & 0xFFFFu));
-              dst += p.M;
-            }
-          }
         } else {
+          // fp32 C: the first half of the slots in registers; each goes out
+          // (n-major through the staging buffer, m-major column by column)
+          // and the second half's chunk is loaded into its registers
           float* const cbase = static_cast<float*>(p.c) + batch_off;
-          constexpr int kCh = CW / 16;         // 16-column chunks of this warp
-          constexpr int kP1 = (kCh + 1) / 2;   // chunks held in registers at once
-          constexpr int kP2 = kCh - kP1;       // the rest, loaded as the first go out
-          // chunk ci (its 16 values in rr): Amax of the stored elements, then
-          // the stores -- n-major through the staging buffer (64 bytes per
-          // row), m-major column by column (32 consecutive rows per store)
-          auto chunk_out = [&](int ci, const uint32_t* rr) {
-            const int nb = n0 + 16 * ci;
-            if (row_ok && nb + 16 <= n_end) {
+          constexpr int kP1 = kNch / 2;
+          auto chunk_out = [&](int col, const uint32_t* rr) {
+            const int nv = n_end - col;  // the chunk's stored columns
+            if (row_ok && nv >= 16) {
 #pragma unroll
               for (int j = 0; j < 16; ++j) vmax = max(vmax, rr[j] & 0x7FFFFFFFu);
             } else {
 #pragma unroll
               for (int j = 0; j < 16; ++j)
-                if (row_ok && nb + j < n_end) vmax = max(vmax, rr[j] & 0x7FFFFFFFu);
+                if (row_ok && j < nv) vmax = max(vmax, rr[j] & 0x7FFFFFFFu);
             }
             if (p.c_major == 0) {
-              const int row0 = tc.mt * kTileM + q * 32;
-              char* const g = reinterpret_cast<char*>(cbase + static_cast<size_t>(row0) * p.N + nb);
+              char* const g = reinterpret_cast<char*>(cbase + static_cast<size_t>(row0) * p.N + col);
               store_rows_coalesced<16>(stg, rr, lane, g, static_cast<size_t>(p.N) * 4, p.M - row0,
-                                       (n_end - nb) * 4);
+                                       nv * 4);
             } else {
-              float* dst = cbase + static_cast<size_t>(nb) * p.M + row;
-              const int ncols = row_ok ? min(16, n_end - nb) : 0;
+              float* dst = cbase + static_cast<size_t>(col) * p.M + row;
+              const int ncols = row_ok ? min(16, nv) : 0;
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 if (j < ncols) *dst = __uint_as_float(rr[j]);
@@ -1159,22 +1090,254 @@ __global__ void __launch_bounds__(kThreads, 1)
           };
           uint32_t r[kP1 * 16];
 #pragma unroll
-          for (int i = 0; i < kP1; ++i) tc_ld_32x32b_x16(taddr + i * 16, r + 16 * i);
+          for (int i = 0; i < kP1; ++i) tc_ld_32x32b_x16(tbase + col_of(i), r + 16 * i);
           tc_wait_ld();
-          if (kP2 == 0) release();
-          // each first chunk out, then the second half's chunk loaded into its
-          // registers: the loads overlap the stores, and the accumulator is
-          // freed as soon as the last of them lands
+          // a whole unit's shared chunks are among its first kP1 slots
+          if (CW == kCols) release_shared();
 #pragma unroll
           for (int i = 0; i < kP1; ++i) {
-            chunk_out(i, r + 16 * i);
-            if (i < kP2) tc_ld_32x32b_x16(taddr + (kP1 + i) * 16, r + 16 * i);
+            chunk_out(ucol0 + col_of(i), r + 16 * i);
+            tc_ld_32x32b_x16(tbase + col_of(kP1 + i), r + 16 * i);
           }
-          if (kP2 > 0) {
-            tc_wait_ld();
-            release();
+          tc_wait_ld();
+          if (CW != kCols) release_shared();
+          release();
 #pragma unroll
-            for (int i = 0; i < kP2; ++i) chunk_out(kP1 + i, r + 16 * i);
+          for (int i = 0; i < kP1; ++i) chunk_out(ucol0 + col_of(kP1 + i), r + 16 * i);
+        }
+      };
+      // the unit's stores: CW accumulator columns per warp, a compile-time
+      // width (a runtime one spilled registers in these unrolled loops)
+      auto unit = [&](auto cw_tag) {
+        constexpr int CW = decltype(cw_tag)::value;  // columns of this warp in this unit
+        const int n_end = min(p.N, ucol0 + 2 * CW);   // one past the unit's last stored column
+        if constexpr (kOvl) {
+          drain_overlapped(std::integral_constant<int, CW>{}, n_end);
+        } else {
+          constexpr int kChU = CW / 16;                 // its 16-column chunks
+          const uint32_t taddr = tbase + h * CW;
+          const int n0 = ucol0 + h * CW;
+          // columns of this warp's part stored in this lane's row (may be <= 0)
+          const int lim = row_ok ? n_end - n0 : 0;
+          // one round of tensor-memory loads
+          uint32_t rb[kRnd][16];
+          if constexpr (LOWC) {
+            // FP8 or packed E2M1 C (FP4 operands only): each round of kRnd
+            // 16-column chunks is converted as it leaves tensor memory and
+            // stored at once (holding every code of the warp's columns until
+            // the end spilled registers); Amax is the rounded value of the
+            // largest stored magnitude (the rounding is monotone in |x|)
+            const bool fp4 = p.c_dtype == BSG_E2M1, e5 = p.c_dtype == BSG_E5M2;
+            constexpr int kRc = kRnd * 16;  // columns per round
+            uint8_t* const cbase = static_cast<uint8_t*>(p.c) + (fp4 ? batch_off / 2 : batch_off);
+            const int row0 = tc.mt * kTileM + q * 32;
+            const int ncols = row_ok ? min(CW, n_end - n0) : 0;  // m-major: stored columns
+  #pragma unroll
+            for (int c0 = 0; c0 < kChU; c0 += kRnd) {
+  #pragma unroll
+              for (int i = 0; i < kRnd; ++i)
+                if (c0 + i < kChU) tc_ld_32x32b_x16(taddr + (c0 + i) * 16, rb[i]);
+              tc_wait_ld();
+              // the last round's loads have landed: free the accumulator before
+              // converting them (the MMAs of the next unit wait for this)
+              if (c0 + kRnd >= kChU) release();
+              // the round's codes: four FP8 per word, or eight E2M1 (the first
+              // kRc / 8 words)
+              uint32_t pr[kRc / 4];
+  #pragma unroll
+              for (int i = 0; i < kRnd; ++i) {
+                const int cc = (c0 + i) * 16;
+                const uint32_t* r = rb[i];
+                if (lim >= cc + 16) {
+  #pragma unroll
+                  for (int j = 0; j < 16; ++j) {
+                    uint32_t a = r[j] & 0x7FFFFFFFu;
+                    if (fp4 && a > 0x7F800000u) a = 0u;  // stored as +0
+                    vmax = max(vmax, a);
+                  }
+                } else {
+  #pragma unroll
+                  for (int j = 0; j < 16; ++j) {
+                    uint32_t a = r[j] & 0x7FFFFFFFu;
+                    if (fp4 && a > 0x7F800000u) a = 0u;
+                    if (cc + j >= lim) a = 0u;
+                    vmax = max(vmax, a);
+                  }
+                }
+                if (fp4) {
+                  uint32_t w0 = 0u, w1 = 0u;
+  #pragma unroll
+                  for (int j = 0; j < 8; ++j) {
+                    const uint32_t b = cvt2_e2m1(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                    if (j < 4) w0 |= b << (8 * j);
+                    else w1 |= b << (8 * (j - 4));
+                  }
+                  pr[2 * i] = w0;
+                  pr[2 * i + 1] = w1;
+                } else {
+  #pragma unroll
+                  for (int j = 0; j < 8; j += 2) {
+                    const float a0 = __uint_as_float(r[2 * j]), a1 = __uint_as_float(r[2 * j + 1]);
+                    const float b0 = __uint_as_float(r[2 * j + 2]), b1 = __uint_as_float(r[2 * j + 3]);
+                    const uint32_t lo = e5 ? cvt2_e5m2(a0, a1) : cvt2_e4m3(a0, a1);
+                    const uint32_t hi = e5 ? cvt2_e5m2(b0, b1) : cvt2_e4m3(b0, b1);
+                    pr[4 * i + j / 2] = lo | (hi << 16);
+                  }
+                }
+              }
+              const int cr = c0 * 16;  // the round's first column in this warp's part
+              if (p.c_major == 0) {
+                if (fp4) {
+                  // kRc / 2 bytes per row: one staged chunk of 8 words
+                  char* const g = reinterpret_cast<char*>(
+                      cbase + static_cast<size_t>(row0) * (p.N / 2) + (n0 + cr) / 2);
+                  store_rows_coalesced<kRc / 8>(stg, pr, lane, g, static_cast<size_t>(p.N / 2),
+                                                p.M - row0, (n_end - n0 - cr) / 2);
+                } else {
+                  char* const g = reinterpret_cast<char*>(cbase + static_cast<size_t>(row0) * p.N + n0 + cr);
+                  store_rows_coalesced<kRc / 4>(stg, pr, lane, g, static_cast<size_t>(p.N), p.M - row0,
+                                                n_end - n0 - cr);
+                }
+              } else {
+                // m-major FP8: column by column, the 32 lanes write 32 consecutive rows
+                uint8_t* dst = cbase + static_cast<size_t>(n0 + cr) * p.M + row;
+  #pragma unroll
+                for (int j = 0; j < kRc; ++j) {
+                  if (cr + j < ncols) *dst = static_cast<uint8_t>(pr[j / 4] >> (8 * (j % 4)));
+                  dst += p.M;
+                }
+              }
+            }
+          } else if (p.c_dtype != BSG_F32) {
+            uint32_t pk[CW / 2];
+            // pk: two rounded 16-bit values per register
+            const bool bf = p.c_dtype == BSG_BF16;
+            // rounds of kRnd 16-column loads: all of a round in flight at once,
+            // one wait, then its conversions (fewer waits than one load ahead)
+  #pragma unroll
+            for (int c0 = 0; c0 < kChU; c0 += kRnd) {
+  #pragma unroll
+              for (int i = 0; i < kRnd; ++i)
+                if (c0 + i < kChU) tc_ld_32x32b_x16(taddr + (c0 + i) * 16, rb[i]);
+              tc_wait_ld();
+              // the last round's loads have landed: free the accumulator before
+              // converting them (the MMAs of the next unit wait for this)
+              if (c0 + kRnd >= kChU) release();
+  #pragma unroll
+              for (int i = 0; i < kRnd; ++i) {
+                if (c0 + i >= kChU) continue;
+                const int cc = (c0 + i) * 16;
+                const uint32_t* r = rb[i];
+  #pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float f0 = __uint_as_float(r[2 * j]), f1 = __uint_as_float(r[2 * j + 1]);
+                  // two round-to-nearest-even conversions in one: low half column
+                  // cc + 2j, high half column cc + 2j + 1
+                  uint32_t h;
+                  if (bf) {
+                    const __nv_bfloat162 v = __floats2bfloat162_rn(f0, f1);
+                    h = *reinterpret_cast<const uint32_t*>(&v);
+                  } else {
+                    const __half2 v = __floats2half2_rn(f0, f1);
+                    h = *reinterpret_cast<const uint32_t*>(&v);
+                  }
+                  pk[cc / 2 + j] = h;
+                }
+                // only stored elements count toward Amax: a whole chunk without
+                // per-element tests (which made the drain four times slower),
+                // the ragged edge with them
+                if (lim >= cc + 16) {
+  #pragma unroll
+                  for (int j = 0; j < 8; ++j) vmax = __vmaxu2(vmax, pk[cc / 2 + j] & 0x7FFF7FFFu);
+                } else {
+  #pragma unroll
+                  for (int j = 0; j < 8; ++j) {
+                    uint32_t m = pk[cc / 2 + j] & 0x7FFF7FFFu;
+                    if (cc + 2 * j >= lim) m &= 0xFFFF0000u;
+                    if (cc + 2 * j + 1 >= lim) m &= 0x0000FFFFu;
+                    vmax = __vmaxu2(vmax, m);
+                  }
+                }
+              }
+            }
+            uint16_t* const cbase = static_cast<uint16_t*>(p.c) + batch_off;
+            if (p.c_major == 0) {
+              // 32-column chunks (64 bytes per row) through the staging buffer;
+              // a 112-column half ends with a 16-column chunk
+              const int row0 = tc.mt * kTileM + q * 32;
+              char* const g0 = reinterpret_cast<char*>(cbase + static_cast<size_t>(row0) * p.N + n0);
+              const size_t pitch = static_cast<size_t>(p.N) * 2;
+  #pragma unroll
+              for (int cc = 0; cc + 32 <= CW; cc += 32)
+                if (cc < CW)
+                  store_rows_coalesced<16>(stg, pk + cc / 2, lane, g0 + cc * 2, pitch, p.M - row0,
+                                           (n_end - n0 - cc) * 2);
+              if (CW % 32 == 16)  // (never a half-width unit: those come from 256-wide tiles)
+                store_rows_coalesced<8>(stg, pk + (CW - 16) / 2, lane, g0 + (CW - 16) * 2, pitch,
+                                        p.M - row0, (n_end - n0 - (CW - 16)) * 2);
+            } else {
+              // m-major: column by column, the 32 lanes write 32 consecutive rows
+              uint16_t* dst = cbase + static_cast<size_t>(n0) * p.M + row;
+              const int ncols = row_ok ? min(CW, n_end - n0) : 0;
+  #pragma unroll
+              for (int j = 0; j < CW; ++j) {
+                if (j < ncols)
+                  *dst = static_cast<uint16_t>((j & 1) ? (pk[j / 2] >> 16) : (pk[j / 2] & 0xFFFFu));
+                dst += p.M;
+              }
+            }
+          } else {
+            float* const cbase = static_cast<float*>(p.c) + batch_off;
+            constexpr int kCh = CW / 16;         // 16-column chunks of this warp
+            constexpr int kP1 = (kCh + 1) / 2;   // chunks held in registers at once
+            constexpr int kP2 = kCh - kP1;       // the rest, loaded as the first go out
+            // chunk ci (its 16 values in rr): Amax of the stored elements, then
+            // the stores -- n-major through the staging buffer (64 bytes per
+            // row), m-major column by column (32 consecutive rows per store)
+            auto chunk_out = [&](int ci, const uint32_t* rr) {
+              const int nb = n0 + 16 * ci;
+              if (row_ok && nb + 16 <= n_end) {
+  #pragma unroll
+                for (int j = 0; j < 16; ++j) vmax = max(vmax, rr[j] & 0x7FFFFFFFu);
+              } else {
+  #pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  if (row_ok && nb + j < n_end) vmax = max(vmax, rr[j] & 0x7FFFFFFFu);
+              }
+              if (p.c_major == 0) {
+                const int row0 = tc.mt * kTileM + q * 32;
+                char* const g = reinterpret_cast<char*>(cbase + static_cast<size_t>(row0) * p.N + nb);
+                store_rows_coalesced<16>(stg, rr, lane, g, static_cast<size_t>(p.N) * 4, p.M - row0,
+                                         (n_end - nb) * 4);
+              } else {
+                float* dst = cbase + static_cast<size_t>(nb) * p.M + row;
+                const int ncols = row_ok ? min(16, n_end - nb) : 0;
+  #pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  if (j < ncols) *dst = __uint_as_float(rr[j]);
+                  dst += p.M;
+                }
+              }
+            };
+            uint32_t r[kP1 * 16];
+  #pragma unroll
+            for (int i = 0; i < kP1; ++i) tc_ld_32x32b_x16(taddr + i * 16, r + 16 * i);
+            tc_wait_ld();
+            if (kP2 == 0) release();
+            // each first chunk out, then the second half's chunk loaded into its
+            // registers: the loads overlap the stores, and the accumulator is
+            // freed as soon as the last of them lands
+  #pragma unroll
+            for (int i = 0; i < kP1; ++i) {
+              chunk_out(i, r + 16 * i);
+              if (i < kP2) tc_ld_32x32b_x16(taddr + (kP1 + i) * 16, r + 16 * i);
+            }
+            if (kP2 > 0) {
+              tc_wait_ld();
+              release();
+  #pragma unroll
+              for (int i = 0; i < kP2; ++i) chunk_out(kP1 + i, r + 16 * i);
+            }
           }
         }
       };
@@ -1535,8 +1698,15 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   int stages = (max_smem - reserve) / per_stage;
   if (stages > 8) stages = 8;
   const int sf_cols = 4 * chunks * ksl * (1 + G);
-  while (stages > 2 && num_acc * k.tile_n + stages * sf_cols > static_cast<int>(kTmemCols)) --stages;
-  if (stages < 2 || num_acc * k.tile_n + stages * sf_cols > static_cast<int>(kTmemCols)) {
+  // FP8 256-wide tiles with one accumulator use two overlapping accumulator
+  // regions above the scale sets, which must fit in the 80 columns below
+  const bool ovl = kind == kKindF8F6F4 && k.tile_n == 256 && num_acc == 1;
+  const int tmem_need_acc = ovl ? 2 * k.tile_n - 80 : num_acc * k.tile_n;
+  if (ovl)
+    while (stages > 2 && stages * sf_cols > 80) --stages;
+  while (stages > 2 && tmem_need_acc + stages * sf_cols > static_cast<int>(kTmemCols)) --stages;
+  if (stages < 2 || tmem_need_acc + stages * sf_cols > static_cast<int>(kTmemCols) ||
+      (ovl && stages * sf_cols > 80)) {
     delete plan;
     return BSG_ERR_UNSUPPORTED;
   }
@@ -1547,7 +1717,9 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   k.smem_sfb = k.smem_sfa + stages * sfa_stage;
   k.smem_epi = k.smem_sfb + stages * sfb_stage;
   k.smem_bar = k.smem_epi + kEpiWarps * kEpiStageBytes;
-  plan->smem_bytes = static_cast<int>(k.smem_bar) + 24 * stages + 16 * num_acc + 8 + 16 + 1024;
+  // barriers: 3 per stage, 3 per accumulator slot (at most 2), the drain
+  // barrier, then the flags; then the alignment slack
+  plan->smem_bytes = static_cast<int>(k.smem_bar) + 24 * stages + 48 + 8 + 16 + 1024;
   k.wait_limit_ns = 1000000000ull;  // one second per wait
   if (const char* e = std::getenv("BSG_WAIT_LIMIT_NS")) {
     const unsigned long long v = std::strtoull(e, nullptr, 10);
