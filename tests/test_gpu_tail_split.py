@@ -39,17 +39,29 @@ def test_plan_splits_the_last_wave(M, N, L):
     """half_tiles = the tiles past the full waves, when they fill at most
     half of the resident pairs; else none."""
     G = pairs_resident()
-    op = bsg.GemmAmax(problem_of(P(M, N, 512, L)))
+    op = bsg.GemmAmax(problem_of(P(M, N, 512, L), tile_n=256))
     info = op.describe()
     units = -(-M // 256) * -(-N // 256) * L
     assert info["tile_n"] == 256 and info["cluster_m"] == 2
     assert info["half_tiles"] == expected_half_tiles(units, G), (units, G, info)
 
 
+def test_small_problems_take_128_wide_single_ctas():
+    """With no hints, a problem whose 128 x 128 tiles fill at most half of
+    the SMs runs as 128-wide single CTAs (latency-bound work); a larger one
+    as 256-wide pairs."""
+    op = bsg.GemmAmax(problem_of(P(256, 256, 256)))
+    info = op.describe()
+    assert info["tile_n"] == 128 and info["cluster_m"] == 1
+    op = bsg.GemmAmax(problem_of(P(4096, 4096, 512)))
+    info = op.describe()
+    assert info["tile_n"] == 256 and info["cluster_m"] == 2
+
+
 def test_no_split_for_single_ctas_or_n_major_b():
     op = bsg.GemmAmax(problem_of(P(512, 768, 256), tile_n=256, cluster_m=1))
     assert op.describe()["half_tiles"] == 0
-    op = bsg.GemmAmax(problem_of(P(512, 768, 256, bm="n")))
+    op = bsg.GemmAmax(problem_of(P(512, 768, 256, bm="n"), tile_n=256, cluster_m=2))
     assert op.describe()["half_tiles"] == 0
 
 
@@ -77,7 +89,7 @@ CASES = [
 def test_split_parity(p):
     inp = synth.uniform_codes(p, p.M + p.N + p.K + p.L, 123, 131) if p.sf_dtype == "ue8m0" \
         else synth.uniform_codes(p, p.M + p.N + p.K + p.L, 0x2C, 0x44)
-    c, amax, _, op, guard_ok = run_gpu(inp, guard=4096)
+    c, amax, _, op, guard_ok = run_gpu(inp, guard=4096, tile_n=256)
     assert op.describe()["half_tiles"] > 0
     assert guard_ok, "write outside C"
     assert_parity(inp, c, amax)
@@ -89,7 +101,7 @@ def test_split_matches_the_unsplit_single_cta_plan():
     Amax each equal to max |C| of their own C."""
     p = P(512, 256 * 43, 256, c="f32")
     inp = synth.uniform_codes(p, 77, 123, 131)
-    c1, a1, _, op1, _ = run_gpu(inp)
+    c1, a1, _, op1, _ = run_gpu(inp, tile_n=256)
     c2, a2, _, op2, _ = run_gpu(inp, tile_n=256, cluster_m=1)
     assert op1.describe()["half_tiles"] > 0 and op2.describe()["half_tiles"] == 0
     ref = assert_parity(inp, c1, a1)
