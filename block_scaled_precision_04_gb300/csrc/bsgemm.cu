@@ -14,7 +14,8 @@
 //               the B tile (its half in a pair, always whole 128-row boxes)
 //               through 3-D tensor maps (128-byte swizzle, out-of-range rows
 //               and columns zero-filled).  In a pair both CTAs count their
-//               bytes on the leader's stage barrier.
+//               bytes on the leader's stage barrier, which counts copies
+//               alone.
 //   warp 1      MMA issuer (the leader's, in a pair): once a stage is ready,
 //               block-scaled tcgen05.mma (kind::mxf8f6f4 scale_vec::1X for
 //               FP8, kind::mxf4nvf4 scale_vec::4X / 2X for packed FP4) into
@@ -22,7 +23,8 @@
 //               and publish a finished accumulator.
 //   warps 2..5  scale warps: tcgen05.st of each stage's scale atoms from
 //               shared into tensor memory (one warp per lane quarter), then
-//               an arrival on the stage barrier.
+//               an arrival on the stage's scale barrier, which the MMA tests
+//               together with the operand barrier.
 //   warps 6..13 epilogue: tcgen05.ld the accumulator (one row per thread),
 //               round to C's dtype, keep max |stored value| as an integer max
 //               of the float bits, store through a per-warp staging buffer.
@@ -32,7 +34,8 @@
 //
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
 // an error word in the workspace, stops its pipeline, drains in-flight
-// copies and MMAs, frees tensor memory and returns.
+// copies and MMAs, frees tensor memory and returns.  The drains wait on the
+// barriers the copies and MMAs complete on, so they end as soon as those do.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -176,9 +179,15 @@ __device__ __forceinline__ uint32_t cluster_count_x() {
   asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ void cluster_sync() {
+__device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  cluster_arrive();
+  cluster_wait();
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -213,6 +222,24 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
+}
+
+// Complete `bytes` of the current phase's transaction count without arriving
+// (the drain's stand-in for copies that were never issued).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// A 32-bit store into the shared memory of another CTA of the cluster.
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// Arrive on an mbarrier anywhere in the cluster, releasing this thread's
+// earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster_release(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
 }
 
 // Arrive on an mbarrier anywhere in the cluster (default semantics).
@@ -394,6 +421,21 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Both phases complete (two independent tests in flight at once).
+__device__ __forceinline__ bool mbar_test_wait2(uint32_t bar_a, uint32_t bar_b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred pa, pb;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 pa, [%1], %3;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 pb, [%2], %3;\n\t"
+      "and.pred pa, pa, pb;\n\t"
+      "selp.u32 %0, 1, 0, pa;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_a), "r"(bar_b), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded slow path of a wait.  Returns false when the pipeline is abandoned.
 // Polls with test_wait: warps parked in a blocking try_wait measurably slow
 // the MMA issuer sharing their SM.  `sleep_ns` > 0 (warps off the critical
@@ -429,6 +471,11 @@ __device__ __forceinline__ uint32_t epi_barrier_and(uint32_t v) {
       : "r"(v)
       : "memory");
   return r;
+}
+
+// Named barrier `id` over `count` threads (whole warps).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("barrier.cta.sync.aligned %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Fast path inline: one test_wait; the bounded loop only when the phase is open.
@@ -605,27 +652,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int unit_step = CM > 1 ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
 
   const uint32_t bar0 = base + p.smem_bar;
-  // per stage: full (the stage is ready for the MMA: its A/B bytes -- of
-  // both CTAs of a pair, counted in the leader -- have landed and every
-  // scale warp has put its scales in tensor memory), empty (stage free), sff
-  // (scale bytes landed; issued first, off the A/B path)
+  // per stage:
+  //   full  the stage's A/B bytes have landed -- of both CTAs of a pair,
+  //         counted in the leader (the leader's expect_tx, both CTAs' copies)
+  //   empty the stage is free (the MMA commit; in a pair, in both CTAs)
+  //   sff   this CTA's scale bytes have landed (issued first, off the A/B path)
+  //   sfr   every scale warp has put the stage's scales in tensor memory (in
+  //         the leader; four per CTA)
+  //   pd    (second CTA of a pair, at the exit drain) the leader has seen the
+  //         stage's bytes land
+  // The MMA waits sfr and full.  full counts copies alone, so a producer's
+  // exit drain can wait on it for the copies it issued, whatever the rest
+  // of the pipeline did after an abort.
   const uint32_t full0 = bar0, empty0 = bar0 + 8u * S, sff0 = bar0 + 16u * S;
+  const uint32_t sfr0 = bar0 + 24u * S, pd0 = bar0 + 32u * S;
   // per accumulator slot: accf (accumulator full), acce (fully drained),
   // acco (its columns shared with the other region drained; kOvl only)
-  const uint32_t accf0 = bar0 + 24u * S, acce0 = accf0 + 8u * kRegions;
+  const uint32_t accf0 = bar0 + 40u * S, acce0 = accf0 + 8u * kRegions;
   const uint32_t acco0 = acce0 + 8u * kRegions;
   const uint32_t drain_bar = acco0 + 8u * kRegions;
+  const uint32_t pinfo_bar = drain_bar + 8u;  // the second CTA's drain record is in
   uint32_t* const misc =
-      reinterpret_cast<uint32_t*>(smem + p.smem_bar + 24u * S + 24u * kRegions + 8u);
+      reinterpret_cast<uint32_t*>(smem + p.smem_bar + 40u * S + 24u * kRegions + 16u);
   uint32_t* const tmem_holder = misc + 0;
   volatile uint32_t* const abort_flag = misc + 1;
   uint32_t* const cta_amax = misc + 2;
+  // the operand producer's record for the exit drain: per stage the bytes it
+  // expects (this CTA's share), and (in the leader) the second CTA's record:
+  // its armed-stage mask, their parities and per-stage bytes
+  uint32_t* const stage_bytes = misc + 4;         // [8]
+  uint32_t* const peer_rec = misc + 12;           // [2 + 8]
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      // the producer's expect_tx and the four scale warps (of both CTAs of a
-      // pair; only the leader's barrier is used then)
-      mbar_init(full0 + 8u * s, 1 + (PAIR ? 8 : 4));
+      mbar_init(full0 + 8u * s, 1);                // the leader's expect_tx
+      mbar_init(sfr0 + 8u * s, PAIR ? 8 : 4);      // the scale warps of both CTAs
+      mbar_init(pd0 + 8u * s, 1);
       // freed by the MMA commit (in a pair, the leader's commit arrives in
       // both CTAs)
       mbar_init(empty0 + 8u * s, 1);
@@ -637,6 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(acco0 + 8u * b, PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(drain_bar, 1);
+    mbar_init(pinfo_bar, 1);
     *abort_flag = 0u;
     *cta_amax = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -670,6 +733,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (CM > 1) cluster_sync();  // the peer's barriers initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  // this warp has arrived on the final cluster barrier (the epilogue arrives
+  // as soon as its last accumulator release is out, so that the barrier's
+  // release does not wait for its last stores)
+  bool cl_arrived = false;
 
   if (warp == 0 || warp == kSfProdWarp) {
     // ----------------------------------------------------- producers
@@ -712,6 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_4d(sfb_dst0 + stage * kSfbStage, &tmap_sfb, 0, ks * kCps, atom0, tc.l, bar);
           } else if (PAIR && crank != 0) {
             // the second CTA of a pair: its halves are counted in the leader
+            stage_bytes[stage] = kAStage + b_stage_bytes;
             const uint32_t lbar = mapa_shared(bar, 0);
 #pragma unroll
             for (int sl = 0; sl < KSL; ++sl) {
@@ -725,6 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {
             // a pair's leader expects the bytes of both CTAs
+            stage_bytes[stage] = kAStage + b_stage_bytes;
             mbar_arrive_expect_tx(bar, (PAIR ? 2u : 1u) * (kAStage + b_stage_bytes));
 #pragma unroll
             for (int sl = 0; sl < KSL; ++sl) {
@@ -738,19 +807,64 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
       }
-      // drain: every issued load must have landed before the CTA may exit.
-      // The scale copies complete on this CTA's own sff barrier.  The A/B
-      // barrier also counts the scale warps (and, in a pair, lives in the
-      // leader), so the operand producer instead waits until the MMAs have
-      // released each stage it loaded, which they do only after its bytes
-      // landed.
+      // drain: every issued load must have landed before the CTA may exit,
+      // observed on the barriers the copies complete on (the rest of the
+      // pipeline may have given up after an abort).
       const unsigned long long t_drain = globaltimer();
-      for (int s = 0; s < S; ++s)
-        if (armed & (1u << s)) {
-          const uint32_t parity = (armed_parity >> s) & 1u;
-          if (scales) drain_wait(sff0 + 8u * s, parity, p, 13u, t_drain);
-          else drain_wait(empty0 + 8u * s, parity, p, 10u, t_drain);
+      if (scales || !PAIR) {
+        // the scale copies on this CTA's sff; a lone CTA's operand copies on
+        // its full, which counts copies alone
+        for (int s = 0; s < S; ++s)
+          if (armed & (1u << s))
+            drain_wait((scales ? sff0 : full0) + 8u * s, (armed_parity >> s) & 1u, p,
+                       scales ? 13u : 10u, t_drain);
+      } else if (crank != 0) {
+        // second CTA of a pair: its copies complete on the leader's full.
+        // Hand the leader this CTA's record, then wait for its word, per
+        // stage, that the stage's bytes have landed.
+        const uint32_t lrec = mapa_shared(smem_u32(peer_rec), 0);
+        st_cluster_u32(lrec, armed);
+        st_cluster_u32(lrec + 4u, armed_parity);
+        for (int s = 0; s < S; ++s) st_cluster_u32(lrec + 8u + 4u * s, stage_bytes[s]);
+        mbar_arrive_cluster_release(mapa_shared(pinfo_bar, 0));
+        for (int s = 0; s < S; ++s)
+          if (armed & (1u << s)) drain_wait(pd0 + 8u * s, 0u, p, 17u, t_drain);
+      } else {
+        // the leader: its full counts both CTAs' copies.  With the second
+        // CTA's record (if it arrives), a stage only one of the two issued
+        // after an abort is completed by hand: the share that will never
+        // come off the count, or the expect_tx that was never made.
+        drain_wait(pinfo_bar, 0u, p, 18u, t_drain);
+        asm volatile("fence.acq_rel.cluster;" ::: "memory");
+        // without the record (its wait gave up), assume the second CTA
+        // issued what this one did
+        const bool rec = mbar_test_wait(pinfo_bar, 0u);
+        const uint32_t pm = rec ? peer_rec[0] : armed, pp = rec ? peer_rec[1] : armed_parity;
+        const uint32_t* const precs = rec ? peer_rec + 2 : stage_bytes;
+        for (int s = 0; s < S; ++s) {
+          const bool mine = (armed >> s) & 1u, theirs = (pm >> s) & 1u;
+          if (!mine && !theirs) continue;
+          const uint32_t bar = full0 + 8u * s;
+          const uint32_t mp = (armed_parity >> s) & 1u, tp = (pp >> s) & 1u;
+          // the phase both issued, or the newer of two (the older one is
+          // complete: a newer arming needs the older phase consumed)
+          uint32_t parity = mine ? mp : tp;
+          if (mine && theirs && mp != tp) {
+            if (mbar_test_wait(bar, mp)) {
+              parity = tp;  // ours is the older: the second CTA's phase lacks our expect_tx
+              mbar_arrive_expect_tx(bar, precs[s]);
+            } else {
+              mbar_complete_tx(bar, stage_bytes[s]);  // ours lacks the second CTA's bytes
+            }
+          } else if (mine && !theirs) {
+            mbar_complete_tx(bar, stage_bytes[s]);
+          } else if (!mine && theirs) {
+            mbar_arrive_expect_tx(bar, precs[s]);
+          }
+          drain_wait(bar, parity, p, 10u, t_drain);
+          if (theirs) mbar_arrive_cluster(mapa_shared(pd0 + 8u * s, 1));
         }
+      }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
@@ -807,8 +921,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // CTA's B rows into the first TILE_N / 2 accumulator columns
         const uint32_t id_u = kHalves && u >= p.full_units ? p.idesc_half : idesc;
         for (int ks = 0; ks < p.k_stages; ++ks) {
-          // operands in smem and this stage's scales in tensor memory
-          if (!BSG_WAIT(full0 + 8u * stage, phase, 3)) { ok = false; break; }
+          // this stage's scales in tensor memory and its operands in smem:
+          // both barriers tested at once on the fast path
+          if (!(mbar_test_wait2(sfr0 + 8u * stage, full0 + 8u * stage, phase) ||
+                (BSG_WAIT(sfr0 + 8u * stage, phase, 16) && BSG_WAIT(full0 + 8u * stage, phase, 3)))) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t sfb_t = sfa_t + 4 * kCps;
           const int nm = ks == last ? last_nmma : kMmasPerStage;
@@ -922,8 +1041,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         // one of the stage's arrivals (on the leader's barrier in a pair)
         if (lane == 0) {
-          if (PAIR) mbar_arrive_cluster(mapa_shared(full0 + 8u * stage, 0));
-          else mbar_arrive(full0 + 8u * stage);
+          if (PAIR) mbar_arrive_cluster(mapa_shared(sfr0 + 8u * stage, 0));
+          else mbar_arrive(sfr0 + 8u * stage);
         }
         if (++stage == S) { stage = 0; phase ^= 1u; }
       }
@@ -968,6 +1087,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t batch_off = static_cast<size_t>(tc.l) * p.M * p.N;
       const uint32_t release_bar = acce0 + 8u * slot;
       const uint32_t shared_bar = acco0 + 8u * slot;
+      const bool last_unit = u + unit_step >= p.num_units;
       if (++acc == kRegions) { acc = 0; acc_phase ^= 1u; }
       // this warp is done reading the accumulator (release) or the columns
       // its region shares with the other (release_shared, kOvl only)
@@ -979,7 +1099,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           else mbar_arrive(bar);
         }
       };
-      auto release = [&]() { arrive_on(release_bar); };
+      auto release = [&]() {
+        arrive_on(release_bar);
+        if (CM > 1 && last_unit) {  // no remote access follows in this warp
+          cluster_arrive();
+          cl_arrived = true;
+        }
+      };
       auto release_shared = [&]() { arrive_on(shared_bar); };
       // kOvl units (FP8 operands, so 16-bit or fp32 C): warp h drains the
       // unit's 16-column chunks h, h + 2, h + 4, ...; a whole unit in slot 0
@@ -987,6 +1113,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // chunks 11..15) first, so that the first round of loads frees them
       // (in slot 1 they are the first chunks already).  A half-width unit is
       // always a CTA's last: no unit waits on its shared columns.
+      //
+      // 16-bit n-major C leaves in whole 128-byte row pieces: the two warps
+      // of a lane quarter each hold two of a 64-column group's four chunks,
+      // put them in the quarter's 4 KB staging buffer and, after a barrier
+      // of the pair, each stores 16 of its 32 rows.  A store request then
+      // covers a whole 128-byte line, not one 32-byte sector of 16 lines,
+      // and those scattered sector writes measurably slowed the next unit's
+      // operand loads.
       auto drain_overlapped = [&](auto cw_tag, int n_end) {
         constexpr int CW = decltype(cw_tag)::value;
         constexpr int kNch = CW / 16;  // chunks of this warp: 8, or 4 in a half-width unit
@@ -1000,61 +1134,91 @@ __global__ void __launch_bounds__(kThreads, 1)
           // leaves tensor memory.  Only the first round's release (the shared
           // columns) is on the next unit's path; the full release is needed
           // one unit later, so the rounds need not all stay in registers.
+          // A round is two 64-column groups; slot 0 takes a whole unit's
+          // groups from the last (its shared chunks 11..15 lie in groups 2
+          // and 3), slot 1 and half-width units from the first.
+          auto group_of = [&](int k) { return (CW == kCols && slot == 0) ? 3 - k : k; };
+          // chunk held in round slot i of the round starting at slot c0
+          auto chunk_of = [&](int c0_, int i) { return 4 * group_of(c0_ / 2 + i / 2) + 2 * (i & 1) + h; };
           uint32_t rb[kRnd][16];
           const bool bf = p.c_dtype == BSG_BF16;
           uint16_t* const cbase = static_cast<uint16_t*>(p.c) + batch_off;
+          uint8_t* const qstg = smem + p.smem_epi + q * (2 * kEpiStageBytes);
 #pragma unroll
           for (int c0 = 0; c0 < kNch; c0 += kRnd) {
 #pragma unroll
-            for (int i = 0; i < kRnd; ++i) tc_ld_32x32b_x16(tbase + col_of(c0 + i), rb[i]);
+            for (int i = 0; i < kRnd; ++i) tc_ld_32x32b_x16(tbase + 16 * chunk_of(c0, i), rb[i]);
             tc_wait_ld();
             if (c0 == 0) release_shared();
             if (c0 + kRnd >= kNch) release();
 #pragma unroll
-            for (int i = 0; i < kRnd; ++i) {
-              const uint32_t* r = rb[i];
-              uint32_t w[8];
+            for (int k = 0; k < kRnd / 2; ++k) {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float f0 = __uint_as_float(r[2 * j]), f1 = __uint_as_float(r[2 * j + 1]);
-                if (bf) {
-                  const __nv_bfloat162 v = __floats2bfloat162_rn(f0, f1);
-                  w[j] = *reinterpret_cast<const uint32_t*>(&v);
-                } else {
-                  const __half2 v = __floats2half2_rn(f0, f1);
-                  w[j] = *reinterpret_cast<const uint32_t*>(&v);
-                }
-              }
-              const int col = ucol0 + col_of(c0 + i);
-              // only stored elements count toward Amax
-              const int nv = row_ok ? n_end - col : 0;
-              if (nv >= 16) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) vmax = __vmaxu2(vmax, w[j] & 0x7FFF7FFFu);
-              } else {
+              for (int e = 0; e < 2; ++e) {
+                const uint32_t* r = rb[2 * k + e];
+                uint32_t w[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                  uint32_t m = w[j] & 0x7FFF7FFFu;
-                  if (2 * j >= nv) m &= 0xFFFF0000u;
-                  if (2 * j + 1 >= nv) m &= 0x0000FFFFu;
-                  vmax = __vmaxu2(vmax, m);
+                  const float f0 = __uint_as_float(r[2 * j]), f1 = __uint_as_float(r[2 * j + 1]);
+                  if (bf) {
+                    const __nv_bfloat162 v = __floats2bfloat162_rn(f0, f1);
+                    w[j] = *reinterpret_cast<const uint32_t*>(&v);
+                  } else {
+                    const __half2 v = __floats2half2_rn(f0, f1);
+                    w[j] = *reinterpret_cast<const uint32_t*>(&v);
+                  }
+                }
+                const int col = ucol0 + 16 * chunk_of(c0, 2 * k + e);
+                // only stored elements count toward Amax
+                const int nv = row_ok ? n_end - col : 0;
+                if (nv >= 16) {
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) vmax = __vmaxu2(vmax, w[j] & 0x7FFF7FFFu);
+                } else {
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) {
+                    uint32_t m = w[j] & 0x7FFF7FFFu;
+                    if (2 * j >= nv) m &= 0xFFFF0000u;
+                    if (2 * j + 1 >= nv) m &= 0x0000FFFFu;
+                    vmax = __vmaxu2(vmax, m);
+                  }
+                }
+                if (p.c_major == 0) {
+                  // this row's 32 bytes of the chunk: 16-byte pieces
+                  // 2(2e + h) and 2(2e + h) + 1 of the 128-byte staged row,
+                  // XOR-swizzled by row % 8 (conflict-free both ways)
+                  const int pc0 = 2 * (2 * e + h);
+                  uint8_t* const srow = qstg + lane * 128;
+                  *reinterpret_cast<uint4*>(srow + ((pc0 ^ (lane & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+                  *reinterpret_cast<uint4*>(srow + (((pc0 + 1) ^ (lane & 7)) * 16)) =
+                      make_uint4(w[4], w[5], w[6], w[7]);
+                } else {
+                  // m-major: column by column, the 32 lanes write 32 consecutive rows
+                  uint16_t* dst = cbase + static_cast<size_t>(col) * p.M + row;
+                  const int ncols = row_ok ? min(16, n_end - col) : 0;
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) {
+                    if (j < ncols)
+                      *dst = static_cast<uint16_t>((j & 1) ? (w[j / 2] >> 16) : (w[j / 2] & 0xFFFFu));
+                    dst += p.M;
+                  }
                 }
               }
               if (p.c_major == 0) {
-                // 32 rows x 32 bytes through the staging buffer
-                char* const g = reinterpret_cast<char*>(cbase + static_cast<size_t>(row0) * p.N + col);
-                store_rows_coalesced<8>(stg, w, lane, g, static_cast<size_t>(p.N) * 2, p.M - row0,
-                                        (n_end - col) * 2);
-              } else {
-                // m-major: column by column, the 32 lanes write 32 consecutive rows
-                uint16_t* dst = cbase + static_cast<size_t>(col) * p.M + row;
-                const int ncols = row_ok ? min(16, n_end - col) : 0;
+                // the group's 32 rows x 128 bytes: this warp stores rows
+                // 16h .. 16h + 15, four rows (eight lanes each) per store
+                named_bar_sync(2 + q, 64);
+                const int gcol = ucol0 + 64 * group_of(c0 / 2 + k);
+                const int bytes_valid = (n_end - gcol) * 2;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  if (j < ncols)
-                    *dst = static_cast<uint16_t>((j & 1) ? (w[j / 2] >> 16) : (w[j / 2] & 0xFFFFu));
-                  dst += p.M;
+                for (int j = 0; j < 4; ++j) {
+                  const int rr = 16 * h + 4 * j + (lane >> 3), pc = lane & 7;
+                  const uint4 x = *reinterpret_cast<const uint4*>(qstg + rr * 128 + ((pc ^ (rr & 7)) * 16));
+                  if (row0 + rr < p.M && pc * 16 < bytes_valid)
+                    *reinterpret_cast<uint4*>(reinterpret_cast<char*>(
+                        cbase + static_cast<size_t>(row0 + rr) * p.N + gcol) + pc * 16) = x;
                 }
+                named_bar_sync(2 + q, 64);  // the buffer is free for the next group
               }
             }
           }
@@ -1366,8 +1530,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before();
+  if (CM > 1 && !cl_arrived) {
+    __syncwarp();
+    cluster_arrive();
+  }
   __syncthreads();
-  if (CM > 1) cluster_sync();  // the peer arrives into this CTA no more
+  if (CM > 1) cluster_wait();  // the peer arrives into this CTA no more
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
@@ -1722,9 +1890,10 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
   k.smem_sfb = k.smem_sfa + stages * sfa_stage;
   k.smem_epi = k.smem_sfb + stages * sfb_stage;
   k.smem_bar = k.smem_epi + kEpiWarps * kEpiStageBytes;
-  // barriers: 3 per stage, 3 per accumulator slot (at most 2), the drain
-  // barrier, then the flags; then the alignment slack
-  plan->smem_bytes = static_cast<int>(k.smem_bar) + 24 * stages + 48 + 8 + 16 + 1024;
+  // barriers: 5 per stage, 3 per accumulator slot (at most 2), the drain
+  // and peer-record barriers, then 22 words of flags and the producers'
+  // drain records; then the alignment slack
+  plan->smem_bytes = static_cast<int>(k.smem_bar) + 40 * stages + 48 + 16 + 88 + 1024;
   k.wait_limit_ns = 1000000000ull;  // one second per wait
   if (const char* e = std::getenv("BSG_WAIT_LIMIT_NS")) {
     const unsigned long long v = std::strtoull(e, nullptr, 10);

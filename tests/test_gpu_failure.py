@@ -2,8 +2,13 @@
 kernel is bounded.  With a wait limit far below a tile's running time the
 waits run out; the kernel records it in the workspace error word, abandons
 its pipeline, drains its own copies and MMAs, frees tensor memory and
-returns.  The host reads BSG_ERR_DEVICE_TIMEOUT, and the same context then
-runs a normal plan correctly."""
+returns.  The drains wait on the barriers the copies and MMAs complete on
+(in a CTA pair the leader settles the stages only one CTA issued), so an
+abandoned launch returns within microseconds of its first timeout, not after
+a drain's own limit.  The host reads BSG_ERR_DEVICE_TIMEOUT, and the same
+context then runs a normal plan correctly."""
+
+import time
 
 import pytest
 import torch
@@ -23,12 +28,15 @@ def _built():
     bsg.library()
 
 
-@pytest.mark.parametrize("tile_n", [0, 128])
-def test_wait_limit_reports_timeout_then_context_recovers(tile_n, monkeypatch):
+@pytest.mark.parametrize("tile_n,cluster_m", [(0, 0), (128, 1), (256, 2)],
+                         ids=["default", "single-cta", "cta-pair"])
+def test_wait_limit_reports_timeout_then_context_recovers(tile_n, cluster_m, monkeypatch):
     inp = synth.workload(2, M=1024, N=1024, K=4096)
     p = inp.problem
     monkeypatch.setenv("BSG_WAIT_LIMIT_NS", "2000")  # 2 us: shorter than one tile
-    op = bsg.GemmAmax(problem_of(p, tile_n=tile_n))  # the plan reads the limit
+    op = bsg.GemmAmax(problem_of(p, tile_n=tile_n, cluster_m=cluster_m))  # the plan reads the limit
+    if cluster_m == 2:
+        assert op.describe()["cluster_m"] == 2
     monkeypatch.delenv("BSG_WAIT_LIMIT_NS")
     A, B, SFA, SFB = to_device(inp)
     C = torch.zeros(synth.c_shape(p), dtype=torch.bfloat16, device="cuda:0")
@@ -37,7 +45,14 @@ def test_wait_limit_reports_timeout_then_context_recovers(tile_n, monkeypatch):
     torch.cuda.synchronize()  # the kernel returned (no hang, no fault)
     assert op.device_status() == bsg.BSG_ERR_DEVICE_TIMEOUT
     assert op.device_status() == bsg.BSG_OK  # reading clears the error word
+    # again, timed: no drain sat out its 200 ms floor
+    t0 = time.perf_counter()
+    op.run(A, B, SFA, SFB, C, amax)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert op.device_status() == bsg.BSG_ERR_DEVICE_TIMEOUT
+    assert elapsed < 0.1, f"abandoned launch took {elapsed * 1e3:.1f} ms"
     op.close()
     # a normal plan on the same context
-    c, a, *_ = run_gpu(inp, tile_n=tile_n)
+    c, a, *_ = run_gpu(inp, tile_n=tile_n, cluster_m=cluster_m)
     assert_parity(inp, c, a)
