@@ -64,11 +64,13 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # comments and whitespace removed, so only a code change invalidates an
 # entry) and workload.
 TRAFFIC = {
-    ("56ab9e2f61816786", 2): 36834816,
-    ("56ab9e2f61816786", 3): 415449856,
-    ("56ab9e2f61816786", 4): 202578688,
-    ("56ab9e2f61816786", 6): 202518016,
-    ("56ab9e2f61816786", 7): 36510464,
+    ("9fa2f36973400a8c", 1): 183296,
+    ("9fa2f36973400a8c", 2): 36463872,
+    ("9fa2f36973400a8c", 3): 415549440,
+    ("9fa2f36973400a8c", 4): 201539584,
+    ("9fa2f36973400a8c", 5): 174163968,
+    ("9fa2f36973400a8c", 6): 201764608,
+    ("9fa2f36973400a8c", 7): 36468224,
 }
 
 
@@ -77,8 +79,8 @@ TRAFFIC = {
 # it ends (up to the 129 MB L2), so its write bytes read below the codes and
 # scales it writes.
 TRAFFIC_Q = {
-    ("b603e92150e0b482", 1): 624015104,
-    ("b603e92150e0b482", 2): 289099776,
+    ("c02687a909cfda97", 3): 625256704,
+    ("c02687a909cfda97", 4): 375985408,
 }
 
 QMETRIC = "MX quantize GB/s on 1 GB300 (X read + codes and scales written); % of HBM copy bandwidth"

@@ -301,16 +301,129 @@ struct ColTile {
   static constexpr int kUnitCols = 8 * kColsPerWarp;    // 8 warps
 };
 
+// Loads in flight (bf16 input): each thread copies its eight 16-byte row
+// pieces of a block into its own slots of a shared ring (cp.async, zero-filled
+// past `cols`) and keeps kColStages - 1 blocks in flight ahead of the one it
+// converts, so the bytes in flight no longer depend on registers: the bf16
+// conversion needs ~112 registers, two CTAs per SM, and loading through
+// registers left half the fp32 kernel's bytes in flight (67 % of the copy
+// bandwidth, against 77 % this way).  A thread reads back only what it copied
+// itself, so no barrier is needed.  fp32 input (64 registers, four CTAs per
+// SM) already keeps enough in flight through registers and loads directly.
+constexpr int kColStages = 3;
+constexpr int kColStageBytes = 8 * kThreads * 16;  // one block: 8 row pieces per thread
+constexpr int kColSmemBytes = kColStages * kColStageBytes;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// One block of 32 rows of this thread's columns (its eight row pieces in
+// raw, zero past `cols`): the column maxima over the block, the scale bytes
+// (into byte b of sfw), the codes.
 template <int IN_BF16, int OUT>
-__global__ void __launch_bounds__(kThreads) bsq_quantize_colwise_kernel(const QCParams p) {
-  using T = ColTile<IN_BF16>;
-  constexpr int E = T::kE;
-  constexpr int kInBytes = IN_BF16 ? 2 : 4;
+__device__ __forceinline__ void colwise_block(const QCParams& p, const uint4 (&raw)[8], uint32_t l,
+                                              uint32_t row0, uint32_t b, uint32_t c0, bool col_ok,
+                                              uint32_t (&sfw)[ColTile<IN_BF16>::kE]) {
+  constexpr int E = ColTile<IN_BF16>::kE;
   using F = OutFmt<OUT>;
+  // per column: max of the magnitude bits over this lane's 8 rows, then
+  // over the 4 row groups (NaN and infinity order above every finite value)
+  uint32_t amax[E];
+#pragma unroll
+  for (int j = 0; j < E; ++j) amax[j] = 0u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      const uint32_t bits = IN_BF16 ? ((j & 1) ? (w[j / 2] & 0xFFFF0000u) : (w[j / 2] << 16))
+                                    : w[j];
+      amax[j] = max(amax[j], bits & 0x7FFFFFFFu);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    amax[j] = max(amax[j], __shfl_xor_sync(0xFFFFFFFFu, amax[j], 8));
+    amax[j] = max(amax[j], __shfl_xor_sync(0xFFFFFFFFu, amax[j], 16));
+  }
+  if (!col_ok) return;  // a chunk past `cols`: it only took part in the shuffles
+  float inv[E];
+  bool nonfinite[E];
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    uint32_t byte = 127u;
+    inv[j] = 1.0f;
+    nonfinite[j] = amax[j] >= 0x7F800000u;
+    if (nonfinite[j]) {
+      byte = 0xFFu;
+    } else if (amax[j] != 0u) {
+      int e = floor_log2_bits(amax[j]) - F::kEmax;
+      e = min(max(e, -127), 127);
+      byte = static_cast<uint32_t>(e + 127);
+      inv[j] = -e >= -126 ? __uint_as_float(static_cast<uint32_t>(127 - e) << 23)
+                          : __uint_as_float(0x00400000u);
+    }
+    sfw[j] = (sfw[j] & ~(0xFFu << (8 * b))) | (byte << (8 * b));
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+    float v[E];
+#pragma unroll
+    for (int j = 0; j < E; ++j)
+      v[j] = __uint_as_float(IN_BF16 ? ((j & 1) ? (w[j / 2] & 0xFFFF0000u) : (w[j / 2] << 16))
+                                     : w[j]);
+    uint32_t out[E / 4];
+#pragma unroll
+    for (int k = 0; k < E / 4; ++k) out[k] = 0u;
+#pragma unroll
+    for (int j = 0; j < E; j += 2) {
+      // exact products (powers of two), then two codes per conversion
+      uint32_t c2 = cvt2<OUT>(v[j] * inv[j], v[j + 1] * inv[j + 1]);
+      if (nonfinite[j]) c2 = (c2 & 0xFF00u) | F::kNan;
+      if (nonfinite[j + 1]) c2 = (c2 & 0x00FFu) | (F::kNan << 8);
+      out[j / 4] |= c2 << (16 * ((j / 2) % 2));
+    }
+    uint8_t* dst = p.codes + (static_cast<size_t>(l) * p.rows + row0 + 4 * i) * p.cols + c0;
+    if (E == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(out[0], out[E / 4 - 1]);
+    else *reinterpret_cast<uint32_t*>(dst) = out[0];
+  }
+}
+
+// A unit's scale words: lanes of row group 0, one word per column of a real
+// atom (columns past `cols` in the last atom: padding 127).
+template <int IN_BF16>
+__device__ __forceinline__ void colwise_scale_words(const QCParams& p, uint32_t l, uint32_t kt,
+                                                    uint32_t c0, int rg,
+                                                    const uint32_t (&sfw)[ColTile<IN_BF16>::kE]) {
+  if (rg != 0) return;
+#pragma unroll
+  for (int j = 0; j < ColTile<IN_BF16>::kE; ++j) {
+    const uint32_t c = c0 + j;
+    const uint32_t atom = c >> 7;
+    if (atom < p.t_c) {
+      const uint32_t off = (((l * p.t_c + atom) * p.t_k + kt) << 9) + (c & 31) * 16 + ((c & 127) >> 5) * 4;
+      *reinterpret_cast<uint32_t*>(p.sf + off) = sfw[j];
+    }
+  }
+}
+
+// fp32 input: loads through registers, eight 16-byte row pieces per block in
+// flight per thread, four CTAs per SM.
+template <int OUT>
+__device__ __forceinline__ void colwise_direct(const QCParams& p) {
+  using T = ColTile<0>;
+  constexpr int E = T::kE;
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const int chunk = lane & 7, rg = lane >> 3;  // column chunk of the warp, row group
-
   for (uint32_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
     const uint32_t lk = fdiv(u, p.cu_div);  // l * t_k + kt
     const uint32_t cu = u - lk * p.cu_div.d;
@@ -319,7 +432,7 @@ __global__ void __launch_bounds__(kThreads) bsq_quantize_colwise_kernel(const QC
     const uint32_t c0 = cu * T::kUnitCols + warp * T::kColsPerWarp + chunk * E;
     const bool col_ok = c0 < p.cols;  // cols % 16 == 0: a chunk is wholly in or out
     const uint32_t nb = min(4u, p.nblk - kt * 4);
-    uint32_t sfw[E];  // per column: the scale bytes of K-blocks 0..3 of this atom
+    uint32_t sfw[E];
 #pragma unroll
     for (int j = 0; j < E; ++j) sfw[j] = 0x7F7F7F7Fu;
     for (uint32_t b = 0; b < nb; ++b) {
@@ -328,87 +441,102 @@ __global__ void __launch_bounds__(kThreads) bsq_quantize_colwise_kernel(const QC
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const size_t e = (static_cast<size_t>(l) * p.rows + row0 + 4 * i) * p.cols + c0;
-        raw[i] = col_ok ? __ldcs(reinterpret_cast<const uint4*>(p.x + e * kInBytes))
+        raw[i] = col_ok ? __ldcs(reinterpret_cast<const uint4*>(p.x + e * 4))
                         : make_uint4(0u, 0u, 0u, 0u);
       }
-      // per column: max of the magnitude bits over this lane's 8 rows, then
-      // over the 4 row groups (NaN and infinity order above every finite value)
-      uint32_t amax[E];
-#pragma unroll
-      for (int j = 0; j < E; ++j) amax[j] = 0u;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-#pragma unroll
-        for (int j = 0; j < E; ++j) {
-          const uint32_t bits = IN_BF16 ? ((j & 1) ? (w[j / 2] & 0xFFFF0000u) : (w[j / 2] << 16))
-                                        : w[j];
-          amax[j] = max(amax[j], bits & 0x7FFFFFFFu);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < E; ++j) {
-        amax[j] = max(amax[j], __shfl_xor_sync(0xFFFFFFFFu, amax[j], 8));
-        amax[j] = max(amax[j], __shfl_xor_sync(0xFFFFFFFFu, amax[j], 16));
-      }
-      if (!col_ok) continue;
-      float inv[E];
-      bool nonfinite[E];
-#pragma unroll
-      for (int j = 0; j < E; ++j) {
-        uint32_t byte = 127u;
-        inv[j] = 1.0f;
-        nonfinite[j] = amax[j] >= 0x7F800000u;
-        if (nonfinite[j]) {
-          byte = 0xFFu;
-        } else if (amax[j] != 0u) {
-          int e = floor_log2_bits(amax[j]) - F::kEmax;
-          e = min(max(e, -127), 127);
-          byte = static_cast<uint32_t>(e + 127);
-          inv[j] = -e >= -126 ? __uint_as_float(static_cast<uint32_t>(127 - e) << 23)
-                              : __uint_as_float(0x00400000u);
-        }
-        sfw[j] = (sfw[j] & ~(0xFFu << (8 * b))) | (byte << (8 * b));
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-        float v[E];
-#pragma unroll
-        for (int j = 0; j < E; ++j)
-          v[j] = __uint_as_float(IN_BF16 ? ((j & 1) ? (w[j / 2] & 0xFFFF0000u) : (w[j / 2] << 16))
-                                         : w[j]);
-        uint32_t out[E / 4];
-#pragma unroll
-        for (int k = 0; k < E / 4; ++k) out[k] = 0u;
-#pragma unroll
-        for (int j = 0; j < E; j += 2) {
-          // exact products (powers of two), then two codes per conversion
-          uint32_t c2 = cvt2<OUT>(v[j] * inv[j], v[j + 1] * inv[j + 1]);
-          if (nonfinite[j]) c2 = (c2 & 0xFF00u) | F::kNan;
-          if (nonfinite[j + 1]) c2 = (c2 & 0x00FFu) | (F::kNan << 8);
-          out[j / 4] |= c2 << (16 * ((j / 2) % 2));
-        }
-        uint8_t* dst = p.codes + (static_cast<size_t>(l) * p.rows + row0 + 4 * i) * p.cols + c0;
-        if (E == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(out[0], out[E / 4 - 1]);
-        else *reinterpret_cast<uint32_t*>(dst) = out[0];
-      }
+      colwise_block<0, OUT>(p, raw, l, row0, b, c0, col_ok, sfw);
     }
-    // the unit's scale words: lanes of row group 0, one word per column of a
-    // real atom (columns past `cols` in the last atom: padding 127)
-    if (rg == 0) {
-#pragma unroll
-      for (int j = 0; j < E; ++j) {
-        const uint32_t c = c0 + j;
-        const uint32_t atom = c >> 7;
-        if (atom < p.t_c) {
-          const uint32_t off = (((l * p.t_c + atom) * p.t_k + kt) << 9) + (c & 31) * 16 +
-                               ((c & 127) >> 5) * 4;
-          *reinterpret_cast<uint32_t*>(p.sf + off) = sfw[j];
-        }
-      }
-    }
+    colwise_scale_words<0>(p, l, kt, c0, rg, sfw);
   }
+}
+
+// bf16 input: the load ring (above).
+template <int OUT>
+__device__ __forceinline__ void colwise_ring(const QCParams& p) {
+  using T = ColTile<1>;
+  constexpr int E = T::kE;
+  extern __shared__ __align__(16) uint8_t qc_ring[];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int chunk = lane & 7, rg = lane >> 3;  // column chunk of the warp, row group
+  // this thread's piece i of ring slot s (consecutive threads, consecutive 16 bytes)
+  const uint32_t ring0 = static_cast<uint32_t>(__cvta_generic_to_shared(qc_ring)) + tid * 16u;
+  auto slot_addr = [&](int s, int i) { return ring0 + static_cast<uint32_t>((s * 8 + i) * kThreads * 16); };
+  // a position in this CTA's walk over (unit, block of 32 rows)
+  struct Cursor {
+    uint32_t u, b, nb, l, kt, c0;
+    bool col_ok, valid;
+  };
+  auto set_unit = [&](Cursor& c, uint32_t u) {
+    c.u = u;
+    c.b = 0;
+    c.valid = u < p.num_units;
+    if (!c.valid) return;
+    const uint32_t lk = fdiv(u, p.cu_div);  // l * t_k + kt
+    const uint32_t cu = u - lk * p.cu_div.d;
+    c.l = fdiv(lk, p.tk_div);
+    c.kt = lk - c.l * p.t_k;
+    c.c0 = cu * T::kUnitCols + warp * T::kColsPerWarp + chunk * E;
+    c.col_ok = c.c0 < p.cols;  // cols % 16 == 0: a chunk is wholly in or out
+    c.nb = min(4u, p.nblk - c.kt * 4);
+  };
+  auto advance = [&](Cursor& c) {
+    if (++c.b == c.nb) set_unit(c, c.u + gridDim.x);
+  };
+  // the copies of the cursor's block into ring slot s (one commit group)
+  auto issue = [&](const Cursor& c, int s) {
+    if (c.valid) {
+      const uint32_t row0 = c.kt * 128 + c.b * 32 + rg;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const size_t e = (static_cast<size_t>(c.l) * p.rows + row0 + 4 * i) * p.cols + c.c0;
+        cp_async16(slot_addr(s, i), c.col_ok ? static_cast<const void*>(p.x + e * 2) : p.x,
+                   c.col_ok ? 16u : 0u);
+      }
+    }
+    cp_async_commit();
+  };
+  Cursor ld, cur;
+  set_unit(ld, blockIdx.x);
+  cur = ld;
+#pragma unroll
+  for (int s = 0; s < kColStages - 1; ++s) {
+    issue(ld, s);
+    if (ld.valid) advance(ld);
+  }
+  int slot = 0;
+  uint32_t sfw[E];  // per column: the scale bytes of K-blocks 0..3 of this atom
+#pragma unroll
+  for (int j = 0; j < E; ++j) sfw[j] = 0x7F7F7F7Fu;
+  while (cur.valid) {
+    issue(ld, slot == 0 ? kColStages - 1 : slot - 1);
+    if (ld.valid) advance(ld);
+    cp_async_wait<kColStages - 1>();  // this block's copies have landed
+    uint4 raw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint4 v;
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                   : "r"(slot_addr(slot, i)));
+      raw[i] = v;
+    }
+    colwise_block<1, OUT>(p, raw, cur.l, cur.kt * 128 + cur.b * 32 + rg, cur.b, cur.c0, cur.col_ok, sfw);
+    if (cur.b + 1 == cur.nb) {  // the unit's last block
+      colwise_scale_words<1>(p, cur.l, cur.kt, cur.c0, rg, sfw);
+#pragma unroll
+      for (int j = 0; j < E; ++j) sfw[j] = 0x7F7F7F7Fu;
+    }
+    advance(cur);
+    slot = slot == kColStages - 1 ? 0 : slot + 1;
+  }
+  cp_async_wait<0>();  // no copy of this thread outlives it
+}
+
+template <int IN_BF16, int OUT>
+__global__ void __launch_bounds__(kThreads) bsq_quantize_colwise_kernel(const QCParams p) {
+  if constexpr (IN_BF16) colwise_ring<OUT>(p);
+  else colwise_direct<OUT>(p);
 }
 
 template <int IN_BF16, int OUT, int SFV>
@@ -472,13 +600,16 @@ bsg_status launch_colwise(const bsg_quant_problem* q, const void* X, void* codes
   p.cu_div = make_fastdiv(static_cast<uint32_t>(col_units));
   p.tk_div = make_fastdiv(p.t_k);
   const void* fn = pick_colwise_kernel(in_bf16, out);
+  const int ring_bytes = in_bf16 ? kColSmemBytes : 0;  // the bf16 kernel's load ring
   int occ;
   {
     std::lock_guard<std::mutex> lock(g_dev_mu);
     int& slot = g_dev_occ[dev][8 + in_bf16 * 2 + out];
     if (slot == 0) {
       int n = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, 0) != cudaSuccess) {
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ring_bytes) !=
+              cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, ring_bytes) != cudaSuccess) {
         cudaGetLastError();
         return BSG_ERR_CUDA;
       }
@@ -489,7 +620,7 @@ bsg_status launch_colwise(const bsg_quant_problem* q, const void* X, void* codes
   int64_t grid = static_cast<int64_t>(sms) * occ;
   if (grid > p.num_units) grid = p.num_units;
   void* args[1] = {&p};
-  if (cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(kThreads), args, 0,
+  if (cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(kThreads), args, ring_bytes,
                        static_cast<cudaStream_t>(stream)) != cudaSuccess) {
     cudaGetLastError();
     return BSG_ERR_CUDA;
