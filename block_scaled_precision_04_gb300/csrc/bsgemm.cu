@@ -2223,10 +2223,14 @@ bsg_status bsg_check_device_status(const bsg_plan* plan, void* ws, void* stream)
   if (!plan || !ws) return BSG_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint32_t words[2] = {0, 0};
+  // read and clear the error words on the caller's stream, so that the
+  // clear is ordered before the next launch there (a non-blocking stream
+  // does not wait for the legacy default stream)
   if (cudaStreamSynchronize(s) != cudaSuccess ||
-      cudaMemcpy(words, static_cast<uint8_t*>(ws) + 8, sizeof(words), cudaMemcpyDeviceToHost) !=
-          cudaSuccess ||
-      cudaMemset(static_cast<uint8_t*>(ws) + 8, 0, sizeof(words)) != cudaSuccess) {
+      cudaMemcpyAsync(words, static_cast<uint8_t*>(ws) + 8, sizeof(words), cudaMemcpyDeviceToHost,
+                      s) != cudaSuccess ||
+      cudaMemsetAsync(static_cast<uint8_t*>(ws) + 8, 0, sizeof(words), s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
     cudaGetLastError();
     return BSG_ERR_CUDA;
   }

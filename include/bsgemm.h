@@ -206,7 +206,9 @@ bsg_status bsg_run_host(const bsg_plan *plan, const void *hA, const void *hB, co
                         const bsg_device_buffers *dev, void *stream);
 
 /* Synchronise `stream`, then read and clear the workspace's device error
- * word.  Returns BSG_ERR_DEVICE_TIMEOUT if a kernel of an earlier run gave
+ * word (the read and the clear are enqueued on `stream` and waited for, so
+ * the clear is ordered before later launches on it).  Returns
+ * BSG_ERR_DEVICE_TIMEOUT if a kernel of an earlier run gave
  * up on a pipeline wait (its outputs are then invalid), else BSG_OK.  The
  * pages have no counterpart: the bounded waits and their error word are
  * this library's own. */
