@@ -64,13 +64,13 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # comments and whitespace removed, so only a code change invalidates an
 # entry) and workload.
 TRAFFIC = {
-    ("9fa2f36973400a8c", 1): 183296,
-    ("9fa2f36973400a8c", 2): 36463872,
-    ("9fa2f36973400a8c", 3): 415549440,
-    ("9fa2f36973400a8c", 4): 201539584,
-    ("9fa2f36973400a8c", 5): 174163968,
-    ("9fa2f36973400a8c", 6): 201764608,
-    ("9fa2f36973400a8c", 7): 36468224,
+    ("65b63ef5b8c953ff", 1): 183296,
+    ("65b63ef5b8c953ff", 2): 36040960,
+    ("65b63ef5b8c953ff", 3): 415172608,
+    ("65b63ef5b8c953ff", 4): 202050816,
+    ("65b63ef5b8c953ff", 5): 173824512,
+    ("65b63ef5b8c953ff", 6): 201180928,
+    ("65b63ef5b8c953ff", 7): 36361472,
 }
 
 
