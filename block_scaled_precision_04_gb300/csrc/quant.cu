@@ -334,24 +334,39 @@ __device__ __forceinline__ void colwise_block(const QCParams& p, const uint4 (&r
   constexpr int E = ColTile<IN_BF16>::kE;
   using F = OutFmt<OUT>;
   // per column: max of the magnitude bits over this lane's 8 rows, then
-  // over the 4 row groups (NaN and infinity order above every finite value)
+  // over the 4 row groups (NaN and infinity order above every finite value).
+  // bf16: a SIMD max of the packed 16-bit magnitudes (they order like the
+  // fp32 bits they widen to), two columns per word.
   uint32_t amax[E];
+  if constexpr (IN_BF16) {
+    uint32_t m2[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-  for (int j = 0; j < E; ++j) amax[j] = 0u;
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+      for (int k = 0; k < 4; ++k) m2[k] = __vmaxu2(m2[k], w[k] & 0x7FFF7FFFu);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      m2[k] = __vmaxu2(m2[k], __shfl_xor_sync(0xFFFFFFFFu, m2[k], 8));
+      m2[k] = __vmaxu2(m2[k], __shfl_xor_sync(0xFFFFFFFFu, m2[k], 16));
+    }
+#pragma unroll
+    for (int j = 0; j < E; ++j) amax[j] = (j & 1) ? (m2[j / 2] & 0xFFFF0000u) : (m2[j / 2] << 16);
+  } else {
+#pragma unroll
+    for (int j = 0; j < E; ++j) amax[j] = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+      for (int j = 0; j < E; ++j) amax[j] = max(amax[j], w[j] & 0x7FFFFFFFu);
+    }
 #pragma unroll
     for (int j = 0; j < E; ++j) {
-      const uint32_t bits = IN_BF16 ? ((j & 1) ? (w[j / 2] & 0xFFFF0000u) : (w[j / 2] << 16))
-                                    : w[j];
-      amax[j] = max(amax[j], bits & 0x7FFFFFFFu);
+      amax[j] = max(amax[j], __shfl_xor_sync(0xFFFFFFFFu, amax[j], 8));
+      amax[j] = max(amax[j], __shfl_xor_sync(0xFFFFFFFFu, amax[j], 16));
     }
-  }
-#pragma unroll
-  for (int j = 0; j < E; ++j) {
-    amax[j] = max(amax[j], __shfl_xor_sync(0xFFFFFFFFu, amax[j], 8));
-    amax[j] = max(amax[j], __shfl_xor_sync(0xFFFFFFFFu, amax[j], 16));
   }
   if (!col_ok) return;  // a chunk past `cols`: it only took part in the shuffles
   float inv[E];
@@ -385,8 +400,13 @@ __device__ __forceinline__ void colwise_block(const QCParams& p, const uint4 (&r
     for (int k = 0; k < E / 4; ++k) out[k] = 0u;
 #pragma unroll
     for (int j = 0; j < E; j += 2) {
-      // exact products (powers of two), then two codes per conversion
-      uint32_t c2 = cvt2<OUT>(v[j] * inv[j], v[j + 1] * inv[j + 1]);
+      // exact products (powers of two, a pair per multiply), then two codes
+      // per conversion
+      const uint64_t pr = (static_cast<uint64_t>(__float_as_uint(v[j + 1])) << 32) | __float_as_uint(v[j]);
+      const uint64_t iv = (static_cast<uint64_t>(__float_as_uint(inv[j + 1])) << 32) | __float_as_uint(inv[j]);
+      const uint64_t sc = mul2(pr, iv);
+      uint32_t c2 = cvt2<OUT>(__uint_as_float(static_cast<uint32_t>(sc)),
+                              __uint_as_float(static_cast<uint32_t>(sc >> 32)));
       if (nonfinite[j]) c2 = (c2 & 0xFF00u) | F::kNan;
       if (nonfinite[j + 1]) c2 = (c2 & 0x00FFu) | (F::kNan << 8);
       out[j / 4] |= c2 << (16 * ((j / 2) % 2));
