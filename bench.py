@@ -79,10 +79,10 @@ TRAFFIC = {
 # it ends (up to the 129 MB L2), so its write bytes read below the codes and
 # scales it writes.
 TRAFFIC_Q = {
-    ("c02687a909cfda97", 1): 624306944,
-    ("c02687a909cfda97", 2): 288890112,
-    ("c02687a909cfda97", 3): 625256704,
-    ("c02687a909cfda97", 4): 375985408,
+    ("0f77d477e8d11bf4", 1): 624514304,
+    ("0f77d477e8d11bf4", 2): 289173504,
+    ("0f77d477e8d11bf4", 3): 625460224,
+    ("0f77d477e8d11bf4", 4): 374182144,
 }
 
 QMETRIC = "MX quantize GB/s on 1 GB300 (X read + codes and scales written); % of HBM copy bandwidth"
