@@ -185,10 +185,6 @@ __device__ __forceinline__ void cluster_arrive() {
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void cluster_sync() {
-  cluster_arrive();
-  cluster_wait();
-}
 
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -705,6 +701,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
+  // The setup's cluster barrier, split: every warp arrives here (thread 0
+  // after its barrier inits, which the arrival releases) and waits after the
+  // CTA barrier, so that the barrier's latency overlaps the tensor-memory
+  // allocation.  The peer's allocation is still ordered before the leader's
+  // first MMA: that waits for the peer's scale warps, which start after it.
+  if (CM > 1) {
+    __syncwarp();
+    cluster_arrive();
+  }
   if (warp == 0 && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
@@ -730,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (CM > 1) cluster_sync();  // the peer's barriers initialised before any remote arrival
+  if (CM > 1) cluster_wait();  // the peer's barriers initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   // this warp has arrived on the final cluster barrier (the epilogue arrives
