@@ -64,13 +64,13 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # comments and whitespace removed, so only a code change invalidates an
 # entry) and workload.
 TRAFFIC = {
-    ("65b63ef5b8c953ff", 1): 183296,
-    ("65b63ef5b8c953ff", 2): 36040960,
-    ("65b63ef5b8c953ff", 3): 415172608,
-    ("65b63ef5b8c953ff", 4): 202050816,
-    ("65b63ef5b8c953ff", 5): 173824512,
-    ("65b63ef5b8c953ff", 6): 201180928,
-    ("65b63ef5b8c953ff", 7): 36361472,
+    ("b1bacf256884d171", 1): 183552,
+    ("b1bacf256884d171", 2): 35725312,
+    ("b1bacf256884d171", 3): 415837184,
+    ("b1bacf256884d171", 4): 201287680,
+    ("b1bacf256884d171", 5): 173830912,
+    ("b1bacf256884d171", 6): 201147392,
+    ("b1bacf256884d171", 7): 35693056,
 }
 
 

@@ -1107,6 +1107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto release = [&]() {
         arrive_on(release_bar);
         if (CM > 1 && last_unit) {  // no remote access follows in this warp
+          __syncwarp();             // (lane 0 alone made the arrival)
           cluster_arrive();
           cl_arrived = true;
         }
