@@ -64,13 +64,13 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # comments and whitespace removed, so only a code change invalidates an
 # entry) and workload.
 TRAFFIC = {
-    ("b1bacf256884d171", 1): 183552,
-    ("b1bacf256884d171", 2): 35725312,
-    ("b1bacf256884d171", 3): 415837184,
-    ("b1bacf256884d171", 4): 201287680,
-    ("b1bacf256884d171", 5): 173830912,
-    ("b1bacf256884d171", 6): 201147392,
-    ("b1bacf256884d171", 7): 35693056,
+    ("0b4cb9aa8ffee0ab", 1): 184320,
+    ("0b4cb9aa8ffee0ab", 2): 40956672,
+    ("0b4cb9aa8ffee0ab", 3): 416777984,
+    ("0b4cb9aa8ffee0ab", 4): 201289472,
+    ("0b4cb9aa8ffee0ab", 5): 190086400,
+    ("0b4cb9aa8ffee0ab", 6): 201464832,
+    ("0b4cb9aa8ffee0ab", 7): 41391104,
 }
 
 

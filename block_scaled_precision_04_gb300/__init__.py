@@ -64,7 +64,8 @@ class bsg_plan_info(ctypes.Structure):
                 ("grid", ctypes.c_int32), ("threads", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("num_tiles", ctypes.c_int32),
                 ("mma_kind", ctypes.c_int32), ("cluster_m", ctypes.c_int32),
-                ("kernel_name", ctypes.c_char * 64), ("half_tiles", ctypes.c_int32)]
+                ("kernel_name", ctypes.c_char * 64), ("half_tiles", ctypes.c_int32),
+                ("k_split_tiles", ctypes.c_int32)]
 
 
 BSG_QUANT_ROWWISE = 0

@@ -97,6 +97,12 @@ struct Params {
   float* amax;
   uint32_t* ws;
   unsigned long long wait_limit_ns;
+  // tiles left over after the whole waves, each run as two K halves (0: none)
+  int ks_tiles;
+  int ks_k0;              // first K stage of the second half
+  int ks_first;           // index of the first split tile (they follow the whole ones)
+  float* part;            // per split tile, K half and CTA rank: 128 x 256 fp32 partial sums
+  uint32_t* ks_cnt;       // per split tile and CTA rank: halves claimed, partial sum out
 };
 
 // ------------------------------------------------------------------ PTX
@@ -366,7 +372,10 @@ struct KindTraits<kKindF4x2X> {  // FP4, block 32: two scale bytes per K=64 MMA
 
 struct Tile {
   int l, mt, nt;
-  int half;  // -1: the whole tile; 0 / 1: its left / right half (N = TILE_N / 2)
+  int half;    // -1: the whole tile; 0 / 1: its left / right half (N = TILE_N / 2)
+  int ks;      // -1: all of K; else the split tile whose K half kh this unit is
+  int kh;
+  int kb, ke;  // the unit's K stages [kb, ke)
 };
 
 // Unit u (one per cluster) -> (l, group of cluster_m M tiles, N tile); the
@@ -375,10 +384,38 @@ struct Tile {
 // Units from full_units on split the last tiles in two halves: the schedule's
 // final wave is then half-width tiles, so a partly filled last wave costs half
 // a tile time instead of a whole one.
+//
+// K halves instead (ks_tiles = R > 0, G clusters, at least two whole waves):
+// the R tiles past the whole waves each run as two units over the first and
+// the second half of the K stages, at full width.  The first halves are
+// units 0 .. R-1 and the second halves R .. 2R-1: the first units of
+// clusters 0 .. 2R-1, whose epilogues exchange the partial sums while whole
+// tiles' MMAs run (a half placed after a whole tile left its epilogue too
+// little time for that tile's stores, and a half in the last wave put the
+// exchange at the end of the launch; both measured slower).  Every cluster
+// then carries at most half a tile more than the whole waves, where a
+// half-width tail tile (the other split) takes about as long as a whole one:
+// its pipeline is bound by the ring's round trip, not the tensor rate.  The
+// whole tiles fill the other units in order.
 __device__ __forceinline__ Tile tile_coords(const Params& p, int u, int cm, int rank) {
   Tile r;
   r.half = -1;
-  if (u >= p.full_units) {
+  r.ks = -1;
+  r.kh = 0;
+  r.kb = 0;
+  r.ke = p.k_stages;
+  if (p.ks_tiles > 0) {
+    const int R = p.ks_tiles;
+    if (u < 2 * R) {
+      r.ks = u < R ? u : u - R;
+      r.kh = u < R ? 0 : 1;
+      u = p.ks_first + r.ks;
+      if (r.kh) r.kb = p.ks_k0;
+      else r.ke = p.ks_k0;
+    } else {
+      u -= 2 * R;
+    }
+  } else if (u >= p.full_units) {
     const int hu = u - p.full_units;
     u = p.full_units + (hu >> 1);
     r.half = hu & 1;
@@ -467,6 +504,60 @@ __device__ __forceinline__ uint32_t epi_barrier_and(uint32_t v) {
       : "r"(v)
       : "memory");
   return r;
+}
+
+// The K-half hand-off counters in global memory: an acquire load and an
+// acq_rel add at GPU scope.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* a) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* a, uint32_t x) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(x)
+               : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* a, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+
+// Bounded wait for a flag in global memory another CTA sets (release) once
+// work it has already begun is done.  Returns false when the pipeline is
+// abandoned, as wait_slow does.
+__device__ __noinline__ bool wait_flag_gpu(const uint32_t* f, const Params& p,
+                                           volatile uint32_t* abort_flag, uint32_t where) {
+  const unsigned long long start = globaltimer();
+  while (ld_acquire_gpu(f) == 0u) {
+    __nanosleep(64);
+    if (*abort_flag) return false;
+    if (globaltimer() - start > p.wait_limit_ns) {
+      atomicOr(p.ws + 2, kErrTimeout);
+      atomicCAS(p.ws + 3, 0u, where);
+      *abort_flag = 1u;
+      return false;
+    }
+  }
+  return true;
+}
+
+// 16 fp32 words of a K-half partial sum from L2: four 16-byte pieces 512
+// bytes apart.  One statement, so that the pieces of one chunk are in flight
+// together and the next chunk's are not hoisted above this one's adds.
+__device__ __forceinline__ void ld_part16(const float4* a, uint32_t (&x)[16]) {
+  asm volatile(
+      "ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%16];\n\t"
+      "ld.global.cg.v4.u32 {%4, %5, %6, %7}, [%16+512];\n\t"
+      "ld.global.cg.v4.u32 {%8, %9, %10, %11}, [%16+1024];\n\t"
+      "ld.global.cg.v4.u32 {%12, %13, %14, %15}, [%16+1536];"
+      : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]),
+        "=r"(x[7]), "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]),
+        "=r"(x[14]), "=r"(x[15])
+      : "l"(a)
+      : "memory");
 }
 
 // Named barrier `id` over `count` threads (whole warps).
@@ -619,6 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // has drained the shared columns, not the whole accumulator
   constexpr bool kOvl = KIND == kKindF8F6F4 && TILE_N == 256 && NUM_ACC == 1;
   constexpr uint32_t kOvlCols = 80;                       // 5 chunks of 16 columns
+  constexpr int kPartF4 = kTileM * TILE_N / 4;            // float4 per K-half partial sum buffer
   constexpr int kRegions = kOvl ? 2 : NUM_ACC;            // accumulator hand-off slots
   constexpr uint32_t kSfCol0 = kOvl ? 0u : NUM_ACC * TILE_N;
   static_assert(!kOvl || 2 * TILE_N <= kTmemCols, "regions fit");
@@ -769,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int brows = hu ? kBRows / 2 : kBRows;
         const CUtensorMap* const bmap = hu ? &tmap_bh : &tmap_b;
         const uint32_t b_stage_bytes = hu ? kBStage / 2 : kBStage;
-        for (int ks = 0; ks < p.k_stages; ++ks) {
+        for (int ks = tc.kb; ks < tc.ke; ++ks) {
           if (!BSG_WAIT(empty0 + 8u * stage, phase ^ 1u, scales ? 12 : 1)) { ok = false; break; }
           const uint32_t bar = bar_base + 8u * stage;
           armed |= 1u << stage;
@@ -925,7 +1017,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // a half-width unit runs N = TILE_N / 2 from the first half of each
         // CTA's B rows into the first TILE_N / 2 accumulator columns
         const uint32_t id_u = kHalves && u >= p.full_units ? p.idesc_half : idesc;
-        for (int ks = 0; ks < p.k_stages; ++ks) {
+        // the unit's K stages (a K half of a split tile: part of them)
+        const Tile tc = tile_coords(p, u, CM, crank);
+        const int kb = tc.kb;
+        for (int ks = kb; ks < tc.ke; ++ks) {
           // this stage's scales in tensor memory and its operands in smem:
           // both barriers tested at once on the fast path
           if (!(mbar_test_wait2(sfr0 + 8u * stage, full0 + 8u * stage, phase) ||
@@ -946,7 +1041,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_issue(d_tmem, ad + ((sl * kASlice) >> 4) + jj * a_kstep,
                         bd + ((sl * kBSlice) >> 4) + jj * b_kstep,
                         id_u | (sf_id << 29) | (sf_id << 4), sfa_t + 4 * c, sfb_t + 4 * G * c,
-                        (j != 0 || ks != 0) ? 1u : 0u);
+                        (j != 0 || ks != kb) ? 1u : 0u);
             }
           }
           // frees the smem stage (in both CTAs of a pair) once these MMAs
@@ -1001,8 +1096,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int u = unit0; u < p.num_units && ok; u += unit_step) {
       // row offset of the tile's first B row inside its first scale atom
-      const int n_off = (tile_coords(p, u, CM, crank).nt * TILE_N) % 128;
-      for (int ks = 0; ks < p.k_stages; ++ks) {
+      const Tile tc = tile_coords(p, u, CM, crank);
+      const int n_off = (tc.nt * TILE_N) % 128;
+      for (int ks = tc.kb; ks < tc.ke; ++ks) {
         // one lane sleeps on the barrier (the scale bytes are issued ahead of
         // the operand tiles, so there is slack; a polling warp would steal
         // issue slots from the MMA warp, which shares a sub-partition with
@@ -1078,7 +1174,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // take its verdict at a named barrier, which also wakes them at once
       // (napping warps added up to a nap's length to every hand-off)
       uint32_t ready = 1;
-      if (warp == kEpiWarp0 && lane == 0) ready = BSG_WAIT(accf0 + 8u * acc, acc_phase, 4) ? 1u : 0u;
+      // a K half: the same lane claims the split tile before the wait, so
+      // that the claim's round trip stays off the accumulator hand-off
+      uint32_t ks_first = 1;
+      if (warp == kEpiWarp0 && lane == 0) {
+        if (kOvl && tc.ks >= 0) ks_first = atom_add_acq_rel_gpu(p.ks_cnt + 4 * tc.ks + 2 * crank, 1u) == 0u;
+        ready = BSG_WAIT(accf0 + 8u * acc, acc_phase, 4) ? 1u : 0u;
+      }
       if (!epi_barrier_and(ready)) break;
       tc_fence_after();
       // a half-width unit (N = TILE_N / 2 in the first accumulator columns)
@@ -1113,6 +1215,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       auto release_shared = [&]() { arrive_on(shared_bar); };
+      // K halves of a split tile (kOvl kernels).  src 0: a unit over all of K;
+      // 2: this half claimed the tile first and publishes its partial sum;
+      // 1: the other half claimed first: this half parks its own partial sum
+      // too (freeing its tensor memory at once, as the claimant does), waits
+      // for the claimant's, and stores C from the two.  fp32 addition is
+      // commutative, so C does not depend on which half is which.
+      int src = 0;
+      // float4 offset in p.part of this CTA rank's buffer of K half kh
+      auto part_of = [&](int kh) { return (4 * tc.ks + 2 * kh + crank) * kPartF4; };
+      // a partial sum buffer holds, per 16-column chunk ch of the unit, lane
+      // quarter q and 16-byte piece v, the 32 lanes' pieces in 512 contiguous
+      // bytes: float4 ((ch * 4 + q) * 4 + v) * 32 + lane.  sum_part2: this
+      // lane's 16 values of chunks ch and ch + 2, both halves added (all
+      // four loads issued before the first add).
+      auto sum_part2 = [&](uint32_t (&r0)[16], uint32_t (&r1)[16], int ch) {
+        const float4* const a = reinterpret_cast<const float4*>(p.part) + (ch * 4 + q) * 128 + lane;
+        const float4* const b = a + 8 * 128;  // chunk ch + 2
+        uint32_t o0[16], o1[16];
+        ld_part16(a + part_of(tc.kh), r0);
+        ld_part16(b + part_of(tc.kh), r1);
+        ld_part16(a + part_of(tc.kh ^ 1), o0);
+        ld_part16(b + part_of(tc.kh ^ 1), o1);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          r0[j] = __float_as_uint(__uint_as_float(r0[j]) + __uint_as_float(o0[j]));
+          r1[j] = __float_as_uint(__uint_as_float(r1[j]) + __uint_as_float(o1[j]));
+        }
+      };
+      // src 1, after its own partial sum is out: the claimant's.  One lane
+      // waits for the flag (the claimant is past its MMAs and depends on no
+      // other CTA, so the bounded wait ends) and zeroes the tile's words for
+      // the next launch; every epilogue thread takes the verdict (false: an
+      // abandoned pipeline, whose error word is set).
+      auto await_part = [&]() -> bool {
+        uint32_t ok = 1;
+        if (warp == kEpiWarp0 && lane == 0) {
+          uint32_t* const cnt = p.ks_cnt + 4 * tc.ks + 2 * crank;
+          ok = wait_flag_gpu(cnt + 1, p, abort_flag, 19u) ? 1u : 0u;
+          cnt[0] = 0u;
+          cnt[1] = 0u;
+        }
+        return epi_barrier_and(ok) != 0u;
+      };
+      // src 1 and 2: the whole accumulator out to this half's buffer, in the
+      // 16-bit path's round order (a slot's shared columns first) and with
+      // its releases
+      auto drain_partial = [&]() {
+        constexpr int kNch = kCols / 16;
+        auto group_of = [&](int k) { return slot == 0 ? 3 - k : k; };
+        auto chunk_of = [&](int c0_, int i) { return 4 * group_of(c0_ / 2 + i / 2) + 2 * (i & 1) + h; };
+        uint32_t rb[kRnd][16];
+#pragma unroll
+        for (int c0 = 0; c0 < kNch; c0 += kRnd) {
+#pragma unroll
+          for (int i = 0; i < kRnd; ++i) tc_ld_32x32b_x16(tbase + 16 * chunk_of(c0, i), rb[i]);
+          tc_wait_ld();
+          if (c0 == 0) release_shared();
+          if (c0 + kRnd >= kNch) release();
+#pragma unroll
+          for (int i = 0; i < kRnd; ++i) {
+            float4* const d = reinterpret_cast<float4*>(p.part) + part_of(tc.kh) + (chunk_of(c0, i) * 4 + q) * 128 + lane;
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              d[32 * v] = make_float4(__uint_as_float(rb[i][4 * v]), __uint_as_float(rb[i][4 * v + 1]),
+                                      __uint_as_float(rb[i][4 * v + 2]), __uint_as_float(rb[i][4 * v + 3]));
+          }
+        }
+      };
       // kOvl units (FP8 operands, so 16-bit or fp32 C): warp h drains the
       // unit's 16-column chunks h, h + 2, h + 4, ...; a whole unit in slot 0
       // takes its chunks in the columns shared with slot 1 (its last 80:
@@ -1150,82 +1320,101 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool bf = p.c_dtype == BSG_BF16;
           uint16_t* const cbase = static_cast<uint16_t*>(p.c) + batch_off;
           uint8_t* const qstg = smem + p.smem_epi + q * (2 * kEpiStageBytes);
+          // chunk ch of the unit (piece pair e of its 64-column group):
+          // rounded, packed, counted toward Amax, and staged (n-major) or
+          // stored (m-major)
+          auto emit16 = [&](const uint32_t* r, int ch, int e) {
+            uint32_t w[8];
 #pragma unroll
-          for (int c0 = 0; c0 < kNch; c0 += kRnd) {
-#pragma unroll
-            for (int i = 0; i < kRnd; ++i) tc_ld_32x32b_x16(tbase + 16 * chunk_of(c0, i), rb[i]);
-            tc_wait_ld();
-            if (c0 == 0) release_shared();
-            if (c0 + kRnd >= kNch) release();
-#pragma unroll
-            for (int k = 0; k < kRnd / 2; ++k) {
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const uint32_t* r = rb[2 * k + e];
-                uint32_t w[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const float f0 = __uint_as_float(r[2 * j]), f1 = __uint_as_float(r[2 * j + 1]);
-                  if (bf) {
-                    const __nv_bfloat162 v = __floats2bfloat162_rn(f0, f1);
-                    w[j] = *reinterpret_cast<const uint32_t*>(&v);
-                  } else {
-                    const __half2 v = __floats2half2_rn(f0, f1);
-                    w[j] = *reinterpret_cast<const uint32_t*>(&v);
-                  }
-                }
-                const int col = ucol0 + 16 * chunk_of(c0, 2 * k + e);
-                // only stored elements count toward Amax
-                const int nv = row_ok ? n_end - col : 0;
-                if (nv >= 16) {
-#pragma unroll
-                  for (int j = 0; j < 8; ++j) vmax = __vmaxu2(vmax, w[j] & 0x7FFF7FFFu);
-                } else {
-#pragma unroll
-                  for (int j = 0; j < 8; ++j) {
-                    uint32_t m = w[j] & 0x7FFF7FFFu;
-                    if (2 * j >= nv) m &= 0xFFFF0000u;
-                    if (2 * j + 1 >= nv) m &= 0x0000FFFFu;
-                    vmax = __vmaxu2(vmax, m);
-                  }
-                }
-                if (p.c_major == 0) {
-                  // this row's 32 bytes of the chunk: 16-byte pieces
-                  // 2(2e + h) and 2(2e + h) + 1 of the 128-byte staged row,
-                  // XOR-swizzled by row % 8 (conflict-free both ways)
-                  const int pc0 = 2 * (2 * e + h);
-                  uint8_t* const srow = qstg + lane * 128;
-                  *reinterpret_cast<uint4*>(srow + ((pc0 ^ (lane & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
-                  *reinterpret_cast<uint4*>(srow + (((pc0 + 1) ^ (lane & 7)) * 16)) =
-                      make_uint4(w[4], w[5], w[6], w[7]);
-                } else {
-                  // m-major: column by column, the 32 lanes write 32 consecutive rows
-                  uint16_t* dst = cbase + static_cast<size_t>(col) * p.M + row;
-                  const int ncols = row_ok ? min(16, n_end - col) : 0;
-#pragma unroll
-                  for (int j = 0; j < 16; ++j) {
-                    if (j < ncols)
-                      *dst = static_cast<uint16_t>((j & 1) ? (w[j / 2] >> 16) : (w[j / 2] & 0xFFFFu));
-                    dst += p.M;
-                  }
-                }
+            for (int j = 0; j < 8; ++j) {
+              const float f0 = __uint_as_float(r[2 * j]), f1 = __uint_as_float(r[2 * j + 1]);
+              if (bf) {
+                const __nv_bfloat162 v = __floats2bfloat162_rn(f0, f1);
+                w[j] = *reinterpret_cast<const uint32_t*>(&v);
+              } else {
+                const __half2 v = __floats2half2_rn(f0, f1);
+                w[j] = *reinterpret_cast<const uint32_t*>(&v);
               }
-              if (p.c_major == 0) {
-                // the group's 32 rows x 128 bytes: this warp stores rows
-                // 16h .. 16h + 15, four rows (eight lanes each) per store
-                named_bar_sync(2 + q, 64);
-                const int gcol = ucol0 + 64 * group_of(c0 / 2 + k);
-                const int bytes_valid = (n_end - gcol) * 2;
+            }
+            const int col = ucol0 + 16 * ch;
+            // only stored elements count toward Amax
+            const int nv = row_ok ? n_end - col : 0;
+            if (nv >= 16) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  const int rr = 16 * h + 4 * j + (lane >> 3), pc = lane & 7;
-                  const uint4 x = *reinterpret_cast<const uint4*>(qstg + rr * 128 + ((pc ^ (rr & 7)) * 16));
-                  if (row0 + rr < p.M && pc * 16 < bytes_valid)
-                    *reinterpret_cast<uint4*>(reinterpret_cast<char*>(
-                        cbase + static_cast<size_t>(row0 + rr) * p.N + gcol) + pc * 16) = x;
-                }
-                named_bar_sync(2 + q, 64);  // the buffer is free for the next group
+              for (int j = 0; j < 8; ++j) vmax = __vmaxu2(vmax, w[j] & 0x7FFF7FFFu);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                uint32_t m = w[j] & 0x7FFF7FFFu;
+                if (2 * j >= nv) m &= 0xFFFF0000u;
+                if (2 * j + 1 >= nv) m &= 0x0000FFFFu;
+                vmax = __vmaxu2(vmax, m);
               }
+            }
+            if (p.c_major == 0) {
+              // this row's 32 bytes of the chunk: 16-byte pieces
+              // 2(2e + h) and 2(2e + h) + 1 of the 128-byte staged row,
+              // XOR-swizzled by row % 8 (conflict-free both ways)
+              const int pc0 = 2 * (2 * e + h);
+              uint8_t* const srow = qstg + lane * 128;
+              *reinterpret_cast<uint4*>(srow + ((pc0 ^ (lane & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+              *reinterpret_cast<uint4*>(srow + (((pc0 + 1) ^ (lane & 7)) * 16)) =
+                  make_uint4(w[4], w[5], w[6], w[7]);
+            } else {
+              // m-major: column by column, the 32 lanes write 32 consecutive rows
+              uint16_t* dst = cbase + static_cast<size_t>(col) * p.M + row;
+              const int ncols = row_ok ? min(16, n_end - col) : 0;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                if (j < ncols)
+                  *dst = static_cast<uint16_t>((j & 1) ? (w[j / 2] >> 16) : (w[j / 2] & 0xFFFFu));
+                dst += p.M;
+              }
+            }
+          };
+          // n-major: the staged 64-column group g out, 32 rows x 128 bytes;
+          // this warp stores rows 16h .. 16h + 15, four rows (eight lanes
+          // each) per store
+          auto store_group = [&](int g) {
+            if (p.c_major != 0) return;
+            named_bar_sync(2 + q, 64);
+            const int gcol = ucol0 + 64 * g;
+            const int bytes_valid = (n_end - gcol) * 2;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int rr = 16 * h + 4 * j + (lane >> 3), pc = lane & 7;
+              const uint4 x = *reinterpret_cast<const uint4*>(qstg + rr * 128 + ((pc ^ (rr & 7)) * 16));
+              if (row0 + rr < p.M && pc * 16 < bytes_valid)
+                *reinterpret_cast<uint4*>(reinterpret_cast<char*>(
+                    cbase + static_cast<size_t>(row0 + rr) * p.N + gcol) + pc * 16) = x;
+            }
+            named_bar_sync(2 + q, 64);  // the buffer is free for the next group
+          };
+          if (src == 0) {
+#pragma unroll
+            for (int c0 = 0; c0 < kNch; c0 += kRnd) {
+#pragma unroll
+              for (int i = 0; i < kRnd; ++i) tc_ld_32x32b_x16(tbase + 16 * chunk_of(c0, i), rb[i]);
+              tc_wait_ld();
+              if (c0 == 0) release_shared();
+              if (c0 + kRnd >= kNch) release();
+#pragma unroll
+              for (int k = 0; k < kRnd / 2; ++k) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) emit16(rb[2 * k + e], chunk_of(c0, 2 * k + e), e);
+                store_group(group_of(c0 / 2 + k));
+              }
+            }
+          } else {
+            // a K half: C from the two partial sums, a 64-column group at a
+            // time (its two chunks' loads in flight together)
+#pragma unroll 1
+            for (int g = 0; g < 4; ++g) {
+              uint32_t r0[16], r1[16];
+              sum_part2(r0, r1, 4 * g + h);
+              emit16(r0, 4 * g + h, 0);
+              emit16(r1, 4 * g + 2 + h, 1);
+              store_group(g);
             }
           }
         } else {
@@ -1259,21 +1448,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           };
           uint32_t r[kP1 * 16];
+          if (src == 0) {
 #pragma unroll
-          for (int i = 0; i < kP1; ++i) tc_ld_32x32b_x16(tbase + col_of(i), r + 16 * i);
-          tc_wait_ld();
-          // a whole unit's shared chunks are among its first kP1 slots
-          if (CW == kCols) release_shared();
+            for (int i = 0; i < kP1; ++i) tc_ld_32x32b_x16(tbase + col_of(i), r + 16 * i);
+            tc_wait_ld();
+            // a whole unit's shared chunks are among its first kP1 slots
+            if (CW == kCols) release_shared();
 #pragma unroll
-          for (int i = 0; i < kP1; ++i) {
-            chunk_out(ucol0 + col_of(i), r + 16 * i);
-            tc_ld_32x32b_x16(tbase + col_of(kP1 + i), r + 16 * i);
+            for (int i = 0; i < kP1; ++i) {
+              chunk_out(ucol0 + col_of(i), r + 16 * i);
+              tc_ld_32x32b_x16(tbase + col_of(kP1 + i), r + 16 * i);
+            }
+            tc_wait_ld();
+            if (CW != kCols) release_shared();
+            release();
+#pragma unroll
+            for (int i = 0; i < kP1; ++i) chunk_out(ucol0 + col_of(kP1 + i), r + 16 * i);
+          } else {
+            // a K half: C from the two partial sums, two chunks at a time
+            // (their loads in flight together)
+#pragma unroll 1
+            for (int ch = h; ch < 2 * kNch; ch += 4) {
+              uint32_t r0[16], r1[16];
+              sum_part2(r0, r1, ch);
+              chunk_out(ucol0 + 16 * ch, r0);
+              chunk_out(ucol0 + 16 * (ch + 2), r1);
+            }
           }
-          tc_wait_ld();
-          if (CW != kCols) release_shared();
-          release();
-#pragma unroll
-          for (int i = 0; i < kP1; ++i) chunk_out(ucol0 + col_of(kP1 + i), r + 16 * i);
         }
       };
       // the unit's stores: CW accumulator columns per warp, a compile-time
@@ -1511,6 +1712,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
+      if constexpr (kOvl) {
+        if (tc.ks >= 0) {
+          // both halves' partial sums go out; the claimant publishes its
+          // own, the other half waits for it and stores C
+          src = epi_barrier_and(ks_first) ? 2 : 1;
+          drain_partial();
+          if (src == 2) {
+            // every thread's stores ordered before the flag
+            __threadfence();
+            epi_barrier_and(1u);
+            if (warp == kEpiWarp0 && lane == 0) st_release_gpu(p.ks_cnt + 4 * tc.ks + 2 * crank + 1, 1u);
+            continue;
+          }
+          if (!await_part()) continue;
+        }
+      }
       if constexpr (kHalves) {
         if (hu) unit(std::integral_constant<int, kCols / 2>{});
         else unit(std::integral_constant<int, kCols>{});
@@ -1635,6 +1852,15 @@ EncodeTiledFn get_encode_fn() {
 }
 
 constexpr size_t kWorkspaceBytes = 256;
+// Past those words, for a plan with K halves: two words per split tile and
+// CTA rank (halves claimed, partial sum out; rounded up to 256 bytes), then
+// per split tile, K half and CTA rank a 128 x 256 fp32 partial sum.
+constexpr size_t kPartBytes = static_cast<size_t>(128) * 256 * 4;
+inline size_t ks_cnt_bytes(int tiles) { return (static_cast<size_t>(16) * tiles + 255) / 256 * 256; }
+inline size_t ws_need(int ks_tiles) {
+  return ks_tiles ? kWorkspaceBytes + ks_cnt_bytes(ks_tiles) + static_cast<size_t>(ks_tiles) * 4 * kPartBytes
+                  : kWorkspaceBytes;
+}
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -1663,6 +1889,9 @@ struct bsg_plan {
   int kslices;           // 128-byte K slices per pipeline stage
   int pair;              // 1: the cluster is a cta_group::2 pair (256-row MMAs)
   int half_tiles;        // tiles of the last wave run as two half-width units
+  int ks_tiles;          // tiles past the whole waves run as two K halves (a full workspace)
+  int max_clusters;      // clusters resident at once (persistent launches of pairs)
+  size_t ws_bytes;       // workspace of the plan's fastest form (with the K halves' buffers)
   int grid;
   int smem_bytes;
   // tensor maps for the last A/B pointers seen
@@ -1678,6 +1907,34 @@ struct bsg_plan {
   CUtensorMap map_sfa;
   CUtensorMap map_sfb;
 };
+
+// The schedule of one launch, by the workspace it is given: K halves when it
+// holds their buffers, else the half-width split of the last wave, else
+// whole tiles alone.
+static Params launch_params(const bsg_plan* plan, size_t ws_bytes) {
+  Params k = plan->base;
+  const int tiles = k.num_units;
+  if (plan->ks_tiles && ws_bytes >= plan->ws_bytes) {
+    k.ks_tiles = plan->ks_tiles;
+    k.ks_k0 = k.k_stages / 2;
+    k.ks_first = tiles - plan->ks_tiles;
+    k.num_units = tiles + plan->ks_tiles;
+    k.full_units = k.num_units;
+  } else if (plan->half_tiles) {
+    k.full_units = tiles - plan->half_tiles;
+    k.num_units = k.full_units + 2 * plan->half_tiles;
+  }
+  return k;
+}
+
+// CTAs of that launch: persistent clusters, at most as many as are resident
+static int launch_grid(const bsg_plan* plan, const Params& k) {
+  if (plan->cluster_m > 1) {
+    const int clusters = k.num_units < plan->max_clusters ? k.num_units : plan->max_clusters;
+    return plan->cluster_m * clusters;
+  }
+  return k.num_units < plan->sm_count ? k.num_units : plan->sm_count;
+}
 
 extern "C" {
 
@@ -1947,13 +2204,23 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
     // with k-major B only (a 64-row box of an MN-major B is not a whole
     // 128-byte swizzle span).
     const int tail = k.num_units % max_clusters;
-    if (plan->pair && k.tile_n == 256 && !b_mn && tail != 0 && 2 * tail <= max_clusters) {
+    if (plan->pair && k.tile_n == 256 && !b_mn && tail != 0 && 2 * tail <= max_clusters)
       plan->half_tiles = tail;
-      k.full_units = k.num_units - tail;
-      k.num_units = k.full_units + 2 * tail;
-    }
-    const int clusters = k.num_units < max_clusters ? k.num_units : max_clusters;
-    plan->grid = cm * clusters;
+    // K halves, preferred where they apply (FP8 256-wide pairs, at least two
+    // whole waves and two K stages): every cluster then carries at most half
+    // a tile more than the whole waves, at full width, where a half-width
+    // tile streams its operands at a lower tensor rate.  They need the
+    // workspace's partial-sum buffers; a smaller workspace runs the
+    // half-width split (or none).
+    if (plan->pair && kind == kKindF8F6F4 && k.tile_n == 256 && num_acc == 1 && tail != 0 &&
+        2 * tail <= max_clusters && k.num_units / max_clusters >= 2 && k.k_stages >= 2)
+      plan->ks_tiles = tail;
+    plan->max_clusters = max_clusters;
+  }
+  plan->ws_bytes = ws_need(plan->ks_tiles);
+  {
+    const Params f = launch_params(plan, plan->ws_bytes);
+    plan->grid = launch_grid(plan, f);
   }
   if (std::getenv("BSG_LOG"))
     std::fprintf(stderr,
@@ -1968,14 +2235,20 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
 
 bsg_status bsg_plan_workspace_size(const bsg_plan* plan, size_t* bytes) {
   if (!plan || !bytes) return BSG_ERR_INVALID_ARG;
-  *bytes = kWorkspaceBytes;
+  *bytes = plan->ws_bytes;
   return BSG_OK;
 }
 
 bsg_status bsg_workspace_init(const bsg_plan* plan, void* ws, size_t ws_bytes, void* stream) {
   if (!plan || !ws) return BSG_ERR_INVALID_ARG;
   if (ws_bytes < kWorkspaceBytes) return BSG_ERR_WORKSPACE;
-  if (cudaMemsetAsync(ws, 0, kWorkspaceBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+  // the words every run needs, and the K halves' counters when the
+  // workspace is large enough for their form (the partial sums need no
+  // initial value)
+  const size_t zero = ws_bytes >= plan->ws_bytes && plan->ks_tiles
+                          ? kWorkspaceBytes + ks_cnt_bytes(plan->ks_tiles)
+                          : kWorkspaceBytes;
+  if (cudaMemsetAsync(ws, 0, zero, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
     cudaGetLastError();
     return BSG_ERR_CUDA;
   }
@@ -2054,7 +2327,12 @@ bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const vo
   bsg_plan* plan = const_cast<bsg_plan*>(cplan);
   const bsg_problem& pr = plan->prob;
   const int64_t row_bytes = plan->base.k_bytes;
-  Params k = plan->base;
+  Params k = launch_params(plan, ws_bytes);
+  if (k.ks_tiles) {
+    char* const w = static_cast<char*>(ws);
+    k.ks_cnt = reinterpret_cast<uint32_t*>(w + kWorkspaceBytes);
+    k.part = reinterpret_cast<float*>(w + kWorkspaceBytes + ks_cnt_bytes(k.ks_tiles));
+  }
   k.sfa = static_cast<const uint8_t*>(SFA);
   k.sfb = static_cast<const uint8_t*>(SFB);
   k.c = C;
@@ -2078,7 +2356,7 @@ bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const vo
       }
       plan->map_b_ptr = B;
     }
-    if (plan->half_tiles && plan->map_bh_ptr != B) {
+    if (k.full_units < k.num_units && plan->map_bh_ptr != B) {
       // each CTA of a pair loads 64 rows of a half-width unit's B
       if (!encode_operand(&plan->map_bh, B, row_bytes, pr.N, pr.L, k.tile_n / 4, false)) {
         plan->map_bh_ptr = nullptr;
@@ -2105,14 +2383,14 @@ bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const vo
     }
     ma = plan->map_a;
     mb = plan->map_b;
-    mbh = plan->half_tiles ? plan->map_bh : plan->map_b;
+    mbh = k.full_units < k.num_units ? plan->map_bh : plan->map_b;
     msfa = plan->map_sfa;
     msfb = plan->map_sfb;
   }
   void* args[6] = {&ma, &mb, &mbh, &msfa, &msfb, &k};
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(plan->grid);
+  cfg.gridDim = dim3(launch_grid(plan, k));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = static_cast<size_t>(plan->smem_bytes);
   cfg.stream = static_cast<cudaStream_t>(stream);
@@ -2137,9 +2415,11 @@ bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const vo
 // that cannot allocate device memory at all (no allocator of their own, or a
 // context in which cudaMalloc is not allowed).
 
-// Largest workspace the fixed array can stand in for; a plan needing more is
-// rejected with BSG_ERR_WORKSPACE.
+// The fixed array: the words every run needs.  A plan whose fastest form
+// needs more (the K halves' partial sums) runs the form a small workspace
+// gets, as bsg_run does with one.
 static constexpr size_t kNoAllocScratchBytes = 4096;
+static_assert(kWorkspaceBytes <= kNoAllocScratchBytes, "every plan runs on the fixed array");
 
 // Loaded (zero, having no initialiser) on every GPU that loads this library,
 // held until exit.  Host code must not hand this name to a kernel: on the
@@ -2173,13 +2453,9 @@ static bsg_status noalloc_scratch(int device, void** out) {
 bsg_status bsg_run_noalloc(const bsg_plan* plan, const void* A, const void* B, const void* SFA,
                            const void* SFB, void* C, float* amax, void* stream) {
   if (!plan) return BSG_ERR_INVALID_ARG;
-  size_t need = 0;
-  bsg_status st = bsg_plan_workspace_size(plan, &need);
-  if (st != BSG_OK) return st;
-  if (need > kNoAllocScratchBytes) return BSG_ERR_WORKSPACE;
   // the checks bsg_run makes, before the array is looked up or cleared, so
   // that a bad pointer or the wrong current device touches no device state
-  st = check_run_args(plan, A, B, SFA, SFB, C, amax);
+  bsg_status st = check_run_args(plan, A, B, SFA, SFB, C, amax);
   if (st != BSG_OK) return st;
   void* scratch = nullptr;
   st = noalloc_scratch(plan->device, &scratch);
@@ -2262,6 +2538,7 @@ bsg_status bsg_plan_describe(const bsg_plan* plan, bsg_plan_info* info) {
   info->mma_kind = plan->kind;
   info->cluster_m = plan->cluster_m;
   info->half_tiles = plan->half_tiles;
+  info->k_split_tiles = plan->ks_tiles;
   std::snprintf(info->kernel_name, sizeof(info->kernel_name), "bsg_gemm_amax_kernel");
   return BSG_OK;
 }

@@ -129,7 +129,11 @@ typedef struct {
     int32_t cluster_m;                     /* 1: CTAs alone; 2: cta_group::2 pairs */
     char kernel_name[64];
     int32_t half_tiles;                    /* tiles of the last wave run as two 256 x 128
-                                              half-width units (0: none) */
+                                              half-width units (0: none), when the
+                                              K halves below are not run */
+    int32_t k_split_tiles;                 /* tiles past the whole waves run as two K
+                                              halves at full width, with the plan's full
+                                              workspace (0: none) */
 } bsg_plan_info;
 
 /* Host-only validation of a problem against the support surface; touches
@@ -142,16 +146,24 @@ bsg_status bsg_problem_check(const bsg_problem *problem);
  * is sm_103.  *out is set only on BSG_OK. */
 bsg_status bsg_plan_create(const bsg_problem *problem, int device, bsg_plan **out);
 
-/* Bytes of device workspace a run of this plan needs (a small fixed
- * amount: a cross-CTA amax slot, an arrival counter and an error word).
+/* Bytes of device workspace for the plan's fastest form.  256 bytes hold
+ * a cross-CTA amax slot, an arrival counter and an error word; a plan that
+ * runs its leftover tiles as two K halves (bsg_plan_info.k_split_tiles > 0:
+ * FP8 256-wide pairs with at least two whole waves of tiles) adds one
+ * counter per split tile and CTA and, per split tile, four 128 x 256 fp32
+ * partial sums (512 KiB).  bsg_run accepts any workspace of at least 256
+ * bytes and runs the K halves only when it is at least this size; a smaller
+ * one runs the half-width split of the last wave instead (same inputs, C
+ * within the same tolerance, not bit-identical).
  * The workspace lives in the caller's allocator, as the workspaces of
  * "Grouped GEMM (SM100 BF16)", section "Using JAX arrays", do. */
 bsg_status bsg_plan_workspace_size(const bsg_plan *plan, size_t *bytes);
 
 /* Zero a workspace on `stream` (cudaMemsetAsync).  Must be called once
- * before a workspace is first used; every run leaves it zeroed again
- * (caller-allocator workspaces: "Grouped GEMM (SM100 BF16)", "Using JAX
- * arrays"). */
+ * before a workspace is first used, with the size later runs pass; every
+ * completed run leaves it zeroed again (after BSG_ERR_DEVICE_TIMEOUT, call
+ * it again) (caller-allocator workspaces: "Grouped GEMM (SM100 BF16)",
+ * "Using JAX arrays"). */
 bsg_status bsg_workspace_init(const bsg_plan *plan, void *workspace, size_t ws_bytes,
                               void *stream);
 
@@ -171,8 +183,9 @@ bsg_status bsg_run(const bsg_plan *plan, const void *A, const void *B, const voi
  * cudaMalloc is not permitted).  The pages have no counterpart: it is a
  * convenience of this library.  The workspace comes from a fixed array
  * inside the library (4096 bytes on every GPU that loads it, kept until the
- * process exits; zero when the library is loaded); a plan needing more
- * returns BSG_ERR_WORKSPACE.  The arguments are checked first, exactly as
+ * process exits; zero when the library is loaded); a plan whose fastest form
+ * needs more runs the form a small workspace gets (see
+ * bsg_plan_workspace_size).  The arguments are checked first, exactly as
  * bsg_run checks them, so a bad pointer or the wrong current device returns
  * its status before anything is enqueued.  The first call on a device then
  * looks up the array's device address (cudaGetSymbolAddress, host side
