@@ -64,13 +64,13 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # comments and whitespace removed, so only a code change invalidates an
 # entry) and workload.
 TRAFFIC = {
-    ("0b4cb9aa8ffee0ab", 1): 184320,
-    ("0b4cb9aa8ffee0ab", 2): 40956672,
-    ("0b4cb9aa8ffee0ab", 3): 416777984,
-    ("0b4cb9aa8ffee0ab", 4): 201289472,
-    ("0b4cb9aa8ffee0ab", 5): 190086400,
-    ("0b4cb9aa8ffee0ab", 6): 201464832,
-    ("0b4cb9aa8ffee0ab", 7): 41391104,
+    ("9e46d5bf2a9f03a4", 1): 185856,
+    ("9e46d5bf2a9f03a4", 2): 41282816,
+    ("9e46d5bf2a9f03a4", 3): 419034880,
+    ("9e46d5bf2a9f03a4", 4): 201497856,
+    ("9e46d5bf2a9f03a4", 5): 190082048,
+    ("9e46d5bf2a9f03a4", 6): 201939968,
+    ("9e46d5bf2a9f03a4", 7): 41329152,
 }
 
 

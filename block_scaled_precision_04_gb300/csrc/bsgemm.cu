@@ -1245,17 +1245,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // src 1, after its own partial sum is out: the claimant's.  One lane
       // waits for the flag (the claimant is past its MMAs and depends on no
-      // other CTA, so the bounded wait ends) and zeroes the tile's words for
-      // the next launch; every epilogue thread takes the verdict (false: an
-      // abandoned pipeline, whose error word is set).
+      // other CTA, so the bounded wait ends); every epilogue thread takes the
+      // verdict (false: an abandoned pipeline, whose error word is set).
       auto await_part = [&]() -> bool {
         uint32_t ok = 1;
-        if (warp == kEpiWarp0 && lane == 0) {
-          uint32_t* const cnt = p.ks_cnt + 4 * tc.ks + 2 * crank;
-          ok = wait_flag_gpu(cnt + 1, p, abort_flag, 19u) ? 1u : 0u;
-          cnt[0] = 0u;
-          cnt[1] = 0u;
-        }
+        if (warp == kEpiWarp0 && lane == 0)
+          ok = wait_flag_gpu(p.ks_cnt + 4 * tc.ks + 2 * crank + 1, p, abort_flag, 19u) ? 1u : 0u;
         return epi_barrier_and(ok) != 0u;
       };
       // src 1 and 2: the whole accumulator out to this half's buffer, in the
@@ -1773,7 +1768,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     // global Amax: max over CTAs, written by the last CTA to arrive, which
-    // also re-zeroes the two workspace slots for the next run
+    // also re-zeroes the two workspace slots and the K halves' words for the
+    // next run (every CTA is past its epilogue by then, an abandoned launch
+    // too)
     atomicMax(p.ws + 0, *cta_amax);
     __threadfence();
     const uint32_t arrived = atomicAdd(p.ws + 1, 1u);
@@ -1781,6 +1778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __threadfence();
       const uint32_t bits = atomicExch(p.ws + 0, 0u);
       *p.amax = __uint_as_float(bits);
+      for (int i = 0; i < 4 * p.ks_tiles; ++i) p.ks_cnt[i] = 0u;
       atomicExch(p.ws + 1, 0u);
     }
   }

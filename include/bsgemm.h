@@ -161,9 +161,9 @@ bsg_status bsg_plan_workspace_size(const bsg_plan *plan, size_t *bytes);
 
 /* Zero a workspace on `stream` (cudaMemsetAsync).  Must be called once
  * before a workspace is first used, with the size later runs pass; every
- * completed run leaves it zeroed again (after BSG_ERR_DEVICE_TIMEOUT, call
- * it again) (caller-allocator workspaces: "Grouped GEMM (SM100 BF16)",
- * "Using JAX arrays"). */
+ * run leaves it zeroed again, an abandoned one too, but for the error word
+ * that bsg_check_device_status reads and clears (caller-allocator
+ * workspaces: "Grouped GEMM (SM100 BF16)", "Using JAX arrays"). */
 bsg_status bsg_workspace_init(const bsg_plan *plan, void *workspace, size_t ws_bytes,
                               void *stream);
 

@@ -56,3 +56,38 @@ def test_wait_limit_reports_timeout_then_context_recovers(tile_n, cluster_m, mon
     # a normal plan on the same context
     c, a, *_ = run_gpu(inp, tile_n=tile_n, cluster_m=cluster_m)
     assert_parity(inp, c, a)
+
+
+def test_k_halves_timeout_leaves_the_workspace_reusable(monkeypatch):
+    """A plan whose leftover tiles run as K halves (the claim, the partial
+    sums and the bounded wait for the claimant's flag in its epilogues),
+    abandoned by the same 2 us wait limit: the launch returns with
+    BSG_ERR_DEVICE_TIMEOUT, and its workspace, once the error word is read,
+    serves a plan with the normal limit to parity (the abandoned launch left
+    the K halves' words zero)."""
+    G = bsg.GemmAmax(problem_of(synth.Problem(8192, 8192, 256, 1))).describe()["grid"] // 2
+    inp = synth.workload(2, M=256 * (2 * G + 8) - 64, N=256, K=1024)
+    p = inp.problem
+    monkeypatch.setenv("BSG_WAIT_LIMIT_NS", "2000")
+    op = bsg.GemmAmax(problem_of(p))
+    monkeypatch.delenv("BSG_WAIT_LIMIT_NS")
+    assert op.describe()["k_split_tiles"] == 8
+    A, B, SFA, SFB = to_device(inp)
+    C = torch.zeros(synth.c_shape(p), dtype=torch.bfloat16, device="cuda:0")
+    amax = torch.zeros(1, dtype=torch.float32, device="cuda:0")
+    for _ in range(2):
+        op.run(A, B, SFA, SFB, C, amax)
+        torch.cuda.synchronize()
+        assert op.device_status() == bsg.BSG_ERR_DEVICE_TIMEOUT
+    assert op.device_status() == bsg.BSG_OK
+    ok = bsg.GemmAmax(problem_of(p))
+    assert ok.ws_bytes == op.ws_bytes and ok.describe()["k_split_tiles"] == 8
+    s = torch.cuda.current_stream().cuda_stream
+    C.fill_(float("nan"))
+    st = bsg.bsg_run(ok.plan, A.data_ptr(), B.data_ptr(), SFA.data_ptr(), SFB.data_ptr(),
+                     C.data_ptr(), amax.data_ptr(), op.workspace.data_ptr(), op.ws_bytes, s)
+    assert st == bsg.BSG_OK
+    torch.cuda.synchronize()
+    assert bsg.bsg_check_device_status(ok.plan, op.workspace.data_ptr(), s) == bsg.BSG_OK
+    c = C.float().cpu().numpy().astype("float64")
+    assert_parity(inp, c, float(amax.item()))
