@@ -52,7 +52,8 @@ def with_tiles(G, extra, N, K, L=1, trim=37, **kw):
 # (extra tiles, N, K, L, trim, keywords): bf16 with 3 K stages (halves of 1
 # and 2), fp32 m-major over two batches, f16 at the most split tiles with 2
 # stages, MN-major A and B, E5M2 x E4M3 with a ragged K (8 stages, the last
-# partial), fp32 n-major over four N tiles with a ragged N edge
+# partial), fp32 n-major over four N tiles with a ragged N edge, bf16 m-major
+# with a ragged N edge
 SHAPES = [
     (10, 200, 384, 1, 37, dict(c="bf16")),
     (10, 256, 512, 2, 36, dict(c="f32", major="m")),
@@ -60,9 +61,10 @@ SHAPES = [
     (7, 256, 512, 1, 48, dict(c="bf16", am="m", bm="n")),
     (20, 160, 1008, 1, 5, dict(a="e5m2", c="f32")),
     (12, 1000, 256, 1, 100, dict(c="f32")),
+    (9, 232, 512, 1, 40, dict(c="bf16", major="m")),
 ]
 IDS = ["bf16_k3", "f32_mmajor_L2", "f16_max_split_k2", "bf16_mn_major", "e5m2_f32_ragged_k",
-       "f32_ragged_n"]
+       "f32_ragged_n", "bf16_mmajor_ragged_n"]
 
 
 def case(G, i):
