@@ -694,8 +694,9 @@ def main(argv=None):
                          "rows (the workload split in 128-row atoms, strong scaling)")
     ap.add_argument("--qworkload", type=int, default=1, choices=sorted(QWORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--e2e-streams", type=int, default=2,
-                    help="streams the end-to-end GEMM steps alternate between")
+    ap.add_argument("--e2e-streams", type=int, default=3,
+                    help="streams the end-to-end GEMM steps alternate between (3: the host "
+                         "link carries both directions; more streams measured no faster)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
