@@ -64,13 +64,13 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # comments and whitespace removed, so only a code change invalidates an
 # entry) and workload.
 TRAFFIC = {
-    ("9e46d5bf2a9f03a4", 1): 185856,
-    ("9e46d5bf2a9f03a4", 2): 41282816,
-    ("9e46d5bf2a9f03a4", 3): 419034880,
-    ("9e46d5bf2a9f03a4", 4): 201497856,
-    ("9e46d5bf2a9f03a4", 5): 190082048,
-    ("9e46d5bf2a9f03a4", 6): 201939968,
-    ("9e46d5bf2a9f03a4", 7): 41329152,
+    ("c4e10b47e5246bc0", 1): 183552,
+    ("c4e10b47e5246bc0", 2): 35740416,
+    ("c4e10b47e5246bc0", 3): 415345920,
+    ("c4e10b47e5246bc0", 4): 201296896,
+    ("c4e10b47e5246bc0", 5): 190004224,
+    ("c4e10b47e5246bc0", 6): 201825792,
+    ("c4e10b47e5246bc0", 7): 35858944,
 }
 
 

@@ -397,6 +397,7 @@ struct Tile {
 // half-width tail tile (the other split) takes about as long as a whole one:
 // its pipeline is bound by the ring's round trip, not the tensor rate.  The
 // whole tiles fill the other units in order.
+template <bool KS>
 __device__ __forceinline__ Tile tile_coords(const Params& p, int u, int cm, int rank) {
   Tile r;
   r.half = -1;
@@ -404,7 +405,7 @@ __device__ __forceinline__ Tile tile_coords(const Params& p, int u, int cm, int 
   r.kh = 0;
   r.kb = 0;
   r.ke = p.k_stages;
-  if (p.ks_tiles > 0) {
+  if (KS && p.ks_tiles > 0) {
     const int R = p.ks_tiles;
     if (u < 2 * R) {
       r.ks = u < R ? u : u - R;
@@ -669,7 +670,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 // LOWC: the epilogue writes low-precision C (E4M3, E5M2 or packed E2M1; FP4
 // operands only); a kernel of its own, since that path's registers would
 // otherwise spill in every FP4 kernel.
-template <int KIND, int TILE_N, int NUM_ACC, int CM, int PAIR, int KSL, int LOWC>
+template <int KIND, int TILE_N, int NUM_ACC, int CM, int PAIR, int KSL, int LOWC, int KSPL>
 __global__ void __launch_bounds__(kThreads, 1)
     bsg_gemm_amax_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b,
@@ -711,6 +712,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool kOvl = KIND == kKindF8F6F4 && TILE_N == 256 && NUM_ACC == 1;
   constexpr uint32_t kOvlCols = 80;                       // 5 chunks of 16 columns
   constexpr int kPartF4 = kTileM * TILE_N / 4;            // float4 per K-half partial sum buffer
+  // the instantiation that runs K halves of the leftover tiles (launched
+  // only when a run uses them: the code they need, compiled into every
+  // launch, slowed the ordinary one)
+  constexpr bool kKs = KSPL != 0 && kOvl;
   constexpr int kRegions = kOvl ? 2 : NUM_ACC;            // accumulator hand-off slots
   constexpr uint32_t kSfCol0 = kOvl ? 0u : NUM_ACC * TILE_N;
   static_assert(!kOvl || 2 * TILE_N <= kTmemCols, "regions fit");
@@ -852,7 +857,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t bar_base = scales ? sff0 : full0;
       const bool a_mn = KIND == kKindF8F6F4 && p.a_mn, b_mn = KIND == kKindF8F6F4 && p.b_mn;
       for (int u = unit0; u < p.num_units && ok; u += unit_step) {
-        const Tile tc = tile_coords(p, u, CM, crank);
+        const Tile tc = tile_coords<kKs>(p, u, CM, crank);
         const bool hu = kHalves && tc.half >= 0;
         const int m0 = tc.mt * kTileM;
         const int n0 = tc.nt * TILE_N + (hu ? tc.half * (TILE_N / 2) : 0);
@@ -1018,7 +1023,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // CTA's B rows into the first TILE_N / 2 accumulator columns
         const uint32_t id_u = kHalves && u >= p.full_units ? p.idesc_half : idesc;
         // the unit's K stages (a K half of a split tile: part of them)
-        const Tile tc = tile_coords(p, u, CM, crank);
+        const Tile tc = tile_coords<kKs>(p, u, CM, crank);
         const int kb = tc.kb;
         for (int ks = kb; ks < tc.ke; ++ks) {
           // this stage's scales in tensor memory and its operands in smem:
@@ -1096,7 +1101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int u = unit0; u < p.num_units && ok; u += unit_step) {
       // row offset of the tile's first B row inside its first scale atom
-      const Tile tc = tile_coords(p, u, CM, crank);
+      const Tile tc = tile_coords<kKs>(p, u, CM, crank);
       const int n_off = (tc.nt * TILE_N) % 128;
       for (int ks = tc.kb; ks < tc.ke; ++ks) {
         // one lane sleeps on the barrier (the scale bytes are issued ahead of
@@ -1169,7 +1174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = unit0; u < p.num_units; u += unit_step) {
-      const Tile tc = tile_coords(p, u, CM, crank);
+      const Tile tc = tile_coords<kKs>(p, u, CM, crank);
       // one lane of one warp spins on the accumulator; the 8 epilogue warps
       // take its verdict at a named barrier, which also wakes them at once
       // (napping warps added up to a nap's length to every hand-off)
@@ -1178,7 +1183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // that the claim's round trip stays off the accumulator hand-off
       uint32_t ks_first = 1;
       if (warp == kEpiWarp0 && lane == 0) {
-        if (kOvl && tc.ks >= 0) ks_first = atom_add_acq_rel_gpu(p.ks_cnt + 4 * tc.ks + 2 * crank, 1u) == 0u;
+        if constexpr (kKs) {
+          if (tc.ks >= 0) ks_first = atom_add_acq_rel_gpu(p.ks_cnt + 4 * tc.ks + 2 * crank, 1u) == 0u;
+        }
         ready = BSG_WAIT(accf0 + 8u * acc, acc_phase, 4) ? 1u : 0u;
       }
       if (!epi_barrier_and(ready)) break;
@@ -1385,7 +1392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             named_bar_sync(2 + q, 64);  // the buffer is free for the next group
           };
-          if (src == 0) {
+          if (!kKs || src == 0) {
 #pragma unroll
             for (int c0 = 0; c0 < kNch; c0 += kRnd) {
 #pragma unroll
@@ -1443,7 +1450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           };
           uint32_t r[kP1 * 16];
-          if (src == 0) {
+          if (!kKs || src == 0) {
 #pragma unroll
             for (int i = 0; i < kP1; ++i) tc_ld_32x32b_x16(tbase + col_of(i), r + 16 * i);
             tc_wait_ld();
@@ -1707,7 +1714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
-      if constexpr (kOvl) {
+      if constexpr (kKs) {
         if (tc.ks >= 0) {
           // both halves' partial sums go out; the claimant publishes its
           // own, the other half waits for it and stores C
@@ -1778,7 +1785,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __threadfence();
       const uint32_t bits = atomicExch(p.ws + 0, 0u);
       *p.amax = __uint_as_float(bits);
-      for (int i = 0; i < 4 * p.ks_tiles; ++i) p.ks_cnt[i] = 0u;
+      if constexpr (kKs)
+        for (int i = 0; i < 4 * p.ks_tiles; ++i) p.ks_cnt[i] = 0u;
       atomicExch(p.ws + 1, 0u);
     }
   }
@@ -1789,15 +1797,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Kernel variants: MMA kind x (TILE_N, accumulator buffers) x cluster along M
 // (cm 1: a CTA alone; 2: a cta_group::2 pair)
 struct Variant {
-  int kind, tile_n, num_acc, cm, pair, kslices, lowc;
+  int kind, tile_n, num_acc, cm, pair, kslices, lowc, kspl;
   const void* fn;
 };
 
-template <int KIND, int TN, int NACC, int CM, int PAIR, int LOWC = 0, int KSL = 1>
+template <int KIND, int TN, int NACC, int CM, int PAIR, int LOWC = 0, int KSL = 1, int KSPL = 0>
 Variant make_variant() {
-  return Variant{KIND, TN, NACC, CM, PAIR, KSL, LOWC,
+  return Variant{KIND, TN, NACC, CM, PAIR, KSL, LOWC, KSPL,
                  reinterpret_cast<const void*>(
-                     &bsg_gemm_amax_kernel<KIND, TN, NACC, CM, PAIR, KSL, LOWC>)};
+                     &bsg_gemm_amax_kernel<KIND, TN, NACC, CM, PAIR, KSL, LOWC, KSPL>)};
 }
 
 template <int KIND, int LOWC>
@@ -1807,13 +1815,15 @@ void add_kind(Variant* out, int& n) {
   out[n++] = make_variant<KIND, 256, 1, 2, 1, LOWC>();
 }
 
-const Variant* find_variant(int kind, int tile_n, int num_acc, int cm, int kslices, int lowc) {
-  static Variant table[16];
+const Variant* find_variant(int kind, int tile_n, int num_acc, int cm, int kslices, int lowc,
+                            int kspl = 0) {
+  static Variant table[24];
   static int n = 0;
   static std::once_flag once;
   std::call_once(once, [] {
     add_kind<kKindF8F6F4, 0>(table, n);
     table[n++] = make_variant<kKindF8F6F4, 224, 2, 2, 1>();  // 256 x 224 pairs, two accumulators
+    table[n++] = make_variant<kKindF8F6F4, 256, 1, 2, 1, 0, 1, 1>();  // pairs with K halves
     add_kind<kKindF4x4X, 0>(table, n);
     add_kind<kKindF4x2X, 0>(table, n);
     add_kind<kKindF4x4X, 1>(table, n);  // FP4 operands with E4M3 / E5M2 / E2M1 C
@@ -1822,7 +1832,7 @@ const Variant* find_variant(int kind, int tile_n, int num_acc, int cm, int kslic
   for (int i = 0; i < n; ++i) {
     const Variant& v = table[i];
     if (v.kind == kind && v.tile_n == tile_n && v.num_acc == num_acc && v.cm == cm &&
-        v.kslices == kslices && v.lowc == lowc)
+        v.kslices == kslices && v.lowc == lowc && v.kspl == kspl)
       return &v;
   }
   return nullptr;
@@ -1881,6 +1891,7 @@ struct bsg_plan {
   int sm_count;
   Params base;           // everything but the pointers
   const void* kernel;    // the chosen kernel variant
+  const void* kernel_ks; // its instantiation with K halves (plans with k_split_tiles)
   int kind;
   int num_acc;
   int cluster_m;         // CTAs per cluster along M: 1, or 2 for a cta_group::2 pair
@@ -2205,14 +2216,35 @@ bsg_status bsg_plan_create(const bsg_problem* prob, int device, bsg_plan** out) 
     if (plan->pair && k.tile_n == 256 && !b_mn && tail != 0 && 2 * tail <= max_clusters)
       plan->half_tiles = tail;
     // K halves, preferred where they apply (FP8 256-wide pairs, at least two
-    // whole waves and two K stages): every cluster then carries at most half
-    // a tile more than the whole waves, at full width, where a half-width
-    // tile streams its operands at a lower tensor rate.  They need the
-    // workspace's partial-sum buffers; a smaller workspace runs the
-    // half-width split (or none).
+    // whole waves): every cluster then carries at most half a tile more than
+    // the whole waves, at full width, where a half-width tile takes about as
+    // long as a whole one.  The exchange of partial sums costs about as much
+    // as 19 K stages, so they pay from 40 K stages on (the ragged L=2
+    // workload, 56 stages: -2.6 %; 4096^3, 32 stages: +1.6 %, measured by
+    // the benchmark's own timing).  BSG_KSPLIT_MIN_STAGES (read here) moves
+    // that threshold, down to 2.  They need the workspace's partial-sum
+    // buffers; a smaller workspace runs the half-width split (or none).
+    int ks_min = 40;
+    if (const char* e = std::getenv("BSG_KSPLIT_MIN_STAGES")) {
+      const long v = std::strtol(e, nullptr, 10);
+      if (v >= 2 && v <= (1L << 30)) ks_min = static_cast<int>(v);
+    }
     if (plan->pair && kind == kKindF8F6F4 && k.tile_n == 256 && num_acc == 1 && tail != 0 &&
-        2 * tail <= max_clusters && k.num_units / max_clusters >= 2 && k.k_stages >= 2)
-      plan->ks_tiles = tail;
+        2 * tail <= max_clusters && k.num_units / max_clusters >= 2 && k.k_stages >= ks_min) {
+      const Variant* vk = find_variant(kind, k.tile_n, num_acc, cm, ksl, lowc, 1);
+      if (vk) {
+        if (prev != device) cudaSetDevice(device);
+        const cudaError_t ek = cudaFuncSetAttribute(
+            vk->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, plan->smem_bytes);
+        if (prev != device) cudaSetDevice(prev);
+        if (ek == cudaSuccess) {
+          plan->kernel_ks = vk->fn;
+          plan->ks_tiles = tail;
+        } else {
+          cudaGetLastError();
+        }
+      }
+    }
     plan->max_clusters = max_clusters;
   }
   plan->ws_bytes = ws_need(plan->ks_tiles);
@@ -2389,6 +2421,7 @@ bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const vo
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(launch_grid(plan, k));
+  const void* const fn = k.ks_tiles ? plan->kernel_ks : plan->kernel;
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = static_cast<size_t>(plan->smem_bytes);
   cfg.stream = static_cast<cudaStream_t>(stream);
@@ -2400,7 +2433,7 @@ bsg_status bsg_run(const bsg_plan* cplan, const void* A, const void* B, const vo
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  if (cudaLaunchKernelExC(&cfg, plan->kernel, args) != cudaSuccess) {
+  if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
     cudaGetLastError();
     return BSG_ERR_CUDA;
   }

@@ -149,8 +149,10 @@ bsg_status bsg_plan_create(const bsg_problem *problem, int device, bsg_plan **ou
 /* Bytes of device workspace for the plan's fastest form.  256 bytes hold
  * a cross-CTA amax slot, an arrival counter and an error word; a plan that
  * runs its leftover tiles as two K halves (bsg_plan_info.k_split_tiles > 0:
- * FP8 256-wide pairs with at least two whole waves of tiles) adds one
- * counter per split tile and CTA and, per split tile, four 128 x 256 fp32
+ * FP8 256-wide pairs with at least two whole waves of tiles and at least 40
+ * K stages of 128 bytes; the environment variable BSG_KSPLIT_MIN_STAGES,
+ * read by bsg_plan_create, moves that threshold) adds two words per split
+ * tile and CTA and, per split tile, four 128 x 256 fp32
  * partial sums (512 KiB).  bsg_run accepts any workspace of at least 256
  * bytes and runs the K halves only when it is at least this size; a smaller
  * one runs the half-width split of the last wave instead (same inputs, C

@@ -68,6 +68,7 @@ def test_k_halves_timeout_leaves_the_workspace_reusable(monkeypatch):
     G = bsg.GemmAmax(problem_of(synth.Problem(8192, 8192, 256, 1))).describe()["grid"] // 2
     inp = synth.workload(2, M=256 * (2 * G + 8) - 64, N=256, K=1024)
     p = inp.problem
+    monkeypatch.setenv("BSG_KSPLIT_MIN_STAGES", "2")  # K halves at 8 K stages
     monkeypatch.setenv("BSG_WAIT_LIMIT_NS", "2000")
     op = bsg.GemmAmax(problem_of(p))
     monkeypatch.delenv("BSG_WAIT_LIMIT_NS")

@@ -28,6 +28,16 @@ def P(M, N, K, L=1, a="e4m3", b="e4m3", c="f32", major="n", am="k", bm="k"):
     return synth.Problem(M, N, K, L, a, b, 32, c, major, "ue8m0", am, bm)
 
 
+@pytest.fixture(scope="module", autouse=True)
+def _k_halves_from_two_stages():
+    """Plans made in this file take K halves from 2 K stages on (the default
+    threshold, 40, would need far larger test problems)."""
+    mp = pytest.MonkeyPatch()
+    mp.setenv("BSG_KSPLIT_MIN_STAGES", "2")
+    yield
+    mp.undo()
+
+
 @pytest.fixture(scope="module")
 def G():
     """Resident 256-wide FP8 pairs: a full-wave problem's grid / 2."""
@@ -142,6 +152,16 @@ def test_small_workspace_runs_half_width(G):
             assert bsg.bsg_check_device_status(op.plan, ws.data_ptr(), s) == bsg.BSG_OK
         x = C.float().cpu().numpy().astype(np.float64)
         ref = assert_parity(inp, x, float(amax.item()), ref=ref)
+
+
+def test_default_threshold_is_forty_k_stages(G, monkeypatch):
+    """Without the environment setting, a plan takes K halves only from 40
+    K stages (5120 FP8 bytes per row) on."""
+    monkeypatch.delenv("BSG_KSPLIT_MIN_STAGES")
+    short = with_tiles(G, 10, 256, 39 * 128)[0]
+    long_ = with_tiles(G, 10, 256, 40 * 128)[0]
+    assert bsg.GemmAmax(problem_of(short)).describe()["k_split_tiles"] == 0
+    assert bsg.GemmAmax(problem_of(long_)).describe()["k_split_tiles"] > 0
 
 
 @pytest.mark.parametrize("name,prob,hints", [
